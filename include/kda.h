@@ -1,0 +1,231 @@
+/*
+ * kda.h -- C ABI of libkda: the KDA (Kimi Delta Attention) layer step on one
+ * GB300 (sm_103a).
+ *
+ * The layer step, per sequence and per head h, for each token t:
+ *   conv   y = silu(sum_{j<4} w[c][j] * x_{t-3+j}[c]) on every raw q, k, v
+ *          channel c (depthwise causal conv of width 4, last tap on the
+ *          current token, no bias; the 3 previous raw inputs are the slot's
+ *          "conv tail")
+ *   L2     q <- q / sqrt(|q|^2 + eps_l2), k <- k / sqrt(|k|^2 + eps_l2)
+ *   update S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *   read   o_t = S_t^T q_t
+ *   norm   y_t = w_n * o_t / sqrt(mean(o_t^2) + eps_rms) * sigmoid(g_t)
+ * Sources: "vLLM Kimi K3 지원" (agentlenshq.com), section "Kimi K3 아키텍처 개요"
+ * (KDA: linear attention over a fixed-size recurrent state) and section
+ * "Fused Kernels 및 메타데이터 최적화" (the decode step fuses causal conv,
+ * recurrent update and RMSNorm in one launch; prefill runs chunked).  The
+ * pages do not print the recurrence; the formula above is the KDA step this
+ * library implements.
+ *
+ * Conventions shared by every entry point
+ *   - Device memory is owned by the caller: the pool buffer, inputs, outputs
+ *     and workspaces are plain device pointers.  The library allocates no
+ *     device memory.  A pool handle owns host metadata only.
+ *   - Calls that take a stream are asynchronous on that stream.  A host-side
+ *     argument error returns a status synchronously and enqueues nothing.
+ *   - A fault found on the device (a slot index out of range) sets a bit of
+ *     the pool's device error word and the affected item is skipped; read it
+ *     with kda_poll_device_error.  No kernel traps.
+ *   - Not thread-safe per pool unless the callers order their streams.
+ *   - Activations, conv weights, norm weight and the conv tail share one
+ *     dtype (pool "act": fp32 or bf16).  State is always fp32.
+ *
+ * Pool layout (one caller buffer of kda_state_pool_bytes bytes, 256-aligned):
+ *   [0, 256)             header; the uint32 device error word at offset 0
+ *   states               [num_slots][H][d_v][d_k] fp32: each head's state
+ *                        stored transposed, S^T, row j = value channel j,
+ *                        d_k key channels contiguous
+ *   tails (256-aligned)  [num_slots][3][n_ch] act, n_ch = H*(2*d_k + d_v):
+ *                        the 3 previous raw inputs, oldest first; channels
+ *                        q (h*d_k+i), then k (H*d_k+h*d_k+i), then
+ *                        v (2*H*d_k+h*d_v+j)
+ *   A slot that holds zeros is the state of a new sequence.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA stream type (same object as cudaStream_t). */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad shape, bad dtype */
+    KDA_ERR_SLOT_RANGE = 2,  /* a host-visible slot index outside [0, num_slots) */
+    KDA_ERR_ALIAS = 3,       /* the same slot written twice, or read and written by different items */
+    KDA_ERR_UNSUPPORTED = 4, /* a legal shape this build has no kernel for */
+    KDA_ERR_CUDA = 5,        /* a CUDA runtime call failed */
+    KDA_ERR_DEVICE = 6,      /* the device error word was set (kda_poll_device_error) */
+    KDA_ERR_WORKSPACE = 7    /* workspace missing, misaligned or too small */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Device error word bits. */
+#define KDA_DEVERR_SLOT_RANGE 0x1u /* a device-side slot index was out of range */
+#define KDA_DEVERR_META 0x2u       /* prefill metadata inconsistent on the device */
+#define KDA_DEVERR_TIMEOUT 0x4u    /* a bounded wait inside a kernel gave up */
+
+typedef struct {
+    int32_t num_slots;  /* > 0 */
+    int32_t num_heads;  /* H > 0 */
+    int32_t d_k;        /* key channels per head */
+    int32_t d_v;        /* value channels per head */
+    int32_t conv_width; /* must be 4 */
+    int32_t act;        /* kda_dtype of activations, weights and conv tail */
+} kda_pool_desc;
+
+typedef struct {
+    size_t header_offset; /* error word at this byte offset */
+    size_t state_offset;  /* byte offset of slot 0's state */
+    size_t state_slot_bytes;
+    size_t tail_offset;   /* byte offset of slot 0's conv tail */
+    size_t tail_slot_bytes;
+    size_t total_bytes;
+} kda_pool_layout;
+
+/* Layer weights (device pointers, act dtype). */
+typedef struct {
+    const void *conv_w; /* [n_ch][4]: row c holds channel c's taps, tap 3 on the current token */
+    const void *norm_w; /* [d_v], shared by all heads */
+    float eps_l2;       /* added under the root of the q/k L2 norm (1e-6) */
+    float eps_rms;      /* added under the root of the RMSNorm (1e-5) */
+} kda_weights;
+
+/* Per-token tensors (device pointers, act dtype), token-major.  For decode a
+ * token is a sequence of the batch; for verify token (b, t) is row b*T + t;
+ * for prefill the sequences are packed back to back (cu_seqlens). */
+typedef struct {
+    const void *q;     /* [n_tok][H][d_k] raw projections (before the conv) */
+    const void *k;     /* [n_tok][H][d_k] */
+    const void *v;     /* [n_tok][H][d_v] */
+    const void *alpha; /* [n_tok][H][d_k] decay values in (0, 1] */
+    const void *beta;  /* [n_tok][H] write strengths in [0, 1] */
+    const void *gate;  /* [n_tok][H][d_v] output-gate logits */
+    void *out;         /* [n_tok][H][d_v] gated, normalised output */
+} kda_io;
+
+/* A state checkpoint taken inside a prefill: after the first token_pos tokens
+ * of sequence seq's segment, copy its state and conv tail into dst_slot.
+ * token_pos is > 0 and either a multiple of the chunk size or the segment
+ * length. */
+typedef struct {
+    int32_t seq;
+    int32_t token_pos;
+    int32_t dst_slot;
+} kda_ckpt_req;
+
+typedef struct kda_pool kda_pool;
+
+/* Bytes a pool with this description needs; 0 if the description is invalid.
+ * Source: "vLLM Kimi K3 지원", section "하이브리드 KV-Cache 관리" (compact KDA
+ * recurrent-state blocks next to the paged KV blocks) and the DSpark page's
+ * FP32 state cache ("Kimi K3 ... 842 tok/s", section "시간은 어디에 쓰였나"). */
+KDA_API size_t kda_state_pool_bytes(const kda_pool_desc *desc);
+
+/* Wraps a caller-owned device buffer (>= kda_state_pool_bytes, 256-aligned)
+ * as a slot pool.  Does not clear it: the caller zeroes the buffer (or the
+ * slots it hands to new sequences).  On success *out owns host metadata only;
+ * free it with kda_state_pool_destroy.  Errors: KDA_ERR_INVALID_ARG,
+ * KDA_ERR_UNSUPPORTED (dims without a kernel), KDA_ERR_CUDA. */
+KDA_API kda_status kda_state_pool_create(const kda_pool_desc *desc, void *dev_buf, size_t bytes,
+                                 kda_pool **out);
+
+/* Frees the handle (not the caller's buffer).  NULL is ignored. */
+KDA_API void kda_state_pool_destroy(kda_pool *pool);
+
+/* Byte offsets of the pool regions (see the layout above). */
+KDA_API kda_status kda_state_pool_layout(const kda_pool *pool, kda_pool_layout *out);
+
+/* Host-side validation of slot tables before they are used on the device.
+ * in_slots [n_in] and out_slots [n_out] are HOST arrays (either may be NULL
+ * with its count 0).  Fails with KDA_ERR_SLOT_RANGE if an index is outside
+ * [0, num_slots), with KDA_ERR_ALIAS if out_slots repeats a slot, if in_slots
+ * repeats a slot, or if out slot i*per_item + t equals an in slot other than
+ * in_slots[i] (per_item = n_out / n_in when n_in > 0).  Enqueues nothing. */
+KDA_API kda_status kda_check_slots(const kda_pool *pool, const int32_t *in_slots, int32_t n_in,
+                           const int32_t *out_slots, int32_t n_out);
+
+/* One decode step for a batch of B sequences: token b of io advances the
+ * state and conv tail of slot slots[b] in place and writes out[b].  slots is a
+ * DEVICE array [B] (so the call can sit in a CUDA graph); an index outside the
+ * pool sets KDA_DEVERR_SLOT_RANGE and that sequence is skipped.  Slots must be
+ * distinct (check with kda_check_slots).  B = 0 is a no-op.
+ * One launch: conv, L2, update, readout and gated norm are fused.
+ * Source: "vLLM Kimi K3 지원", section "Fused Kernels 및 메타데이터 최적화",
+ * KDA Decode bullet. */
+KDA_API kda_status kda_decode(kda_pool *pool, const kda_weights *w, const kda_io *io,
+                      const int32_t *slots, int32_t B, kda_stream_t stream);
+
+/* Speculative verify: B sequences each advance T draft tokens (1 <= T <= 16)
+ * in one launch.  Token (b, t) is io row b*T + t.  Sequence b starts from slot
+ * in_slots[b] (DEVICE [B]); after its token t the state and conv tail are
+ * written to slot snap_slots[b*T + t] (DEVICE [B*T]) and the output to row
+ * b*T + t.  in_slots[b] is read before any write, so it may equal any of its
+ * own snapshot slots.  Rollback to an accepted length a (1 <= a <= T) is the
+ * caller adopting snap_slots[b*T + a - 1]: no device work.  Snapshot slots
+ * must be distinct and must not be another sequence's in slot.
+ * Source: "vLLM Kimi K3 지원", section "DSpark를 이용한 Speculative Decoding", and
+ * "vLLM Kimi-K3 DSpark 사전 해석 구현", section "추론 성능 및 기능" (8 draft
+ * tokens per step). */
+KDA_API kda_status kda_verify(kda_pool *pool, const kda_weights *w, const kda_io *io,
+                      const int32_t *in_slots, const int32_t *snap_slots, int32_t B, int32_t T,
+                      kda_stream_t stream);
+
+/* Workspace bytes kda_prefill_chunked needs for these sequence lengths
+ * (cu_seqlens: HOST [N+1], nondecreasing from 0).  0 on invalid input. */
+KDA_API size_t kda_prefill_workspace_bytes(const kda_pool *pool, const int32_t *cu_seqlens, int32_t N,
+                                   int32_t chunk);
+
+/* Chunked prefill of N packed sequences.  Sequence n owns io rows
+ * [cu_seqlens[n], cu_seqlens[n+1]) and slot slots[n]; it starts from that
+ * slot's state and tail when has_initial_state[n] != 0, else from zeros, and
+ * leaves its end state and tail in the slot.  Chunks of `chunk` tokens (64)
+ * are aligned to each segment's first token.  reqs[n_reqs] asks for state
+ * checkpoints (see kda_ckpt_req); the destinations must be distinct, must
+ * not be a slot of this call, and a sequence's end may be checkpointed too.
+ * cu_seqlens, slots, has_initial_state and reqs are HOST arrays (checked
+ * here: KDA_ERR_SLOT_RANGE, KDA_ERR_ALIAS, KDA_ERR_INVALID_ARG).
+ * workspace: device, 256-aligned, >= kda_prefill_workspace_bytes.
+ * Source: "vLLM Kimi K3 지원", section "Fused Kernels 및 메타데이터 최적화",
+ * KDA Prefill bullet (FlashKDA), and section "에이전틱 캐시 유지 정책"
+ * (interval-based retention: checkpoints every 32K tokens and at prompt
+ * boundaries). */
+KDA_API kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, const kda_io *io,
+                               const int32_t *cu_seqlens, const int32_t *slots,
+                               const uint8_t *has_initial_state, int32_t N, int32_t chunk,
+                               const kda_ckpt_req *reqs, int32_t n_reqs, void *workspace,
+                               size_t workspace_bytes, kda_stream_t stream);
+
+/* Copies state and conv tail of src_slots[i] into dst_slots[i], bit-exact,
+ * for i < n (HOST arrays).  Restoring a checkpoint is the same call with the
+ * roles swapped.  dst slots must be distinct and must not appear among the
+ * sources.  Source: "vLLM Kimi K3 지원", section "에이전틱 캐시 유지 정책". */
+KDA_API kda_status kda_state_checkpoint(kda_pool *pool, const int32_t *src_slots,
+                                const int32_t *dst_slots, int32_t n, kda_stream_t stream);
+
+/* Waits for `stream`, reads the device error word into *flags (may be NULL)
+ * and clears it.  Returns KDA_ERR_DEVICE if any bit was set, else KDA_OK. */
+KDA_API kda_status kda_poll_device_error(kda_pool *pool, kda_stream_t stream, uint32_t *flags);
+
+/* Static text for a status code. */
+KDA_API const char *kda_status_string(kda_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,53 @@
+"""Shared test helpers: tolerance metric, conversions between the GPU pool's
+layout and the oracle's, and a mirrored GPU/oracle pool driver."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Tolerances (max relative error per block, see block_rel_err).
+STATE_TOL = 1e-4      # fp32 state
+OUT_TOL_BF16 = 2e-2   # bf16 outputs
+OUT_TOL_F32 = 1e-4    # fp32 outputs (tiny fp32 workload)
+
+
+def block_rel_err(x, ref, block_dims: int) -> float:
+    """max over blocks of max|x - ref| / max|ref|, a block being the trailing
+    ``block_dims`` axes (one (token, head) output row, or one (slot, head)
+    state matrix)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert x.shape == ref.shape, (x.shape, ref.shape)
+    if x.size == 0:
+        return 0.0
+    axes = tuple(range(x.ndim - block_dims, x.ndim))
+    num = np.max(np.abs(x - ref), axis=axes)
+    den = np.max(np.abs(ref), axis=axes)
+    den = np.where(den == 0.0, 1.0, den)
+    return float(np.max(num / den))
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def oracle_inputs(inp: dict) -> dict:
+    return {k: f64(v) for k, v in inp.items()}
+
+
+def oracle_weights(w: dict) -> dict:
+    return {k: f64(v) for k, v in w.items()}
+
+
+def gpu_state_as_oracle(states_slot: torch.Tensor) -> np.ndarray:
+    """GPU slot state [H][d_v][d_k] (S^T) -> oracle S [H][d_k][d_v]."""
+    return f64(states_slot).transpose(0, 2, 1)
+
+
+def to_device(inp: dict, device="cuda") -> dict:
+    return {k: v.to(device).contiguous() for k, v in inp.items()}
+
+
+def out_tol(act: torch.dtype) -> float:
+    return OUT_TOL_BF16 if act == torch.bfloat16 else OUT_TOL_F32

@@ -1,0 +1,74 @@
+"""A GPU slot pool and an oracle slot pool driven through the same calls.
+
+Each method runs one library entry point on the GPU pool and the matching
+oracle computation on the float64 pool, and returns both outputs.  Only the
+seeded inputs are shared; the oracle never reads anything the GPU produced.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from hybrid_linear_attention_03_gb300 import kda
+from oracle import kda_oracle as ko
+
+import helpers as hp
+
+
+class Mirror:
+    def __init__(self, num_slots, H, D, act, weights: dict, eps_l2=1e-6, eps_rms=1e-5):
+        self.H, self.D, self.act = H, D, act
+        self.gpu = kda.StatePool(num_slots, H, D, D, act)
+        self.w_dev = hp.to_device(weights)
+        self.w = kda.make_weights(self.w_dev["conv_w"], self.w_dev["norm_w"], eps_l2, eps_rms)
+        self.ora = ko.OraclePool(H, D, D, 4, eps_l2, eps_rms)
+        self.w_ora = hp.oracle_weights(weights)
+
+    # -- entry points ---------------------------------------------------------
+    def decode(self, slots, inp, stream=None):
+        B = len(slots)
+        dev = hp.to_device(inp)
+        out = torch.empty(B, self.H, self.D, dtype=self.act, device="cuda")
+        sl = torch.tensor(slots, dtype=torch.int32, device="cuda")
+        kda.kda_decode(self.gpu, self.w, kda.make_io(dev, out), sl, B, stream)
+        ref = np.zeros((B, self.H, self.D))
+        oi = hp.oracle_inputs(inp)
+        for b, s in enumerate(slots):
+            tok = {k: v[b:b + 1] for k, v in oi.items()}
+            ref[b] = self.ora.run(int(s), tok, self.w_ora)[0]
+        return out, ref
+
+    def verify(self, in_slots, snap_slots, T, inp, stream=None):
+        """snap_slots: [B][T]; inp rows b*T + t."""
+        B = len(in_slots)
+        dev = hp.to_device(inp)
+        out = torch.empty(B * T, self.H, self.D, dtype=self.act, device="cuda")
+        si = torch.tensor(in_slots, dtype=torch.int32, device="cuda")
+        ss = torch.tensor(np.asarray(snap_slots).reshape(-1), dtype=torch.int32, device="cuda")
+        kda.kda_verify(self.gpu, self.w, kda.make_io(dev, out), si, ss, B, T, stream)
+        ref = np.zeros((B * T, self.H, self.D))
+        oi = hp.oracle_inputs(inp)
+        starts = [self.ora.get(int(s)) for s in in_slots]
+        for b in range(B):
+            tok = {k: v[b * T:(b + 1) * T] for k, v in oi.items()}
+            S0, t0 = starts[b]
+            o, _, _, hs, ht = self.ora.o.layer(tok, self.w_ora, S0, t0, want_hist=True,
+                                               eps_l2=self.ora.eps_l2, eps_rms=self.ora.eps_rms)
+            ref[b * T:(b + 1) * T] = o
+            for t in range(T):
+                self.ora.put(int(snap_slots[b][t]), hs[t], ht[t])
+        return out, ref
+
+    def checkpoint(self, src, dst):
+        kda.kda_state_checkpoint(self.gpu, src, dst)
+        self.ora.checkpoint(src, dst)
+
+    # -- comparisons ------------------------------------------------------------
+    def state_err(self, slot) -> float:
+        g = hp.gpu_state_as_oracle(self.gpu.states()[slot])
+        return hp.block_rel_err(g, self.ora.get(int(slot))[0], 2)
+
+    def tail_equal(self, slot) -> bool:
+        g = hp.f64(self.gpu.tails()[slot])
+        return bool(np.array_equal(g, self.ora.get(int(slot))[1]))

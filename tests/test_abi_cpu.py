@@ -1,0 +1,66 @@
+"""CPU-side checks of the C ABI: the library loads and exports every symbol
+include/kda.h declares; host arithmetic and status text need no GPU."""
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+from hybrid_linear_attention_03_gb300 import build as kbuild
+from hybrid_linear_attention_03_gb300 import kda
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "kda.h"
+
+
+def declared_symbols():
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"KDA_API\s+[^;(]*?\b(kda_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.lib()
+
+
+def test_header_declares_the_bound_entry_points():
+    assert declared_symbols() == sorted(kda.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(str(kda.lib_path()))
+    for name in declared_symbols():
+        assert hasattr(raw, name), f"libkda.so does not export {name}"
+
+
+def test_pool_bytes_layout_arithmetic(lib):
+    # H=64, d=128, bf16: 4 MiB state + 3*64*384*2 B tail per slot, 256 B header, 256-aligned regions
+    desc = kda.make_desc(256, 64, 128, 128, kda.torch.bfloat16)
+    state = 256 * 64 * 128 * 128 * 4
+    tail_off = (256 + state + 255) // 256 * 256
+    total = (tail_off + 256 * 3 * 64 * 384 * 2 + 255) // 256 * 256
+    assert kda.kda_state_pool_bytes(desc) == total
+
+
+@pytest.mark.parametrize("bad", [dict(num_slots=0), dict(num_heads=0), dict(d_k=-1), dict(conv_width=3),
+                                 dict(act=7)])
+def test_pool_bytes_rejects_bad_descriptions(lib, bad):
+    fields = dict(num_slots=4, num_heads=2, d_k=16, d_v=16, conv_width=4, act=kda.KDA_F32)
+    fields.update(bad)
+    desc = kda.kda_pool_desc(**fields)
+    assert kda.kda_state_pool_bytes(desc) == 0
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = kda.kda_status_string(code)
+        assert s and s != "unknown status"
+    assert kda.kda_status_string(99) == "unknown status"
+
+
+def test_create_rejects_null_buffer(lib):
+    desc = kda.make_desc(4, 2, 16, 16, kda.torch.float32)
+    h = ctypes.c_void_p()
+    st = lib.kda_state_pool_create(ctypes.byref(desc), None, 1 << 20, ctypes.byref(h))
+    assert st == kda.KDA_ERR_INVALID_ARG and not h.value
