@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA layer step on GB300.
+
+Headline workload (one bench step): KDA decode at batch 1, H = 64 heads,
+d_k = d_v = 128, bf16 activations, fp32 state in a 256-slot pool, the state
+warmed by 512 prior tokens; one step is 1000 chained decode launches
+replayed from a CUDA graph.  value = decoded tokens / second.
+
+Beside it the same JSON line carries the HBM roofline of the step kernel at
+batch 64 (decode, and verify with T = 8 drafts) and the chunked prefill of
+one 32768-token sequence; the CPU oracle is timed on the host cores as the
+baseline.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torchrun; each rank runs an independent replica
+(the layer step has no exchange between sequences), and value sums them.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from hybrid_linear_attention_03_gb300 import inputs as I  # noqa: E402
+
+METRIC = "KDA decode tok/s (batch 1, H=64, d=128, 1000 chained steps)"
+UNIT = "tok/s"
+STEP_KERNEL = "kda_step_kernel"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def args_():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
+    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "prefill"], default=None,
+                    help="run one secondary case alone (for profiling) and print its numbers")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [int(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": float(statistics.median(sm)), "sm_max_mhz": float(max(int(r[2]) for r in rows)),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def step_bytes(H, D, B, T, act_bytes=2):
+    """Algorithmic HBM bytes of one step-kernel launch: each sequence reads
+    its state and conv tail once and writes them T times (decode: in place),
+    reads its T tokens' q, k, v, alpha, gate, beta, writes T outputs; conv
+    weights and the norm weight are read once per launch."""
+    state = H * D * D * 4
+    tail = 3 * H * 3 * D * act_bytes
+    io_tok = H * D * act_bytes * 5 + H * act_bytes + H * D * act_bytes
+    weights = H * 3 * D * 4 * act_bytes + D * act_bytes
+    return B * (state * (1 + T) + tail * (1 + T) + io_tok * T) + weights
+
+
+# --------------------------------------------------------------------------- ours
+
+def run_ours(a, rank, world, local):
+    from hybrid_linear_attention_03_gb300 import build as kbuild
+    from hybrid_linear_attention_03_gb300 import kda
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, tf_peak, _, peak_kind = load_peaks()
+    if a.only:
+        kbuild.build()
+        if a.only == "prefill":
+            res = prefill_case(kda, dev, iters=a.steps, warmup=a.warmup)
+        else:
+            res = secondary(kda, dev, hbm_peak, peak_kind, only=a.only, iters=a.steps)
+        print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    kbuild.build()
+    kda.lib()
+    wl = I.DECODE_B1
+    H, D, act, n_steps = wl.H, wl.dk, wl.act, wl.extra["steps"]
+
+    w_cpu = wl.weights()
+    w_dev = {k: v.to(dev) for k, v in w_cpu.items()}
+    w = kda.make_weights(w_dev["conv_w"], w_dev["norm_w"], wl.eps_l2, wl.eps_rms)
+    pool = kda.StatePool(wl.num_slots, H, D, D, act)
+    slot = int(I.integers(wl.seed, 0, 0, wl.num_slots - 1, 1)[0])
+    spare = (slot + 1) % wl.num_slots
+    slot_t = torch.tensor([slot], dtype=torch.int32, device=dev)
+    # warm the slot with 512 tokens (16 drafts per verify launch, the last one in place)
+    warm = {k: v.to(dev) for k, v in wl.tokens(0, wl.extra["warm"]).items()}
+    wout = torch.empty(16, H, D, dtype=act, device=dev)
+    table = [s for s in range(wl.num_slots) if s not in (slot, spare)][:15] + [slot]
+    snaps = torch.tensor(table, dtype=torch.int32, device=dev)
+    for c in range(wl.extra["warm"] // 16):
+        part = {k: v[c * 16:(c + 1) * 16] for k, v in warm.items()}
+        kda.kda_verify(pool, w, kda.make_io(part, wout), slot_t, snaps, 1, 16)
+    kda.kda_state_checkpoint(pool, [slot], [spare])  # the warm state, restored before every step
+    torch.cuda.synchronize()
+
+    toks = {k: v.to(dev) for k, v in wl.tokens(100, n_steps).items()}
+    out = torch.empty(n_steps, H, D, dtype=act, device=dev)
+    ios = [kda.make_io({k: v[i:i + 1] for k, v in toks.items()}, out[i:i + 1]) for i in range(n_steps)]
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(3):  # first launches set kernel attributes, outside the capture
+            kda.kda_decode(pool, w, ios[i], slot_t, 1)
+        kda.kda_state_checkpoint(pool, [spare], [slot])
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(n_steps):
+            kda.kda_decode(pool, w, ios[i], slot_t, 1)
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            kda.kda_state_checkpoint(pool, [spare], [slot])
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            graph.replay()
+            e.record(stream)
+        return s, e
+
+    for _ in range(a.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    st, flags = kda.kda_poll_device_error(pool, stream)
+    assert st == 0, f"device error word {flags:#x}"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [one_step() for _ in range(a.steps)]
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = sum(s.elapsed_time(e) for s, e in evs)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    value = a.steps * n_steps * world / (ms / 1e3)
+    bytes_b1 = step_bytes(H, D, 1, 1)
+    launch_us = ms * 1e3 / (a.steps * n_steps)
+    achieved = bytes_b1 / (launch_us * 1e-6) / 1e9
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs,
+    # 1000 decodes, D2H of the outputs, all inside the timed region
+    host_in = {k: v.pin_memory() for k, v in wl.tokens(100, n_steps).items()}
+    host_out = torch.empty(n_steps, H, D, dtype=act).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            kda.kda_state_checkpoint(pool, [spare], [slot])
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            for k, v in host_in.items():
+                toks[k].copy_(v, non_blocking=True)
+            graph.replay()
+            host_out.copy_(out, non_blocking=True)
+            e.record(stream)
+        return s, e
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    evs2 = [e2e_step() for _ in range(a.steps)]
+    torch.cuda.synchronize()
+    ms2 = sum(s.elapsed_time(e) for s, e in evs2)
+    e2e_value = a.steps * n_steps * world / (ms2 / 1e3)
+    clk = clocks.stop()
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy, value recipe of the workload)",
+        "config": {"workload": wl.name, "batch": 1, "heads": H, "d_k": D, "d_v": D, "io_dtype": "bf16",
+                   "state_dtype": "f32", "pool_slots": wl.num_slots, "warm_tokens": wl.extra["warm"],
+                   "decode_steps_per_bench_step": n_steps, "cuda_graph": True,
+                   "l2": "flushed (512 MiB write) between timed steps; within a step the 4 MiB state of the "
+                         "single sequence stays L2-resident across its 1000 chained decodes",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": a.steps * n_steps,
+        "roofline": {"bound": "hbm", "kernel": STEP_KERNEL, "achieved": round(achieved, 1), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "bytes_per_launch": bytes_b1, "launch_us": round(launch_us, 3),
+                     "note": f"peak = {peak_kind} HBM copy bandwidth; at batch 1 the state stays in L2 and the "
+                             "launch is latency-bound; the HBM rooflines of this kernel are the batch-64 entries "
+                             "under secondary"},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clk,
+    }
+    if not a.no_secondary:
+        sec = secondary(kda, dev, hbm_peak, peak_kind)
+        try:
+            sec["prefill"] = prefill_case(kda, dev, iters=3, warmup=1)
+        except Exception as e:  # reported, not hidden: the line says why prefill is absent
+            sec["prefill"] = {"error": f"{type(e).__name__}: {e}"}
+        line["secondary"] = sec
+    if rank == 0:
+        if not a.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(sample_tokens=n_steps)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
+    """Batch-64 rooflines of the step kernel: decode (T = 1) and verify (T = 8)."""
+    res = {}
+    wl = I.VERIFY_B64
+    H, D, act, B = wl.H, wl.dk, wl.act, wl.extra["B"]
+    w_dev = {k: v.to(dev) for k, v in wl.weights().items()}
+    w = kda.make_weights(w_dev["conv_w"], w_dev["norm_w"], wl.eps_l2, wl.eps_rms)
+    pool = kda.StatePool(wl.num_slots, H, D, D, act)
+    pool.states().normal_(0.0, 0.02)
+    perm = torch.from_numpy(I.permutation(wl.seed, 0, wl.num_slots)).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for name, T in (("decode_b64", 1), ("verify_b64_t8", 8)):
+        if only is not None and name != only:
+            continue
+        toks = {k: v.to(dev) for k, v in wl.tokens(200, B * T).items()}
+        out = torch.empty(B * T, H, D, dtype=act, device=dev)
+        io = kda.make_io(toks, out)
+        snap = perm[:B * T].contiguous()
+        ins = snap.view(B, T)[:, 0].contiguous()
+
+        def launch():
+            if T == 1:
+                kda.kda_decode(pool, w, io, ins, B)
+            else:
+                kda.kda_verify(pool, w, io, ins, snap, B, T)
+
+        for _ in range(3):
+            launch()
+        times = []
+        for _ in range(iters):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            launch()
+            e.record(stream)
+            e.synchronize()
+            times.append(s.elapsed_time(e) * 1e3)
+        us = float(np.mean(times))
+        byts = step_bytes(H, D, B, T)
+        ach = byts / (us * 1e-6) / 1e9
+        res[name] = {"tok_per_s": round(B * T / (us * 1e-6), 1), "launch_us": round(us, 2),
+                     "gpu_launches": iters,
+                     "roofline": {"bound": "hbm", "kernel": STEP_KERNEL, "achieved": round(ach, 1),
+                                  "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
+                                  "traffic": None, "bytes_per_launch": byts, "peak_kind": peak_kind},
+                     "l2": "flushed before every timed launch"}
+    st, flags = kda.kda_poll_device_error(pool)
+    assert st == 0, f"device error word {flags:#x}"
+    return res
+
+
+def prefill_case(kda, dev, iters=3, warmup=1):
+    """Chunked prefill of one 32768-token sequence (H = 64, d = 128, C = 64,
+    alpha = sigmoid(N(3, 1))) from a zero slot; tok/s of the whole call."""
+    wl = I.PREFILL_32K
+    H, D, act, L = wl.H, wl.dk, wl.act, wl.extra["L"]
+    w_dev = {k: v.to(dev) for k, v in wl.weights().items()}
+    w = kda.make_weights(w_dev["conv_w"], w_dev["norm_w"], wl.eps_l2, wl.eps_rms)
+    pool = kda.StatePool(wl.num_slots, H, D, D, act)
+    toks = {k: v.to(dev) for k, v in wl.tokens(300, L).items()}
+    out = torch.empty(L, H, D, dtype=act, device=dev)
+    cu = [0, L]
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(pool, cu), dtype=torch.uint8, device=dev)
+    io = kda.make_io(toks, out)
+    stream = torch.cuda.current_stream()
+
+    def launch():
+        kda.kda_prefill_chunked(pool, w, io, cu, [0], [0], 64, (), ws)
+
+    for _ in range(warmup):
+        launch()
+    times = []
+    for _ in range(iters):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        launch()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    ms = float(np.mean(times))
+    st, flags = kda.kda_poll_device_error(pool)
+    assert st == 0, f"device error word {flags:#x}"
+    return {"workload": wl.name, "tok_per_s": round(L / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
+            "workspace_bytes": ws.numel(),
+            "l2": "inputs (3.2 GB) and workspace exceed L2; not flushed between calls"}
+
+
+# ----------------------------------------------------------------------- oracle
+
+def oracle_decode_run(o, wl, w, tok, n):
+    """The CPU oracle over n chained decode tokens of the batch-1 sequence."""
+    S = np.zeros((wl.H, wl.dk, wl.dv))
+    tail = np.zeros((3, wl.H * (2 * wl.dk + wl.dv)))
+    part = {k: v[:n] for k, v in tok.items()}
+    t0 = time.perf_counter()
+    o.layer(part, w, S, tail, eps_l2=wl.eps_l2, eps_rms=wl.eps_rms)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(sample_tokens=1000, min_s=10.0, max_s=30.0):
+    from oracle import kda_oracle as ko
+
+    o = ko.Oracle(ko.build())
+    wl = I.DECODE_B1
+    w = {k: v.double().numpy() for k, v in wl.weights().items()}
+    tok = {k: v.double().numpy() for k, v in wl.tokens(100, sample_tokens).items()}
+    total, n, runs = 0.0, 0, 0
+    while total < min_s and runs < 100:
+        total += oracle_decode_run(o, wl, w, tok, sample_tokens)
+        n += sample_tokens
+        runs += 1
+        if total > max_s:
+            break
+    return {"value": round(n / total, 2), "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
+            "sample": f"{runs} x {sample_tokens} chained decode tokens of the batch-1 workload "
+                      f"(float64 token loop, OpenMP over the 64 heads)"}
+
+
+def run_reference(a, rank, world):
+    if rank != 0:
+        return
+    from oracle import kda_oracle as ko
+
+    o = ko.Oracle(ko.build())
+    wl = I.DECODE_B1
+    n = wl.extra["steps"]
+    w = {k: v.double().numpy() for k, v in wl.weights().items()}
+    tok = {k: v.double().numpy() for k, v in wl.tokens(100, n).items()}
+    for _ in range(a.warmup):
+        oracle_decode_run(o, wl, w, tok, n)
+    total = sum(oracle_decode_run(o, wl, w, tok, n) for _ in range(a.steps))
+    value = a.steps * n / total
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": 1,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(total * 1e3 / a.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy, value recipe of the workload)",
+            "config": {"workload": wl.name, "batch": 1, "heads": wl.H, "d_k": wl.dk, "d_v": wl.dv,
+                       "decode_steps_per_bench_step": n},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
+                             "sample": f"{a.steps} x {n} chained decode tokens (the whole workload per step)"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    a = args_()
+    rank, world, local = dist_env()
+    if a.impl == "reference":
+        run_reference(a, rank, world)
+        return
+    run_ours(a, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

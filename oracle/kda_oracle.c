@@ -266,8 +266,7 @@ static void core_chunked(int L, int C, int dk, int dv, const double *q,
 static void set_threads(int n_threads)
 {
 #ifdef _OPENMP
-    if (n_threads > 0)
-        omp_set_num_threads(n_threads);
+    omp_set_num_threads(n_threads > 0 ? n_threads : omp_get_num_procs());
 #else
     (void)n_threads;
 #endif
