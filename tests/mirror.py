@@ -72,3 +72,37 @@ class Mirror:
     def tail_equal(self, slot) -> bool:
         g = hp.f64(self.gpu.tails()[slot])
         return bool(np.array_equal(g, self.ora.get(int(slot))[1]))
+
+
+def prefill_gpu(m: Mirror, inp_dev: dict, lens, slots, has_init, reqs=(), stream=None):
+    """Run kda_prefill_chunked on the mirror's GPU pool; returns the output."""
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    out = torch.empty(int(cu[-1]), m.H, m.D, dtype=m.act, device="cuda")
+    ws_bytes = kda.kda_prefill_workspace_bytes(m.gpu, cu)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    kda.kda_prefill_chunked(m.gpu, m.w, kda.make_io(inp_dev, out), cu, slots, has_init, 64, reqs, ws, stream)
+    return out
+
+
+def prefill_oracle(m: Mirror, inp: dict, lens, slots, has_init, reqs=()):
+    """The same prefill on the oracle pool: each sequence runs from its slot
+    (or from zeros), split at its checkpoint positions."""
+    oi = hp.oracle_inputs(inp)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    out = np.zeros((int(cu[-1]), m.H, m.D))
+    for n, (slot, init) in enumerate(zip(slots, has_init)):
+        a, b = int(cu[n]), int(cu[n + 1])
+        cuts = sorted({int(r[1]) for r in reqs if r[0] == n} | {b - a})
+        S, t = m.ora.get(int(slot)) if init else m.ora.zero()
+        pos = 0
+        for c in cuts:
+            if c > pos:
+                part = {k: v[a + pos:a + c] for k, v in oi.items()}
+                o, S, t, _, _ = m.ora.o.layer(part, m.w_ora, S, t, eps_l2=m.ora.eps_l2, eps_rms=m.ora.eps_rms)
+                out[a + pos:a + c] = o
+                pos = c
+            for r in reqs:
+                if r[0] == n and r[1] == c:
+                    m.ora.put(int(r[2]), S, t)
+        m.ora.put(int(slot), S, t)
+    return out

@@ -1,0 +1,140 @@
+"""GPU parity of the chunked prefill against the oracle (token loop), its
+checkpoints and resume, and decode after prefill."""
+
+from __future__ import annotations
+
+import pytest
+import torch
+
+from hybrid_linear_attention_03_gb300 import build as kbuild
+from hybrid_linear_attention_03_gb300 import inputs as I
+from hybrid_linear_attention_03_gb300 import kda
+
+import helpers as hp
+from mirror import Mirror, prefill_gpu, prefill_oracle
+
+pytestmark = pytest.mark.gpu
+D = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    kbuild.build()
+    kda.lib()
+
+
+def _check(m, out, ref, slots, reqs=()):
+    assert torch.isfinite(out.float()).all()
+    assert hp.block_rel_err(hp.f64(out), ref, 1) <= hp.out_tol(m.act)
+    for s in list(slots) + [r[2] for r in reqs]:
+        assert m.state_err(int(s)) <= hp.STATE_TOL, f"state of slot {s}"
+        assert m.tail_equal(int(s)), f"tail of slot {s}"
+
+
+@pytest.mark.parametrize("act", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_prefill_ragged_lengths_match_oracle(act):
+    """Lengths around the chunk size (1, 2, 3, 63, 64, 65, 130, 200), half of
+    them continuing a warmed slot, with checkpoints at chunk ends and ends."""
+    H = 2
+    lens = [1, 2, 3, 63, 64, 65, 130, 200]
+    N = len(lens)
+    m = Mirror(32, H, D, act, I.layer_weights(31, H, D, D, 4, act))
+    slots = list(range(N))
+    # warm the odd sequences' slots with a first prefill segment
+    warm_lens = [0 if n % 2 == 0 else 37 + n for n in range(N)]
+    warm = I.token_inputs(31, 0, sum(warm_lens), H, D, D, 2.0, act)
+    out = prefill_gpu(m, hp.to_device(warm), warm_lens, slots, [0] * N)
+    ref = prefill_oracle(m, warm, warm_lens, slots, [0] * N)
+    _check(m, out, ref, slots)
+    has_init = [n % 2 for n in range(N)]
+    reqs = [(5, 64, 20), (5, 65, 21), (6, 64, 22), (6, 128, 23), (7, 200, 24), (3, 63, 25), (0, 1, 26)]
+    inp = I.token_inputs(31, 1, sum(lens), H, D, D, 2.0, act)
+    out = prefill_gpu(m, hp.to_device(inp), lens, slots, has_init, reqs)
+    ref = prefill_oracle(m, inp, lens, slots, has_init, reqs)
+    _check(m, out, ref, slots, reqs)
+    assert kda.kda_poll_device_error(m.gpu) == (kda.KDA_OK, 0)
+
+
+def test_prefill_resume_from_checkpoint_is_bitexact():
+    """Prefill 320 tokens with a checkpoint at 192; restore it into a fresh
+    slot and prefill the last 128 tokens from there: outputs, end state and
+    tail equal the uninterrupted run bit for bit."""
+    H, act, L, cut = 3, torch.bfloat16, 320, 192
+    m = Mirror(8, H, D, act, I.layer_weights(41, H, D, D, 4, act))
+    inp = hp.to_device(I.token_inputs(41, 0, L, H, D, D, 3.0, act))
+    full = prefill_gpu(m, inp, [L], [0], [0], [(0, cut, 1)])
+    kda.kda_state_checkpoint(m.gpu, [1], [2])
+    rest = {k: v[cut:].contiguous() for k, v in inp.items()}
+    part = prefill_gpu(m, rest, [L - cut], [2], [1])
+    torch.cuda.synchronize()
+    assert torch.equal(part, full[cut:])
+    assert torch.equal(m.gpu.states()[2], m.gpu.states()[0])
+    assert torch.equal(m.gpu.tails()[2], m.gpu.tails()[0])
+
+
+def test_prefill_beta0_alpha1_keeps_state_bitexact():
+    H, act, L = 2, torch.float32, 100
+    m = Mirror(4, H, D, act, I.layer_weights(43, H, D, D, 4, act))
+    g = torch.Generator(device="cpu").manual_seed(3)
+    m.gpu.states()[1].copy_(torch.randn(H, D, D, generator=g))
+    before = m.gpu.states()[1].clone()
+    inp = I.token_inputs(43, 0, L, H, D, D, 2.0, act)
+    inp["beta"].zero_()
+    inp["alpha"].fill_(1.0)
+    prefill_gpu(m, hp.to_device(inp), [L], [1], [1])
+    torch.cuda.synchronize()
+    assert torch.equal(m.gpu.states()[1], before)
+
+
+def test_prefill_strong_decay_takes_exact_path():
+    """alpha ~ 0.05 (log-decay span ~190 per chunk, past the split-exponent
+    range): finite results that match the oracle."""
+    H, act, L = 2, torch.float32, 150
+    m = Mirror(4, H, D, act, I.layer_weights(47, H, D, D, 4, act))
+    inp = I.token_inputs(47, 0, L, H, D, D, 2.0, act)
+    inp["alpha"] = torch.full_like(inp["alpha"], 0.05)
+    out = prefill_gpu(m, hp.to_device(inp), [L], [0], [0])
+    ref = prefill_oracle(m, inp, [L], [0], [0])
+    _check(m, out, ref, [0])
+
+
+def test_decode_after_prefill_equals_one_long_run():
+    H, act = 4, torch.bfloat16
+    m = Mirror(4, H, D, act, I.layer_weights(53, H, D, D, 4, act))
+    inp = I.token_inputs(53, 0, 150, H, D, D, 2.0, act)
+    prefill_gpu(m, hp.to_device(inp), [150], [3], [0])
+    prefill_oracle(m, inp, [150], [3], [0])
+    for step in range(5):
+        o, r = m.decode([3], I.token_inputs(53, 10 + step, 1, H, D, D, 2.0, act))
+        assert hp.block_rel_err(hp.f64(o), r, 1) <= hp.OUT_TOL_BF16
+    assert m.state_err(3) <= hp.STATE_TOL and m.tail_equal(3)
+
+
+def test_prefill_host_errors():
+    H, act = 2, torch.bfloat16
+    m = Mirror(8, H, D, act, I.layer_weights(2, H, D, D, 4, act))
+    inp = hp.to_device(I.token_inputs(2, 0, 10, H, D, D, 2.0, act))
+    out = torch.empty(10, H, D, dtype=act, device="cuda")
+    io = kda.make_io(inp, out)
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(m.gpu, [0, 4, 10]), dtype=torch.uint8, device="cuda")
+    cases = [
+        (dict(cu=[0, 4, 10], slots=[1, 1], init=[0, 0]), kda.KDA_ERR_ALIAS),
+        (dict(cu=[0, 4, 10], slots=[1, 9], init=[0, 0]), kda.KDA_ERR_SLOT_RANGE),
+        (dict(cu=[0, 6, 4], slots=[1, 2], init=[0, 0]), kda.KDA_ERR_INVALID_ARG),
+        (dict(cu=[0, 4, 10], slots=[1, 2], init=[0, 0], reqs=[(0, 3, 5)]), kda.KDA_ERR_INVALID_ARG),
+        (dict(cu=[0, 4, 10], slots=[1, 2], init=[0, 0], reqs=[(1, 6, 2)]), kda.KDA_ERR_ALIAS),
+        (dict(cu=[0, 4, 10], slots=[1, 2], init=[0, 0], reqs=[(1, 6, 5), (0, 4, 5)]), kda.KDA_ERR_ALIAS),
+        (dict(cu=[0, 4, 10], slots=[1, 2], init=[0, 0], chunk=32), kda.KDA_ERR_UNSUPPORTED),
+    ]
+    for c, want in cases:
+        with pytest.raises(kda.KdaError) as e:
+            kda.kda_prefill_chunked(m.gpu, m.w, io, c["cu"], c["slots"], c["init"], c.get("chunk", 64),
+                                    c.get("reqs", ()), ws)
+        assert e.value.status == want, c
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_prefill_chunked(m.gpu, m.w, io, [0, 4, 10], [1, 2], [0, 0], 64, (), ws[:256])
+    assert e.value.status == kda.KDA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(m.gpu.states() == 0)
