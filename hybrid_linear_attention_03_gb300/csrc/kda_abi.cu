@@ -180,6 +180,48 @@ size_t kda_prefill_workspace_bytes(const kda_pool *pool, const int32_t *cu_seqle
     return kda::prefill_workspace_bytes(pool, cu_seqlens, N, chunk);
 }
 
+// Host checks shared by both prefill entry points.
+static kda_status check_prefill_args(kda_pool *pool, const kda_weights *w, const kda_io *io,
+                                     const int32_t *cu_seqlens, const int32_t *slots,
+                                     const uint8_t *has_initial_state, int32_t N, int32_t chunk,
+                                     const kda_ckpt_req *reqs, int32_t n_reqs) {
+    if (!pool || !valid_weights(w) || !valid_io(io) || N < 0 || n_reqs < 0 || (n_reqs > 0 && !reqs) ||
+        (N > 0 && (!cu_seqlens || !slots || !has_initial_state)))
+        return KDA_ERR_INVALID_ARG;
+    if (N == 0) return n_reqs == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (cu_seqlens[0] != 0) return KDA_ERR_INVALID_ARG;
+    for (int32_t n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return KDA_ERR_INVALID_ARG;
+    const int32_t ns = pool->desc.num_slots;
+    std::vector<uint8_t> used(size_t(ns), 0);
+    for (int32_t n = 0; n < N; ++n) {
+        if (slots[n] < 0 || slots[n] >= ns) return KDA_ERR_SLOT_RANGE;
+        if (used[slots[n]]) return KDA_ERR_ALIAS;
+        used[slots[n]] = 1;
+    }
+    for (int32_t r = 0; r < n_reqs; ++r) {
+        const kda_ckpt_req &q = reqs[r];
+        if (q.seq < 0 || q.seq >= N) return KDA_ERR_INVALID_ARG;
+        const int32_t len = cu_seqlens[q.seq + 1] - cu_seqlens[q.seq];
+        if (q.token_pos <= 0 || q.token_pos > len || (q.token_pos != len && chunk > 0 && q.token_pos % chunk != 0))
+            return KDA_ERR_INVALID_ARG;
+        if (q.dst_slot < 0 || q.dst_slot >= ns) return KDA_ERR_SLOT_RANGE;
+        if (used[q.dst_slot]) return KDA_ERR_ALIAS;
+        used[q.dst_slot] = 1;
+    }
+    return KDA_OK;
+}
+
+kda_status kda_prefill_chunked_noalloc(kda_pool *pool, const kda_weights *w, const kda_io *io,
+                                       const int32_t *cu_seqlens, const int32_t *slots,
+                                       const uint8_t *has_initial_state, int32_t N, int32_t chunk,
+                                       const kda_ckpt_req *reqs, int32_t n_reqs, kda_stream_t stream) {
+    const kda_status st = check_prefill_args(pool, w, io, cu_seqlens, slots, has_initial_state, N, chunk, reqs, n_reqs);
+    if (st != KDA_OK || N == 0) return st;
+    return kda::launch_prefill_noalloc(pool, w, io, cu_seqlens, slots, has_initial_state, N, chunk, reqs, n_reqs,
+                                       reinterpret_cast<cudaStream_t>(stream));
+}
+
 kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *cu_seqlens,
                                const int32_t *slots, const uint8_t *has_initial_state, int32_t N, int32_t chunk,
                                const kda_ckpt_req *reqs, int32_t n_reqs, void *workspace, size_t workspace_bytes,

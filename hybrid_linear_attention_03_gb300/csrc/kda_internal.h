@@ -65,5 +65,9 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
                           const uint8_t *has_initial_state, int N, int chunk,
                           const kda_ckpt_req *reqs, int n_reqs, void *workspace,
                           size_t workspace_bytes, cudaStream_t stream);
+kda_status launch_prefill_noalloc(const kda_pool *pool, const kda_weights *w, const kda_io *io,
+                                  const int32_t *cu_seqlens, const int32_t *slots,
+                                  const uint8_t *has_initial_state, int N, int chunk, const kda_ckpt_req *reqs,
+                                  int n_reqs, cudaStream_t stream);
 
 }  // namespace kda

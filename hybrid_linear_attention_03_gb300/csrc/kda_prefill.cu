@@ -27,6 +27,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <vector>
 
 namespace kda {
@@ -618,6 +619,43 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
     p.eps_rms = w->eps_rms;
     if (pool->desc.act == KDA_BF16) return launch_act<__nv_bfloat16>(p, N, n_chunks, n_reqs, stream);
     return launch_act<float>(p, N, n_chunks, n_reqs, stream);
+}
+
+// ------------------------------------------------------ no-allocation entry --
+// Fixed scratch for kda_prefill_chunked_noalloc: callers that cannot allocate
+// device memory run the prefill in this array instead of a workspace of
+// their own.  It lives in the module image, so every GPU that loads the
+// library holds it until the process exits.  Host code must not use the
+// array's name as a device address: the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+static __device__ __align__(256) unsigned char g_prefill_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
+
+kda_status launch_prefill_noalloc(const kda_pool *pool, const kda_weights *w, const kda_io *io,
+                                  const int32_t *cu_seqlens, const int32_t *slots,
+                                  const uint8_t *has_initial_state, int N, int chunk, const kda_ckpt_req *reqs,
+                                  int n_reqs, cudaStream_t stream) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void *scratch[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    void *ptr = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!scratch[dev]) {
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_prefill_noalloc_scratch) != cudaSuccess || !addr) {
+                cudaGetLastError();
+                return KDA_ERR_CUDA;
+            }
+            scratch[dev] = addr;
+        }
+        ptr = scratch[dev];
+    }
+    // Every byte of the scratch is written before it is read, so nothing is
+    // cleared; a call that needs more than the array returns KDA_ERR_WORKSPACE.
+    return launch_prefill(pool, w, io, cu_seqlens, slots, has_initial_state, N, chunk, reqs, n_reqs, ptr,
+                          KDA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 }  // namespace kda

@@ -34,7 +34,9 @@ KDA_DEVERR_TIMEOUT = 0x4
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_state_pool_bytes", "kda_state_pool_create", "kda_state_pool_destroy", "kda_state_pool_layout",
            "kda_check_slots", "kda_decode", "kda_verify", "kda_prefill_workspace_bytes", "kda_prefill_chunked",
-           "kda_state_checkpoint", "kda_poll_device_error", "kda_status_string")
+           "kda_state_checkpoint", "kda_poll_device_error", "kda_status_string", "kda_prefill_chunked_noalloc")
+
+KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class kda_pool_desc(ctypes.Structure):
@@ -100,6 +102,9 @@ def lib() -> ctypes.CDLL:
         L.kda_prefill_chunked.argtypes = [vp, P(kda_weights), P(kda_io), vp, vp, vp, i32, i32,
                                           P(kda_ckpt_req), i32, vp, sz, vp]
         L.kda_prefill_chunked.restype = i32
+        L.kda_prefill_chunked_noalloc.argtypes = [vp, P(kda_weights), P(kda_io), vp, vp, vp, i32, i32,
+                                                  P(kda_ckpt_req), i32, vp]
+        L.kda_prefill_chunked_noalloc.restype = i32
         L.kda_state_checkpoint.argtypes = [vp, vp, vp, i32, vp]
         L.kda_state_checkpoint.restype = i32
         L.kda_poll_device_error.argtypes = [vp, vp, P(ctypes.c_uint32)]
@@ -261,6 +266,21 @@ def kda_prefill_chunked(pool: StatePool, weights: kda_weights, io: kda_io, cu_se
                                      ctypes.c_void_p(th.data_ptr()), int(tc.numel() - 1), int(chunk),
                                      req_arr, int(n_req), ws_ptr, ws_bytes, _stream(stream)),
            "kda_prefill_chunked")
+
+
+def kda_prefill_chunked_noalloc(pool: StatePool, weights: kda_weights, io: kda_io, cu_seqlens, slots,
+                                has_initial_state, chunk: int = 64, reqs=(), stream=None) -> None:
+    """kda_prefill_chunked for callers that cannot allocate device memory: the
+    library's fixed 64 MiB scratch array stands in for the workspace."""
+    tc, pc = _host_i32(cu_seqlens)
+    ts, ps = _host_i32(slots)
+    th = torch.as_tensor(has_initial_state, dtype=torch.uint8).contiguous().cpu()
+    n_req = len(reqs)
+    req_arr = (kda_ckpt_req * max(1, n_req))(*[kda_ckpt_req(int(a), int(b), int(c)) for a, b, c in reqs])
+    _check(lib().kda_prefill_chunked_noalloc(pool.handle, ctypes.byref(weights), ctypes.byref(io), pc, ps,
+                                             ctypes.c_void_p(th.data_ptr()), int(tc.numel() - 1), int(chunk),
+                                             req_arr, int(n_req), _stream(stream)),
+           "kda_prefill_chunked_noalloc")
 
 
 def kda_state_checkpoint(pool: StatePool, src_slots, dst_slots, stream=None) -> None:

@@ -210,6 +210,32 @@ KDA_API kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, con
                                const kda_ckpt_req *reqs, int32_t n_reqs, void *workspace,
                                size_t workspace_bytes, kda_stream_t stream);
 
+/* Size of the fixed scratch array behind kda_prefill_chunked_noalloc. */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* kda_prefill_chunked without a caller workspace, for callers that cannot
+ * allocate device memory: for example a plugin whose host runtime reserves
+ * all device memory up front and hands none out, or a C caller with no
+ * device allocator of its own.  The pages have no counterpart for this
+ * entry point; it exists for such callers only.
+ * Arguments, results and errors are those of kda_prefill_chunked, except
+ * that the scratch is a fixed array of KDA_NOALLOC_SCRATCH_BYTES (64 MiB)
+ * compiled into the library: every GPU that loads the library holds it
+ * until the process exits, and no call allocates or frees device memory.
+ * A call that needs more scratch than that (its kda_prefill_workspace_bytes
+ * figure for its own requests; with d = 128 about 270 (chunk, head) pairs of
+ * 64 tokens) returns KDA_ERR_WORKSPACE and enqueues nothing.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.
+ * Every call uses the same array and leaves its contents behind; each call
+ * writes every scratch byte it reads, so nothing needs clearing.  Calls that
+ * overlap on one GPU (other streams, other threads) race on the array:
+ * order them. */
+KDA_API kda_status kda_prefill_chunked_noalloc(kda_pool *pool, const kda_weights *w, const kda_io *io,
+                                               const int32_t *cu_seqlens, const int32_t *slots,
+                                               const uint8_t *has_initial_state, int32_t N, int32_t chunk,
+                                               const kda_ckpt_req *reqs, int32_t n_reqs, kda_stream_t stream);
+
 /* Copies state and conv tail of src_slots[i] into dst_slots[i], bit-exact,
  * for i < n (HOST arrays).  Restoring a checkpoint is the same call with the
  * roles swapped.  dst slots must be distinct and must not appear among the

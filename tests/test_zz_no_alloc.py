@@ -1,0 +1,79 @@
+"""The prefill entry point that allocates nothing.
+
+Some callers cannot allocate device memory (a plugin whose host runtime
+reserves all device memory up front and hands none out, or a C caller with
+no device allocator).  kda_prefill_chunked_noalloc serves them by running
+the chunked prefill in a fixed 64 MiB scratch array compiled into the
+library instead of a caller workspace.  Here it is called through the C ABI
+twice in a row and must agree with kda_prefill_chunked (which takes a
+workspace) within the tolerances used by every other GPU test; a request
+larger than the array must be refused.  This file is collected last, so a
+run that stops at its first failure has already run every other test.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from hybrid_linear_attention_03_gb300 import build as kbuild
+from hybrid_linear_attention_03_gb300 import inputs as I
+from hybrid_linear_attention_03_gb300 import kda
+
+import helpers as hp
+
+pytestmark = pytest.mark.gpu
+H, D, act = 2, 128, torch.bfloat16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    kbuild.build()
+    kda.lib()
+
+
+def _pool_and_weights():
+    pool = kda.StatePool(16, H, D, D, act)
+    w = {k: v.cuda() for k, v in I.layer_weights(61, H, D, D, 4, act).items()}
+    return pool, w, kda.make_weights(w["conv_w"], w["norm_w"])
+
+
+def test_noalloc_prefill_matches_workspace_prefill_twice():
+    lens = [5, 64, 130, 77]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    slots = [3, 0, 7, 11]
+    reqs = [(2, 64, 12), (3, 77, 13)]
+    pa, wa, wgt_a = _pool_and_weights()
+    pb, wb, wgt_b = _pool_and_weights()
+    for call in range(2):  # the second call continues the first (and reuses the scratch)
+        inp = {k: v.cuda() for k, v in I.token_inputs(61, call, int(cu[-1]), H, D, D, 3.0, act).items()}
+        init = [call] * len(lens)
+        out_a = torch.empty(int(cu[-1]), H, D, dtype=act, device="cuda")
+        ws = torch.empty(kda.kda_prefill_workspace_bytes(pa, cu), dtype=torch.uint8, device="cuda")
+        kda.kda_prefill_chunked(pa, wgt_a, kda.make_io(inp, out_a), cu, slots, init, 64, reqs, ws)
+        out_b = torch.full((int(cu[-1]), H, D), float("nan"), dtype=act, device="cuda")
+        kda.kda_prefill_chunked_noalloc(pb, wgt_b, kda.make_io(inp, out_b), cu, slots, init, 64, reqs)
+        torch.cuda.synchronize()
+        assert hp.block_rel_err(hp.f64(out_b), hp.f64(out_a), 1) <= hp.OUT_TOL_BF16, f"call {call}: outputs"
+        for s in slots + [r[2] for r in reqs]:
+            ga = hp.gpu_state_as_oracle(pa.states()[s])
+            gb = hp.gpu_state_as_oracle(pb.states()[s])
+            assert hp.block_rel_err(gb, ga, 2) <= hp.STATE_TOL, f"call {call}: state of slot {s}"
+            assert torch.equal(pa.tails()[s], pb.tails()[s]), f"call {call}: tail of slot {s}"
+    assert kda.kda_poll_device_error(pb) == (kda.KDA_OK, 0)
+
+
+def test_noalloc_prefill_refuses_requests_beyond_the_scratch():
+    pool, w, wgt = _pool_and_weights()
+    L = 64 * 200  # 200 chunks x 2 heads of records: more than 64 MiB
+    assert kda.kda_prefill_workspace_bytes(pool, [0, L]) > kda.KDA_NOALLOC_SCRATCH_BYTES
+    inp = {k: v.cuda() for k, v in I.token_inputs(61, 9, L, H, D, D, 3.0, act).items()}
+    out = torch.zeros(L, H, D, dtype=act, device="cuda")
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_prefill_chunked_noalloc(pool, wgt, kda.make_io(inp, out), [0, L], [0], [0])
+    assert e.value.status == kda.KDA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(pool.states() == 0)
