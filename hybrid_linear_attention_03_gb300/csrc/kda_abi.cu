@@ -40,8 +40,8 @@ bool compute_layout(const kda_pool_desc *d, Layout *L) {
 }
 
 bool valid_weights(const kda_weights *w) {
-    return w && w->conv_w && w->norm_w && std::isfinite(w->eps_l2) && std::isfinite(w->eps_rms) &&
-           w->eps_l2 >= 0.f && w->eps_rms >= 0.f;
+    return w && w->conv_w && w->norm_w && aligned(w->conv_w, 16) && std::isfinite(w->eps_l2) &&
+           std::isfinite(w->eps_rms) && w->eps_l2 >= 0.f && w->eps_rms >= 0.f;
 }
 
 bool valid_io(const kda_io *io) {

@@ -162,30 +162,62 @@ kda_step_kernel(const StepParams p) {
         S[n] = load4(Sin + size_t(row) * D + 4 * c4);
     }
 
+    // Per-token gate inputs of the first token, fetched before the prologue.
+    const int n_own = c4 / C::OWN;
+    const bool owner = (c4 % C::OWN) == 0;
+    const int own_row = n_own * C::RPL + sub;  // 0..15 within the warp
+    const int own_j = gwarp * 16 + own_row;    // value channel this lane reports
+    const Act *alpha = static_cast<const Act *>(p.alpha);
+    const Act *beta = static_cast<const Act *>(p.beta);
+    const Act *gate = static_cast<const Act *>(p.gate);
+    float4 av_next = load4(alpha + (size_t(b) * T * p.H + h) * D + 4 * c4);
+    float bt_next = to_f32(beta[size_t(b) * T * p.H + h]);
+    float gj_next = to_f32(gate[(size_t(b) * T * p.H + h) * D + own_j]);
+
     // ---- conv + SiLU for the head's 3*D channels over the T tokens --------
+    // All loads of a thread's channels (taps, old tail, first token) are
+    // issued before any use, so the prologue costs one memory latency.
     const Act *tail_in = static_cast<const Act *>(p.tails) + size_t(in_slot) * 3 * p.n_ch;
     const Act *cw = static_cast<const Act *>(p.conv_w);
-    for (int idx = threadIdx.x; idx < 3 * D; idx += C::NT) {
-        const int s = idx / D, c = idx - s * D;
-        const int ch = s * p.H * D + h * D + c;
-        const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
-        const float w0 = to_f32(cw[ch * 4 + 0]), w1 = to_f32(cw[ch * 4 + 1]);
-        const float w2 = to_f32(cw[ch * 4 + 2]), w3 = to_f32(cw[ch * 4 + 3]);
-        Act x0 = tail_in[ch], x1 = tail_in[p.n_ch + ch], x2 = tail_in[2 * p.n_ch + ch];
-        raw[(0 * 3 + s) * D + c] = x0;
-        raw[(1 * 3 + s) * D + c] = x1;
-        raw[(2 * 3 + s) * D + c] = x2;
-        for (int t = 0; t < T; ++t) {
-            const Act xt = src[(size_t(b) * T + t) * p.H * D + size_t(h) * D + c];
-            raw[((t + 3) * 3 + s) * D + c] = xt;
-            float acc = w0 * to_f32(x0);
-            acc = fmaf(w1, to_f32(x1), acc);
-            acc = fmaf(w2, to_f32(x2), acc);
-            acc = fmaf(w3, to_f32(xt), acc);
-            conv[(t * 3 + s) * D + c] = acc * sigmoid_f(acc);
-            x0 = x1;
-            x1 = x2;
-            x2 = xt;
+    constexpr int PER = (3 * D + C::NT - 1) / C::NT;
+    float4 wv[PER];
+    Act xv[PER][4];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int idx = threadIdx.x + u * C::NT;
+        if (idx < 3 * D) {
+            const int s = idx / D, c = idx - s * D;
+            const int ch = s * p.H * D + h * D + c;
+            const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
+            wv[u] = load4(cw + size_t(ch) * 4);
+            xv[u][0] = tail_in[ch];
+            xv[u][1] = tail_in[p.n_ch + ch];
+            xv[u][2] = tail_in[2 * p.n_ch + ch];
+            xv[u][3] = src[size_t(b) * T * p.H * D + size_t(h) * D + c];
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int idx = threadIdx.x + u * C::NT;
+        if (idx < 3 * D) {
+            const int s = idx / D, c = idx - s * D;
+            const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
+            Act x0 = xv[u][0], x1 = xv[u][1], x2 = xv[u][2];
+            raw[(0 * 3 + s) * D + c] = x0;
+            raw[(1 * 3 + s) * D + c] = x1;
+            raw[(2 * 3 + s) * D + c] = x2;
+            for (int t = 0; t < T; ++t) {
+                const Act xt = t == 0 ? xv[u][3] : src[(size_t(b) * T + t) * p.H * D + size_t(h) * D + c];
+                raw[((t + 3) * 3 + s) * D + c] = xt;
+                float acc = wv[u].x * to_f32(x0);
+                acc = fmaf(wv[u].y, to_f32(x1), acc);
+                acc = fmaf(wv[u].z, to_f32(x2), acc);
+                acc = fmaf(wv[u].w, to_f32(xt), acc);
+                conv[(t * 3 + s) * D + c] = acc * sigmoid_f(acc);
+                x0 = x1;
+                x1 = x2;
+                x2 = xt;
+            }
         }
     }
     __syncthreads();
@@ -202,13 +234,6 @@ kda_step_kernel(const StepParams p) {
     // All CTAs of the cluster have read the old tail before anyone writes one.
     if constexpr (CL == 1) __syncthreads(); else cluster_sync_all();
 
-    const int n_own = c4 / C::OWN;
-    const bool owner = (c4 % C::OWN) == 0;
-    const int own_row = n_own * C::RPL + sub;  // 0..15 within the warp
-    const int own_j = gwarp * 16 + own_row;    // value channel this lane reports
-    const Act *alpha = static_cast<const Act *>(p.alpha);
-    const Act *beta = static_cast<const Act *>(p.beta);
-    const Act *gate = static_cast<const Act *>(p.gate);
     Act *out = static_cast<Act *>(p.out);
     Act *tails = static_cast<Act *>(p.tails);
     const float wn = to_f32(static_cast<const Act *>(p.norm_w)[own_j]);
@@ -218,9 +243,13 @@ kda_step_kernel(const StepParams p) {
         const size_t tok = size_t(b) * T + t;
         const float4 qv = load4(conv + (t * 3 + 0) * D + 4 * c4);
         const float4 kv = load4(conv + (t * 3 + 1) * D + 4 * c4);
-        const float4 av = load4(alpha + (tok * p.H + h) * D + 4 * c4);
-        const float bt = to_f32(beta[tok * p.H + h]);
-        const float gj = to_f32(gate[(tok * p.H + h) * D + own_j]);
+        const float4 av = av_next;
+        const float bt = bt_next, gj = gj_next;
+        if (t + 1 < T) {
+            av_next = load4(alpha + ((tok + 1) * p.H + h) * D + 4 * c4);
+            bt_next = to_f32(beta[(tok + 1) * p.H + h]);
+            gj_next = to_f32(gate[((tok + 1) * p.H + h) * D + own_j]);
+        }
         const float4 ka = make_float4(kv.x * av.x, kv.y * av.y, kv.z * av.z, kv.w * av.w);
         const float4 bk = make_float4(bt * kv.x, bt * kv.y, bt * kv.z, bt * kv.w);
 
@@ -333,9 +362,13 @@ int sm_count() {
     return cached[dev];
 }
 
-// Split each head over a cluster only when there are too few heads to give
-// every SM two CTAs.
-int pick_cluster(int items, int wph) {
+// Split each head over a cluster only for multi-token launches with too few
+// heads to give every SM two CTAs.  A single-token launch is latency-bound:
+// measured at batch 1 (64 heads), one CTA per head takes 5.3 us per step and
+// splits of 2/4/8 CTAs take 6.6/7.7/9.5 us, the cluster barriers costing more
+// than the shorter per-CTA state stream saves.
+int pick_cluster(int items, int wph, int T) {
+    if (T == 1) return 1;
     const int target = 2 * sm_count();
     int cl = 1;
     while (cl < wph && cl < 8 && items * cl < target) cl *= 2;
@@ -345,7 +378,7 @@ int pick_cluster(int items, int wph) {
 template <int D, typename Act>
 kda_status launch_d(const StepParams &p, cudaStream_t stream) {
     constexpr int WPH = D / 16;
-    const int cl = pick_cluster(p.B * p.H, WPH);
+    const int cl = pick_cluster(p.B * p.H, WPH, p.T);
     switch (cl) {
         case 1: return launch_cfg<D, Act, 1>(p, stream);
         case 2: if constexpr (WPH >= 2) return launch_cfg<D, Act, 2>(p, stream); break;

@@ -99,7 +99,7 @@ typedef struct {
 
 /* Layer weights (device pointers, act dtype). */
 typedef struct {
-    const void *conv_w; /* [n_ch][4]: row c holds channel c's taps, tap 3 on the current token */
+    const void *conv_w; /* [n_ch][4]: row c holds channel c's taps, tap 3 on the current token; 16-byte aligned */
     const void *norm_w; /* [d_v], shared by all heads */
     float eps_l2;       /* added under the root of the q/k L2 norm (1e-6) */
     float eps_rms;      /* added under the root of the RMSNorm (1e-5) */

@@ -114,25 +114,31 @@ def test_verify_snapshots_equal_decode_steps_bitexact():
 
 
 def test_cluster_split_is_bitexact():
-    """The same head computed with 8 CTAs per head (batch 1) and with one CTA
-    per head (batch 64) gives identical bits."""
-    H, D, act = 8, 128, torch.bfloat16
-    pool = kda.StatePool(130, H, D, D, act)
+    """The same heads computed with 8 CTAs per head (a 2-draft verify of one
+    sequence) and with one CTA per head (the same verify in a batch of 64)
+    give identical bits: outputs, both snapshots and tails."""
+    H, D, act, T = 8, 128, torch.bfloat16, 2
+    pool = kda.StatePool(256, H, D, D, act)
     wd = hp.to_device(_weights(3, H, D, act))
     w = kda.make_weights(wd["conv_w"], wd["norm_w"])
     g = torch.Generator(device="cpu").manual_seed(0)
     pool.states()[:64].copy_(torch.randn(64, H, D, D, generator=g) * 0.05)
     pool.tails()[:64].copy_(torch.randn(64, 3, pool.n_ch, generator=g).to(act))
     kda.kda_state_checkpoint(pool, list(range(64)), list(range(64, 128)))
-    inp = hp.to_device(_tokens(3, 0, 64, H, D, act))
-    big = torch.empty(64, H, D, dtype=act, device="cuda")
-    kda.kda_decode(pool, w, kda.make_io(inp, big), torch.arange(64, dtype=torch.int32, device="cuda"), 64)
+    inp = hp.to_device(_tokens(3, 0, 64 * T, H, D, act))
+    big = torch.empty(64 * T, H, D, dtype=act, device="cuda")
+    ins = torch.arange(64, dtype=torch.int32, device="cuda")
+    snaps = torch.stack([ins + 128, ins], 1).reshape(-1).contiguous()  # draft 0 to a spare, draft 1 in place
+    kda.kda_verify(pool, w, kda.make_io(inp, big), ins, snaps, 64, T)
     for b in (0, 17, 63):
-        tok = {k: v[b:b + 1] for k, v in inp.items()}
-        small = torch.empty(1, H, D, dtype=act, device="cuda")
-        kda.kda_decode(pool, w, kda.make_io(tok, small), torch.tensor([64 + b], dtype=torch.int32, device="cuda"), 1)
-        assert torch.equal(small[0], big[b])
+        tok = {k: v[b * T:(b + 1) * T] for k, v in inp.items()}
+        small = torch.empty(T, H, D, dtype=act, device="cuda")
+        kda.kda_verify(pool, w, kda.make_io(tok, small), torch.tensor([64 + b], dtype=torch.int32, device="cuda"),
+                       torch.tensor([192 + b, 64 + b], dtype=torch.int32, device="cuda"), 1, T)
+        assert torch.equal(small, big[b * T:(b + 1) * T])
         assert torch.equal(pool.states()[64 + b], pool.states()[b])
+        assert torch.equal(pool.states()[192 + b], pool.states()[128 + b])
+        assert torch.equal(pool.tails()[64 + b], pool.tails()[b])
 
 
 def test_rollback_adopts_snapshot_and_continues():
