@@ -66,9 +66,8 @@ def test_decode_chain_matches_oracle(D, act):
 
 @pytest.mark.parametrize("B", [1, 12, 20, 40])
 def test_verify_matches_oracle(B):
-    """B sequences x T = 8 drafts (H = 8, d = 128, bf16); B picks the cluster
-    split (8, 4, 2 and 1 CTAs per head).  Snapshots go to a shuffled table and
-    each sequence's start slot doubles as its snapshot 0."""
+    """B sequences x T = 8 drafts (H = 8, d = 128, bf16).  Snapshots go to a
+    shuffled table and each sequence's start slot doubles as its snapshot 0."""
     H, D, T, act = 8, 128, 8, torch.bfloat16
     ns = B * T
     m = Mirror(ns, H, D, act, _weights(11, H, D, act))
@@ -113,10 +112,9 @@ def test_verify_snapshots_equal_decode_steps_bitexact():
         assert torch.equal(pool.tails()[20], pool.tails()[2 + t]), f"tail differs at draft {t}"
 
 
-def test_cluster_split_is_bitexact():
-    """The same heads computed with 8 CTAs per head (a 2-draft verify of one
-    sequence) and with one CTA per head (the same verify in a batch of 64)
-    give identical bits: outputs, both snapshots and tails."""
+def test_batch_composition_is_bitexact():
+    """A 2-draft verify of one sequence alone and the same verify inside a
+    batch of 64 give identical bits: outputs, both snapshots and tails."""
     H, D, act, T = 8, 128, torch.bfloat16, 2
     pool = kda.StatePool(256, H, D, D, act)
     wd = hp.to_device(_weights(3, H, D, act))
