@@ -1,4 +1,5 @@
-// kda_prefill.cu -- chunked KDA prefill (WY / UT form), d_k = d_v = 128, C = 64.
+// kda_prefill.cu -- chunked KDA prefill (WY / UT form) on TMA + tcgen05,
+// d_k = d_v = 128, chunk C = 64.
 //
 // "vLLM Kimi K3 지원", section "Fused Kernels 및 메타데이터 최적화", KDA Prefill
 // bullet: prefill runs chunked (FlashKDA).  Within a chunk of C tokens with
@@ -10,20 +11,34 @@
 // and, carried over chunks with the state S (d_k x d_v):
 //   U = Ut - W S,   O = (exp(G) . Q) S + P U,
 //   S <- Diag(exp(G_last)) S + sum_s (exp(G_last - G_s) . k_s) U_s^T.
-// The exponent of exp(G_r - G_s) is split around a per-channel reference
-// c_i (the middle of the chunk's log-decay range): k_r exp(G_r - c) times
-// k_s exp(c - G_s).  Both factors stay inside fp32 range while the chunk's
-// decay span per channel is below 160 (alpha around 0.08 or larger on
-// average); a chunk beyond that takes an exact per-element path.
+// exp(G_r - G_s) is split around a per-channel reference c_i (the middle of
+// the chunk's log-decay range): k_r exp(G_r - c) times k_s exp(c - G_s).
+// Both factors stay in fp32 range while a channel's decay span over the chunk
+// is at most 160; a chunk beyond that computes A and P with exact
+// per-element exponentials instead.
+//
+// Every product that feeds the state runs on the tensor cores as three bf16
+// MMAs (x = hi + lo with hi = bf16(x), lo = bf16(x - hi): hi*hi + hi*lo +
+// lo*hi, fp32 accumulation in TMEM), which keeps about 16 mantissa bits.  All
+// MMAs are M = 128 (the chunk-pair trick and transposed products below), with
+// operands in the 128-byte-swizzle K-major layout (kda_sm100.cuh).
 //
 // Kernels (one stream, in order):
-//   prep   (chunk, head): conv + SiLU, L2 of q and k, G, beta -> workspace
-//   intra  (chunk, head): A, P, T, W, Ut                     -> workspace
-//   chain  (sequence, head, d_v block): sequential over chunks: U, O, S;
-//          interval checkpoints; end state -> slot
-//   out    (chunk, head): gated RMSNorm of O -> out
-//   tails  checkpoint tails, then end tails -> slots
+//   prep   (chunk, head): TMA loads the raw q, k, v, alpha tiles (with the
+//          3-token conv halo); conv + SiLU, L2 of q and k, G, beta.
+//   intra  (chunk, head): [K exp(G-c); Q exp(G-c)] x (K exp(c-G))^T -> A, P
+//          (one M=128 MMA); T = (I + A)^-1 on CUDA cores; W^T and Ut^T as
+//          M=128 MMAs; writes the chain's operand images.
+//   chain  (sequence, head): sequential over chunks; S^T (fp32) lives in
+//          TMEM; (W S)^T, (Q S)^T, (K^T U)^T and (P U)^T are MMAs; the next
+//          chunk's operand images stream in by TMA bulk copies while the
+//          current chunk computes; interval checkpoints; end state -> slot.
+//   out    (chunk, head): gated RMSNorm of O -> out.
+//   tails  checkpoint tails, then end tails -> slots.
 #include "kda_internal.h"
+#include "kda_sm100.cuh"
+
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cmath>
@@ -34,10 +49,11 @@ namespace kda {
 
 namespace {
 
-constexpr int D = 128;     // channels per head (d_k = d_v)
-constexpr int CH = 64;     // chunk length
-constexpr int NB = 4;      // d_v blocks per head in the chain
-constexpr int DB = D / NB; // value channels per chain CTA
+using namespace sm100;
+
+constexpr int D = 128;   // channels per head (d_k = d_v)
+constexpr int CH = 64;   // chunk length
+constexpr int HALO = 3;  // previous raw inputs the width-4 conv needs
 constexpr float kLogAlphaMin = -100.0f;  // log(alpha) floor: alpha below e^-100 acts as e^-100
 constexpr float kSafeSpan = 160.0f;      // max per-channel log-decay span for the split exponent
 
@@ -51,25 +67,36 @@ struct CkptMeta {
     int32_t seq, token_pos, dst_slot, pad;
 };
 
-// Per (chunk, head) workspace record, fp32.
-struct ChunkRec {
-    static constexpr size_t QH = 0;                 // [64][128] L2-normalised q
-    static constexpr size_t KH = QH + CH * D;       // [64][128] L2-normalised k
-    static constexpr size_t VV = KH + CH * D;       // [64][128] conv'd v
-    static constexpr size_t GG = VV + CH * D;       // [64][128] cumulative log decay
-    static constexpr size_t WW = GG + CH * D;       // [64][128] W
-    static constexpr size_t UT = WW + CH * D;       // [64][128] Ut
-    static constexpr size_t OO = UT + CH * D;       // [64][128] O (pre-norm output)
-    static constexpr size_t PP = OO + CH * D;       // [64][64]  P (zero above the diagonal)
-    static constexpr size_t BB = PP + CH * CH;      // [64]      beta (0 on padding rows)
-    static constexpr size_t FLOATS = BB + CH;
+// Per (chunk, head) workspace record (bytes).  "img" = bf16 operand image in
+// the 128-byte-swizzle K-major layout, [rows][K].
+struct Rec {
+    static constexpr size_t QH = 0;                  // fp32 [64][128] L2-normalised q
+    static constexpr size_t KH = QH + 32768;         // fp32 [64][128] L2-normalised k
+    static constexpr size_t VV = KH + 32768;         // fp32 [64][128] conv'd v
+    static constexpr size_t GG = VV + 32768;         // fp32 [64][128] cumulative log decay
+    static constexpr size_t BB = GG + 32768;         // fp32 [64] beta (0 on padding rows)
+    static constexpr size_t W_HI = BB + 1024;        // img [64 r][128 i]   W
+    static constexpr size_t W_LO = W_HI + 16384;
+    static constexpr size_t Q_HI = W_LO + 16384;     // img [64 r][128 i]   exp(G) . q
+    static constexpr size_t Q_LO = Q_HI + 16384;
+    static constexpr size_t KT_HI = Q_LO + 16384;    // img [128 i][64 r]   (exp(G_last - G) . k)^T
+    static constexpr size_t KT_LO = KT_HI + 16384;
+    static constexpr size_t P_HI = KT_LO + 16384;    // img [64 r][64 s]    P
+    static constexpr size_t P_LO = P_HI + 8192;
+    static constexpr size_t GAM = P_LO + 8192;       // fp32 [128] exp(G_last)
+    static constexpr size_t UT = GAM + 1024;         // fp32 [128 j][64 r]  Ut^T
+    static constexpr size_t OO = UT + 32768;         // fp32 [64 r][128 j]  O (pre-norm)
+    static constexpr size_t BYTES = OO + 32768;
+    static constexpr uint32_t B1_BYTES = uint32_t(KT_HI - W_HI);  // W + Q images
+    static constexpr uint32_t B2_BYTES = uint32_t(UT - KT_HI);    // K^T + P images + gamma
 };
+static_assert(Rec::BYTES % 1024 == 0, "record keeps 1 KiB alignment");
 
 struct PrefillParams {
     const SeqMeta *seqs;
     const ChunkMeta *chunks;
     const CkptMeta *ckpts;
-    float *rec;  // [n_chunks][H] ChunkRec
+    char *rec;  // [n_chunks][H] records
     float *states;
     void *tails;
     uint32_t *err;
@@ -82,362 +109,618 @@ struct PrefillParams {
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 
-__device__ __forceinline__ float *rec_ptr(const PrefillParams &p, int g, int h) {
-    return p.rec + (size_t(g) * p.H + h) * ChunkRec::FLOATS;
+__device__ __forceinline__ char *rec_ptr(const PrefillParams &p, int g, int h) {
+    return p.rec + (size_t(g) * p.H + h) * Rec::BYTES;
 }
 
-// ---------------------------------------------------------------- prep ----
+template <typename T>
+__device__ __forceinline__ T *at(char *base, size_t off) {
+    return reinterpret_cast<T *>(base + off);
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
 template <typename Act>
-__global__ void __launch_bounds__(D) prefill_prep_kernel(const PrefillParams p) {
-    extern __shared__ __align__(16) float sm[];
-    float *qs = sm;             // [64][128]
-    float *ks = qs + CH * D;    // [64][128]
-    float *rq = ks + CH * D;    // [64]
-    float *rk = rq + CH;        // [64]
-    const int g = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
+__device__ __forceinline__ float4 act4(const Act *p);
+template <>
+__device__ __forceinline__ float4 act4<float>(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+template <>
+__device__ __forceinline__ float4 act4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// ============================================================== prep =====
+// One CTA (4 warps) per (chunk, head).  TMA brings the q, k, v tiles of the
+// chunk's 64 tokens plus the 3 before them, and the alpha tile; the halo
+// rows that fall before the segment are replaced by the slot's conv tail (or
+// zeros).  Warp w handles tokens w, w+4, ...; lane l channels 4l..4l+3.
+template <typename Act>
+__global__ void __launch_bounds__(128) prefill_prep_kernel(const PrefillParams p,
+                                                           const __grid_constant__ CUtensorMap tm_q,
+                                                           const __grid_constant__ CUtensorMap tm_k,
+                                                           const __grid_constant__ CUtensorMap tm_v,
+                                                           const __grid_constant__ CUtensorMap tm_a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr size_t TILE = size_t(CH + HALO) * D * sizeof(Act);
+    Act *tq = reinterpret_cast<Act *>(sm);
+    Act *tk = reinterpret_cast<Act *>(sm + TILE);
+    Act *tv = reinterpret_cast<Act *>(sm + 2 * TILE);
+    Act *ta = reinterpret_cast<Act *>(sm + 3 * TILE);
+    __shared__ uint64_t bar;
+    const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const ChunkMeta cm = p.chunks[g];
     const SeqMeta sq = p.seqs[cm.seq];
-    float *rec = rec_ptr(p, g, h);
-    const Act *tail = static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch;
+    char *rec = rec_ptr(p, g, h);
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bar, uint32_t(3 * TILE + size_t(CH) * D * sizeof(Act)));
+        tma_load_3d(tq, &tm_q, &bar, 0, h, cm.row0 - HALO);
+        tma_load_3d(tk, &tm_k, &bar, 0, h, cm.row0 - HALO);
+        tma_load_3d(tv, &tm_v, &bar, 0, h, cm.row0 - HALO);
+        tma_load_3d(ta, &tm_a, &bar, 0, h, cm.row0);
+    }
+    // conv taps of this lane's channels while the tiles fly
     const Act *cw = static_cast<const Act *>(p.conv_w);
-    const size_t HD = size_t(p.H) * D;
-    for (int s = 0; s < 3; ++s) {
-        const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
-        const int ch = s * p.H * D + h * D + i;
-        const float w0 = to_f32(cw[ch * 4 + 0]), w1 = to_f32(cw[ch * 4 + 1]);
-        const float w2 = to_f32(cw[ch * 4 + 2]), w3 = to_f32(cw[ch * 4 + 3]);
-        float x[3];
-        for (int j = 0; j < 3; ++j) {
-            const int pos = cm.pos0 - 3 + j;
-            if (pos >= 0) x[j] = to_f32(src[size_t(sq.row0 + pos) * HD + size_t(h) * D + i]);
-            else x[j] = sq.has_init ? to_f32(tail[size_t(3 + pos) * p.n_ch + ch]) : 0.f;
-        }
-        float *dst = s == 0 ? qs : (s == 1 ? ks : rec + ChunkRec::VV);
-        for (int t = 0; t < CH; ++t) {
-            float y = 0.f;
-            if (t < cm.len) {
-                const float xt = to_f32(src[size_t(cm.row0 + t) * HD + size_t(h) * D + i]);
-                float acc = w0 * x[0];
-                acc = fmaf(w1, x[1], acc);
-                acc = fmaf(w2, x[2], acc);
-                acc = fmaf(w3, xt, acc);
-                y = acc * sigmoid_f(acc);
-                x[0] = x[1];
-                x[1] = x[2];
-                x[2] = xt;
+    float4 w[3][4];
+#pragma unroll
+    for (int s = 0; s < 3; ++s)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) w[s][m] = act4(cw + size_t(s * p.H * D + h * D + 4 * lane + m) * 4);
+    __syncthreads();
+    // a timed-out wait is seen by every thread, so all of them leave together
+    if (!__syncthreads_and(mbar_wait(&bar, 0, p.err))) return;
+    // halo rows before the segment start: the slot's conv tail, or zeros
+    if (cm.pos0 < HALO) {
+        const Act *tail = static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch;
+        for (int e = tid; e < 3 * HALO * D; e += 128) {
+            const int s = e / (HALO * D), j = (e / D) % HALO, c = e % D;
+            const int pos = cm.pos0 - HALO + j;
+            if (pos < 0) {
+                Act *tile = s == 0 ? tq : (s == 1 ? tk : tv);
+                tile[j * D + c] = sq.has_init ? tail[size_t(HALO + pos) * p.n_ch + s * p.H * D + h * D + c]
+                                              : from_f32<Act>(0.f);
             }
-            dst[t * D + i] = y;
         }
     }
     __syncthreads();
-    const int warp = i >> 5, lane = i & 31;
-    for (int t = warp; t < CH; t += D / 32) {
-        float a = 0.f, b = 0.f;
-        for (int c = lane; c < D; c += 32) {
-            a = fmaf(qs[t * D + c], qs[t * D + c], a);
-            b = fmaf(ks[t * D + c], ks[t * D + c], b);
+    float *QH = at<float>(rec, Rec::QH), *KH = at<float>(rec, Rec::KH), *VV = at<float>(rec, Rec::VV);
+    for (int t = warp; t < CH; t += 4) {
+        float y[3][4];
+#pragma unroll
+        for (int s = 0; s < 3; ++s) {
+            const Act *tile = s == 0 ? tq : (s == 1 ? tk : tv);
+            float4 x[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = act4(tile + (t + j) * D + 4 * lane);
+            const float xs[4][4] = {{x[0].x, x[1].x, x[2].x, x[3].x}, {x[0].y, x[1].y, x[2].y, x[3].y},
+                                    {x[0].z, x[1].z, x[2].z, x[3].z}, {x[0].w, x[1].w, x[2].w, x[3].w}};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float acc = w[s][m].x * xs[m][0];
+                acc = fmaf(w[s][m].y, xs[m][1], acc);
+                acc = fmaf(w[s][m].z, xs[m][2], acc);
+                acc = fmaf(w[s][m].w, xs[m][3], acc);
+                y[s][m] = t < cm.len ? acc * sigmoid_f(acc) : 0.f;
+            }
         }
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            a = fmaf(y[0][m], y[0][m], a);
+            b = fmaf(y[1][m], y[1][m], b);
+        }
+#pragma unroll
         for (int o = 16; o; o >>= 1) {
             a += __shfl_xor_sync(0xffffffffu, a, o);
             b += __shfl_xor_sync(0xffffffffu, b, o);
         }
-        if (lane == 0) {
-            rq[t] = rsqrtf(a + p.eps_l2);
-            rk[t] = rsqrtf(b + p.eps_l2);
-        }
+        const float rq = rsqrtf(a + p.eps_l2), rk = rsqrtf(b + p.eps_l2);
+        *reinterpret_cast<float4 *>(QH + t * D + 4 * lane) = make_float4(y[0][0] * rq, y[0][1] * rq, y[0][2] * rq, y[0][3] * rq);
+        *reinterpret_cast<float4 *>(KH + t * D + 4 * lane) = make_float4(y[1][0] * rk, y[1][1] * rk, y[1][2] * rk, y[1][3] * rk);
+        *reinterpret_cast<float4 *>(VV + t * D + 4 * lane) = make_float4(y[2][0], y[2][1], y[2][2], y[2][3]);
     }
-    __syncthreads();
-    const Act *al = static_cast<const Act *>(p.alpha);
+    // cumulative log decay: thread = channel
+    float *GG = at<float>(rec, Rec::GG);
     float G = 0.f;
     for (int t = 0; t < CH; ++t) {
-        rec[ChunkRec::QH + t * D + i] = qs[t * D + i] * rq[t];
-        rec[ChunkRec::KH + t * D + i] = ks[t * D + i] * rk[t];
-        if (t < cm.len) G += fmaxf(logf(to_f32(al[size_t(cm.row0 + t) * HD + size_t(h) * D + i])), kLogAlphaMin);
-        rec[ChunkRec::GG + t * D + i] = G;
+        if (t < cm.len) G += fmaxf(logf(to_f32(ta[t * D + tid])), kLogAlphaMin);
+        GG[t * D + tid] = G;
     }
-    if (i < CH)
-        rec[ChunkRec::BB + i] =
-            i < cm.len ? to_f32(static_cast<const Act *>(p.beta)[size_t(cm.row0 + i) * p.H + h]) : 0.f;
+    if (tid < CH)
+        at<float>(rec, Rec::BB)[tid] =
+            tid < cm.len ? to_f32(static_cast<const Act *>(p.beta)[size_t(cm.row0 + tid) * p.H + h]) : 0.f;
 }
 
-// ---------------------------------------------------------------- intra ---
-// A, P, T = (I + A)^-1, W, Ut for one (chunk, head) on CUDA cores.
-constexpr int LDK = D + 1;   // padded row of a [64][128] smem tile
-constexpr int LDC = CH + 1;  // padded row of a [64][64] smem tile
+// ============================================================== intra ====
+namespace is {  // intra shared-memory map (bytes from a 1 KiB-aligned base)
+constexpr uint32_t X_HI = 0, X_LO = 32768, KB_HI = 65536, KB_LO = 81920;           // phase 1
+constexpr uint32_t A_F32 = 0, XS_F32 = 16384, T_F32 = 81920;                        // inverse
+constexpr uint32_t T_HI = 0, T_LO = 8192, AK_HI = 16384, AK_LO = 32768, AV_HI = 49152, AV_LO = 65536;  // phase 3
+constexpr uint32_t ST_Q = 98304, ST_KT = 131072, ST_P = 163840;  // staging of images for bulk stores
+constexpr uint32_t ST_W = 98304;
+constexpr uint32_t SMALL = 180224;
+constexpr uint32_t BYTES = SMALL + 2048;
+}  // namespace is
 
-__global__ void __launch_bounds__(256) prefill_intra_kernel(const PrefillParams p) {
-    extern __shared__ __align__(16) float sm[];
-    float *Ka = sm;               // [64][LDK]  k exp(G - c), later diag(beta) exp(G) k
-    float *Kb = Ka + CH * LDK;    // [64][LDK]  k exp(c - G), later diag(beta) v
-    float *Qa = Kb + CH * LDK;    // [64][LDK]  q exp(G - c)
-    float *A = Qa + CH * LDK;     // [64][LDC]
-    float *T = A + CH * LDC;      // [64][LDC]
-    float *X = T + CH * LDC;      // [64][LDC] scratch for the block inverse
-    float *cref = X + CH * LDC;   // [128]
-    float *beta = cref + D;       // [64]
-    int *flag = reinterpret_cast<int *>(beta + CH);
-    const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-    float *rec = rec_ptr(p, g, h);
-    const float *QH = rec + ChunkRec::QH, *KH = rec + ChunkRec::KH, *VV = rec + ChunkRec::VV,
-                *GG = rec + ChunkRec::GG;
-    if (tid == 0) *flag = 0;
-    if (tid < CH) beta[tid] = rec[ChunkRec::BB + tid];
-    __syncthreads();
-    if (tid < D) {
-        const float g0 = GG[tid], g1 = GG[(CH - 1) * D + tid];
-        cref[tid] = 0.5f * (g0 + g1);
-        if (g0 - g1 > kSafeSpan) atomicOr(flag, 1);
+// Fills `rows` x (8 * chunks_per_row) elements of an image pair with f(row, k0, out8).
+template <typename F>
+__device__ __forceinline__ void build_image(unsigned char *hi, unsigned char *lo, int rows, int chunks_per_row,
+                                            int tid, int nthreads, F f) {
+    for (int u = tid; u < rows * chunks_per_row; u += nthreads) {
+        const int r = u / chunks_per_row, c = u - r * chunks_per_row;
+        float x[8];
+        f(r, 8 * c, x);
+        uint4 vh, vl;
+        split8(x, vh, vl);
+        const uint32_t off = sw128_chunk(r, c, rows);
+        *reinterpret_cast<uint4 *>(hi + off) = vh;
+        if (lo) *reinterpret_cast<uint4 *>(lo + off) = vl;
     }
+}
+
+// Issues the three bf16 MMAs of a split product: D (+)= Ahi Bhi + Ahi Blo + Alo Bhi.
+__device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo, int a_rows,
+                                     int b_rows, int k_total, uint32_t idesc, bool accumulate) {
+    const int ksteps = k_total / 16;
+    for (int part = 0; part < 3; ++part) {
+        const uint32_t a = part == 2 ? a_lo : a_hi;
+        const uint32_t b = part == 1 ? b_lo : b_hi;
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int kb = ks >> 2, kk = ks & 3;
+            const uint64_t ad = sdesc_sw128(a + uint32_t(kb * a_rows * 128 + kk * 32));
+            const uint64_t bd = sdesc_sw128(b + uint32_t(kb * b_rows * 128 + kk * 32));
+            mma_bf16(d, ad, bd, idesc, (accumulate || part > 0 || ks > 0) ? 1u : 0u);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(128) prefill_intra_kernel(const PrefillParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *cref = reinterpret_cast<float *>(sm + is::SMALL);  // [128]
+    float *beta = cref + D;                                    // [64]
+    int *flag = reinterpret_cast<int *>(beta + CH);            // [1]
+    uint32_t *tbase = reinterpret_cast<uint32_t *>(flag + 1);  // [1]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + is::SMALL + 1024);  // [1]
+    const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    char *rec = rec_ptr(p, g, h);
+    const float *QH = at<float>(rec, Rec::QH), *KH = at<float>(rec, Rec::KH), *VV = at<float>(rec, Rec::VV),
+                *GG = at<float>(rec, Rec::GG);
+    const uint32_t sbase = smem_u32(sm);
+    if (tid == 0) {
+        *flag = 0;
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tbase, 256);
+    if (tid < CH) beta[tid] = at<float>(rec, Rec::BB)[tid];
+    {
+        const float g0 = GG[tid], gl = GG[(CH - 1) * D + tid];
+        cref[tid] = 0.5f * (g0 + gl);
+        at<float>(rec, Rec::GAM)[tid] = expf(gl);
+        if (g0 - gl > kSafeSpan) atomicOr(flag, 1);
+    }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tbase;
     const bool exact = *flag != 0;
-    for (int e = tid; e < CH * D; e += 256) {
-        const int r = e / D, i = e - r * D;
-        const float gr = GG[e], c = cref[i];
-        const float er = exact ? 1.f : expf(gr - c), es = exact ? 1.f : expf(c - gr);
-        Ka[r * LDK + i] = KH[e] * er;
-        Kb[r * LDK + i] = KH[e] * es;
-        Qa[r * LDK + i] = QH[e] * er;
-    }
-    __syncthreads();
-    // A (s < r, scaled by beta_r) and P (s <= r): 4 x 4 output block per thread
-    {
-        const int r0 = (tid >> 4) * 4, s0 = (tid & 15) * 4;
-        float a[4][4] = {}, pp[4][4] = {};
-        if (!exact) {
-            for (int i = 0; i < D; ++i) {
-                float kr[4], qr[4], ks[4];
+    bool ok = true;
+    uint32_t phase = 0;
+
+    // ---- phase 1: X = [K exp(G - c); Q exp(G - c)], Kb = K exp(c - G) -> A, P
+    if (!exact) {
+        build_image(sm + is::X_HI, sm + is::X_LO, 128, 16, tid, 128, [&](int r, int k0, float(&x)[8]) {
+            const float *src = r < CH ? KH + r * D : QH + (r - CH) * D;
+            const float *gg = GG + (r & (CH - 1)) * D;
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    kr[m] = Ka[(r0 + m) * LDK + i];
-                    qr[m] = Qa[(r0 + m) * LDK + i];
-                    ks[m] = Kb[(s0 + m) * LDK + i];
-                }
+            for (int e = 0; e < 8; ++e) x[e] = src[k0 + e] * expf(gg[k0 + e] - cref[k0 + e]);
+        });
+        build_image(sm + is::KB_HI, sm + is::KB_LO, CH, 16, tid, 128, [&](int r, int k0, float(&x)[8]) {
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
-#pragma unroll
-                    for (int n = 0; n < 4; ++n) {
-                        a[m][n] = fmaf(kr[m], ks[n], a[m][n]);
-                        pp[m][n] = fmaf(qr[m], ks[n], pp[m][n]);
-                    }
-            }
-        } else {
-            for (int i = 0; i < D; ++i)
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-#pragma unroll
-                    for (int n = 0; n < 4; ++n) {
-                        const int r = r0 + m, s = s0 + n;
-                        if (s > r) continue;
-                        const float f = expf(GG[r * D + i] - GG[s * D + i]) * Kb[s * LDK + i];
-                        a[m][n] = fmaf(Ka[r * LDK + i], f, a[m][n]);
-                        pp[m][n] = fmaf(Qa[r * LDK + i], f, pp[m][n]);
-                    }
-        }
-        float *P = rec + ChunkRec::PP;
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const int r = r0 + m, s = s0 + n;
-                A[r * LDC + s] = s < r ? beta[r] * a[m][n] : 0.f;
-                P[r * CH + s] = s <= r ? pp[m][n] : 0.f;
-            }
-    }
-    __syncthreads();
-    // T = (I + A)^-1, unit lower triangular, by 16 x 16 blocks.
-    // Diagonal blocks: forward substitution, one warp per block, lane = column
-    // (each lane reads only the column it writes).
-    {
-        const int warp = tid >> 5, lane = tid & 31;
-        for (int e = tid; e < CH * LDC; e += 256) T[e] = 0.f;
+            for (int e = 0; e < 8; ++e) x[e] = KH[r * D + k0 + e] * expf(cref[k0 + e] - GG[r * D + k0 + e]);
+        });
+        fence_proxy_async_smem();
+        tc_fence_before();
         __syncthreads();
-        if (warp < 4 && lane < 16) {
-            const int b0 = warp * 16, c = b0 + lane;
-            for (int r = b0; r < b0 + 16; ++r) {
-                float acc = (r == c) ? 1.f : 0.f;
-                for (int s = c; s < r; ++s) acc = fmaf(-A[r * LDC + s], T[s * LDC + c], acc);
-                T[r * LDC + c] = (r >= c) ? acc : 0.f;
-            }
-        }
-        __syncthreads();
-        // Off-diagonal blocks by distance d: T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
-        for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += 256) {
-                const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-                const int a = blk + d, b = blk;
-                float acc = 0.f;
-                for (int s = b * 16; s < a * 16; ++s)
-                    acc = fmaf(A[(a * 16 + r) * LDC + s], T[s * LDC + b * 16 + cc], acc);
-                X[(a * 16 + r) * LDC + b * 16 + cc] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nblk * 256; e += 256) {
-                const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-                const int a = blk + d, b = blk;
-                float acc = 0.f;
-                for (int s = 0; s <= r; ++s)
-                    acc = fmaf(-T[(a * 16 + r) * LDC + a * 16 + s], X[(a * 16 + s) * LDC + b * 16 + cc], acc);
-                T[(a * 16 + r) * LDC + b * 16 + cc] = acc;
-            }
-            __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            mma3(tm, sbase + is::X_HI, sbase + is::X_LO, sbase + is::KB_HI, sbase + is::KB_LO, 128, CH, D,
+                 idesc_bf16_f32(128, CH), false);
+            mma_commit(bar);
         }
     }
-    // W = T diag(beta) (exp(G) . K),  Ut = T diag(beta) V
-    for (int e = tid; e < CH * D; e += 256) {
-        const int s = e / D, i = e - s * D;
-        Ka[s * LDK + i] = beta[s] * expf(GG[e]) * KH[e];
-        Kb[s * LDK + i] = beta[s] * VV[e];
-    }
+    // chain images that need no MMA: exp(G) . q (rows r) and (exp(G_last - G) . k)^T (rows i)
+    build_image(sm + is::ST_Q, sm + is::ST_Q + 16384, CH, 16, tid, 128, [&](int r, int k0, float(&x)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = QH[r * D + k0 + e] * expf(GG[r * D + k0 + e]);
+    });
+    build_image(sm + is::ST_KT, sm + is::ST_KT + 16384, D, 8, tid, 128, [&](int i, int r0, float(&x)[8]) {
+        const float gl = GG[(CH - 1) * D + i];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = KH[(r0 + e) * D + i] * expf(gl - GG[(r0 + e) * D + i]);
+    });
+    fence_proxy_async_smem();
     __syncthreads();
-    {
-        const int r0 = (tid >> 4) * 4, i0 = (tid & 15) * 8;
-        float w[4][8] = {}, u[4][8] = {};
-        for (int s = 0; s < r0 + 4; ++s) {
-            float t4[4];
+    if (tid == 0) {
+        bulk_store(rec + Rec::Q_HI, sm + is::ST_Q, 32768);
+        bulk_store(rec + Rec::KT_HI, sm + is::ST_KT, 32768);
+        bulk_commit();
+    }
+    // ---- A (s < r, times beta_r) -> fp32, P (s <= r) -> images
+    float *A = reinterpret_cast<float *>(sm + is::A_F32);
+    unsigned char *phi = sm + is::ST_P, *plo = sm + is::ST_P + 8192;
+    if (!exact) {
+        ok = __syncthreads_and(mbar_wait(bar, phase, p.err));
+        phase ^= 1;
+        tc_fence_after();
+        const int m = warp * 32 + lane;  // TMEM lane = row of X
+        if (ok) {
+            for (int c0 = 0; c0 < CH; c0 += 16) {
+                float v[16];
+                tmem_ld16(tm + (uint32_t(warp * 32) << 16) + c0, v);
+                tmem_wait_ld();
+                if (m < CH) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m) t4[m] = T[(r0 + m) * LDC + s];
+                    for (int e = 0; e < 16; ++e) A[m * CH + c0 + e] = (c0 + e < m) ? beta[m] * v[e] : 0.f;
+                } else {
+                    const int r = m - CH;
 #pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                const float kk = Ka[s * LDK + i0 + n], vv = Kb[s * LDK + i0 + n];
+                    for (int half = 0; half < 2; ++half) {
+                        float x[8];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    w[m][n] = fmaf(t4[m], kk, w[m][n]);
-                    u[m][n] = fmaf(t4[m], vv, u[m][n]);
+                        for (int e = 0; e < 8; ++e) x[e] = (c0 + 8 * half + e <= r) ? v[8 * half + e] : 0.f;
+                        uint4 vh, vl;
+                        split8(x, vh, vl);
+                        const uint32_t off = sw128_chunk(r, (c0 >> 3) + half, CH);
+                        *reinterpret_cast<uint4 *>(phi + off) = vh;
+                        *reinterpret_cast<uint4 *>(plo + off) = vl;
+                    }
                 }
             }
         }
-        float *W = rec + ChunkRec::WW, *U = rec + ChunkRec::UT;
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                W[(r0 + m) * D + i0 + n] = w[m][n];
-                U[(r0 + m) * D + i0 + n] = u[m][n];
+    } else {
+        // exact per-element exponentials (chunks whose decay span is too wide)
+        for (int e = tid; e < CH * CH; e += 128) {
+            const int r = e / CH, s = e % CH;
+            float a = 0.f, pq = 0.f;
+            if (s <= r) {
+                for (int i = 0; i < D; ++i) {
+                    const float f = KH[s * D + i] * expf(GG[r * D + i] - GG[s * D + i]);
+                    a = fmaf(KH[r * D + i], f, a);
+                    pq = fmaf(QH[r * D + i], f, pq);
+                }
             }
+            A[r * CH + s] = s < r ? beta[r] * a : 0.f;
+            const float pv = s <= r ? pq : 0.f;
+            const __nv_bfloat16 ph = __float2bfloat16_rn(pv);
+            const __nv_bfloat16 pl = __float2bfloat16_rn(pv - __bfloat162float(ph));
+            const uint32_t off = sw128_offset(r, s, CH);
+            *reinterpret_cast<__nv_bfloat16 *>(phi + off) = ph;
+            *reinterpret_cast<__nv_bfloat16 *>(plo + off) = pl;
+        }
     }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(rec + Rec::P_HI, phi, 16384);
+        bulk_commit();
+    }
+    // ---- T = (I + A)^-1 (unit lower triangular), 16 x 16 blocks
+    float *T = reinterpret_cast<float *>(sm + is::T_F32);
+    float *XS = reinterpret_cast<float *>(sm + is::XS_F32);
+    for (int e = tid; e < CH * CH; e += 128) T[e] = 0.f;
+    __syncthreads();
+    if (lane < 16) {
+        const int b0 = warp * 16, c = b0 + lane;  // each lane reads only the column it writes
+        for (int r = b0; r < b0 + 16; ++r) {
+            float acc = (r == c) ? 1.f : 0.f;
+            for (int s = c; s < r; ++s) acc = fmaf(-A[r * CH + s], T[s * CH + c], acc);
+            T[r * CH + c] = (r >= c) ? acc : 0.f;
+        }
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {  // T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
+        const int nblk = 4 - d;
+        for (int e = tid; e < nblk * 256; e += 128) {
+            const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
+            float acc = 0.f;
+            for (int s = b * 16; s < a * 16; ++s) acc = fmaf(A[(a * 16 + r) * CH + s], T[s * CH + b * 16 + cc], acc);
+            XS[(a * 16 + r) * CH + b * 16 + cc] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < nblk * 256; e += 128) {
+            const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
+            float acc = 0.f;
+            for (int s = 0; s <= r; ++s) acc = fmaf(-T[(a * 16 + r) * CH + a * 16 + s], XS[(a * 16 + s) * CH + b * 16 + cc], acc);
+            T[(a * 16 + r) * CH + b * 16 + cc] = acc;
+        }
+        __syncthreads();
+    }
+    // ---- phase 3: W^T = (beta exp(G) . K)^T T^T and Ut^T = (beta V)^T T^T
+    build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, 128, [&](int r, int s0, float(&x)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = T[r * CH + s0 + e];
+    });
+    build_image(sm + is::AK_HI, sm + is::AK_LO, D, 8, tid, 128, [&](int i, int s0, float(&x)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * expf(GG[(s0 + e) * D + i]) * KH[(s0 + e) * D + i];
+    });
+    build_image(sm + is::AV_HI, sm + is::AV_LO, D, 8, tid, 128, [&](int j, int s0, float(&x)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * VV[(s0 + e) * D + j];
+    });
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        const uint32_t id = idesc_bf16_f32(128, CH);
+        mma3(tm + 64, sbase + is::AK_HI, sbase + is::AK_LO, sbase + is::T_HI, sbase + is::T_LO, D, CH, CH, id, false);
+        mma3(tm + 128, sbase + is::AV_HI, sbase + is::AV_LO, sbase + is::T_HI, sbase + is::T_LO, D, CH, CH, id, false);
+        mma_commit(bar);
+        bulk_wait_read();  // the Q / K^T / P staging may be overwritten now
+    }
+    __syncthreads();
+    // W image staging is zeroed by the drain below (every element written)
+    ok = __syncthreads_and(ok && mbar_wait(bar, phase, p.err));
+    tc_fence_after();
+    unsigned char *whi = sm + is::ST_W, *wlo = sm + is::ST_W + 16384;
+    const int i = warp * 32 + lane;  // TMEM lane: key channel i (W^T row) / value channel j (Ut^T row)
+    if (ok) {
+        float *UT = at<float>(rec, Rec::UT) + i * CH;
+        for (int c0 = 0; c0 < CH; c0 += 16) {
+            float v[16], u[16];
+            tmem_ld16(tm + (uint32_t(warp * 32) << 16) + 64 + c0, v);
+            tmem_ld16(tm + (uint32_t(warp * 32) << 16) + 128 + c0, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int r = c0 + e;
+                const __nv_bfloat16 wh = __float2bfloat16_rn(v[e]);
+                const __nv_bfloat16 wl = __float2bfloat16_rn(v[e] - __bfloat162float(wh));
+                const uint32_t off = sw128_offset(r, i, CH);
+                *reinterpret_cast<__nv_bfloat16 *>(whi + off) = wh;
+                *reinterpret_cast<__nv_bfloat16 *>(wlo + off) = wl;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4 *>(UT + c0 + e) = make_float4(u[e], u[e + 1], u[e + 2], u[e + 3]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(rec + Rec::W_HI, whi, 32768);
+        bulk_commit();
+        bulk_wait();
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
 }
 
-// ---------------------------------------------------------------- chain ---
-// One CTA per (sequence, head, d_v block of DB columns), sequential over the
-// sequence's chunks.  S block [128][DB] lives in shared memory.
-constexpr int LDS = DB + 1;
+// ============================================================== chain ====
+namespace cs {  // chain shared-memory map
+constexpr uint32_t A1_HI = 0, A1_LO = 32768;             // S^T images [128 j][128 i]
+constexpr uint32_t B1 = 65536;                            // W hi/lo, Q hi/lo images (64 KiB)
+constexpr uint32_t W_HI = B1, W_LO = B1 + 16384, Q_HI = B1 + 32768, Q_LO = B1 + 49152;
+constexpr uint32_t B2 = 131072;                           // K^T hi/lo, P hi/lo, gamma
+constexpr uint32_t KT_HI = B2, KT_LO = B2 + 16384, P_HI = B2 + 32768, P_LO = B2 + 40960, GAM = B2 + 49152;
+constexpr uint32_t A2_HI = 181248, A2_LO = 181248 + 16384;  // U^T images [128 j][64 r]
+constexpr uint32_t GCUR = A2_LO + 16384;                   // gamma of the current chunk
+constexpr uint32_t BARS = GCUR + 512;
+constexpr uint32_t BYTES = BARS + 512;
+}  // namespace cs
+static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
 
-__global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams p) {
-    extern __shared__ __align__(16) float sm[];
-    float *S = sm;                 // [128][LDS]
-    float *Wt = S + D * LDS;       // [64][LDK]  W
-    float *Qt = Wt + CH * LDK;     // [64][LDK]  exp(G) . q
-    float *Kt = Qt + CH * LDK;     // [64][LDK]  exp(G_last - G) . k
-    float *P = Kt + CH * LDK;      // [64][LDC]
-    float *U = P + CH * LDC;       // [64][LDS]
-    float *gam = U + CH * LDS;     // [128]  exp(G_last)
-    const int tid = threadIdx.x;
-    const int jb = blockIdx.x % NB, h = (blockIdx.x / NB) % p.H, n = blockIdx.x / (NB * p.H);
+// TMEM columns: (W S)^T [0,64), O^T [64,128), (K^T U)^T [128,256), S^T [256,384)
+__global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar_b1 = reinterpret_cast<uint64_t *>(sm + cs::BARS);
+    uint64_t *bar_b2 = bar_b1 + 1, *bar_m1 = bar_b1 + 2, *bar_m2 = bar_b1 + 3;
+    uint32_t *tbase = reinterpret_cast<uint32_t *>(bar_b1 + 4);
+    float *gcur = reinterpret_cast<float *>(sm + cs::GCUR);
+    const int tid = threadIdx.x, warp = tid >> 5, j = tid;  // j: value channel = TMEM lane
+    const int h = blockIdx.x % p.H, n = blockIdx.x / p.H;
     const SeqMeta sq = p.seqs[n];
     const size_t head_elems = size_t(D) * D;
-    float *slot_state = p.states + size_t(sq.slot) * p.H * head_elems + size_t(h) * head_elems;  // [j][i]
-    for (int e = tid; e < D * DB; e += 256) {
-        const int j = e / D, i = e - j * D;  // coalesced over i
-        S[i * LDS + j] = sq.has_init ? slot_state[size_t(jb * DB + j) * D + i] : 0.f;
+    float *slot_state = p.states + size_t(sq.slot) * p.H * head_elems + size_t(h) * head_elems;  // S^T [j][i]
+    const uint32_t sbase = smem_u32(sm);
+    if (tid == 0) {
+        for (int b = 0; b < 4; ++b) mbar_init(bar_b1 + b, 1);
+        fence_mbar_init();
     }
+    if (warp == 0) tmem_alloc(tbase, 512);
+    tc_fence_before();
     __syncthreads();
-    for (int c = 0; c < sq.n_chunks; ++c) {
+    tc_fence_after();
+    const uint32_t tm = *tbase, tl = tm + (uint32_t(warp * 32) << 16);
+    if (tid == 0 && sq.n_chunks > 0) {
+        const char *r0 = rec_ptr(p, sq.chunk0, h);
+        mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
+        bulk_load(sm + cs::B1, r0 + Rec::W_HI, Rec::B1_BYTES, bar_b1);
+        mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
+        bulk_load(sm + cs::B2, r0 + Rec::KT_HI, Rec::B2_BYTES, bar_b2);
+    }
+    // S^T row j: fp32 into TMEM, hi/lo into the A1 images
+    for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            const float4 x = sq.has_init ? ld4(slot_state + size_t(j) * D + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
+        }
+        tmem_st16(tl + 256 + c0, v);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = v[8 * half + e];
+            uint4 vh, vl;
+            split8(x, vh, vl);
+            const uint32_t off = sw128_chunk(j, (c0 >> 3) + half, D);
+            *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
+            *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
+        }
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    bool ok = true;
+    const uint32_t id64 = idesc_bf16_f32(128, CH), id128 = idesc_bf16_f32(128, D);
+    for (int c = 0; c < sq.n_chunks && ok; ++c) {
         const int g = sq.chunk0 + c;
-        float *rec = rec_ptr(p, g, h);
-        const float *GG = rec + ChunkRec::GG;
-        for (int e = tid; e < CH * D; e += 256) {
-            const int r = e / D, i = e - r * D;
-            const float gl = GG[(CH - 1) * D + i], gr = GG[e];
-            Wt[r * LDK + i] = rec[ChunkRec::WW + e];
-            Qt[r * LDK + i] = expf(gr) * rec[ChunkRec::QH + e];
-            Kt[r * LDK + i] = expf(gl - gr) * rec[ChunkRec::KH + e];
+        char *rec = rec_ptr(p, g, h);
+        const uint32_t par = uint32_t(c & 1);
+        ok = __syncthreads_and(mbar_wait(bar_b1, par, p.err));
+        if (!ok) break;
+        if (tid == 0) {
+            tc_fence_after();
+            mma3(tm + 0, sbase + cs::A1_HI, sbase + cs::A1_LO, sbase + cs::W_HI, sbase + cs::W_LO, D, CH, D, id64, false);
+            mma3(tm + 64, sbase + cs::A1_HI, sbase + cs::A1_LO, sbase + cs::Q_HI, sbase + cs::Q_LO, D, CH, D, id64, false);
+            mma_commit(bar_m1);
         }
-        for (int e = tid; e < CH * CH; e += 256) P[(e / CH) * LDC + (e % CH)] = rec[ChunkRec::PP + e];
-        if (tid < D) gam[tid] = expf(GG[(CH - 1) * D + tid]);
-        __syncthreads();
-        // U = Ut - W S   (64 x DB, 8 outputs per thread)
-        {
-            const int r = tid >> 2, j0 = (tid & 3) * (DB / 4);
-            float acc[DB / 4];
+        // Ut^T row j while the MMAs run
+        float ut[CH];
+        const float *UTg = reinterpret_cast<const float *>(rec + Rec::UT) + size_t(j) * CH;
 #pragma unroll
-            for (int m = 0; m < DB / 4; ++m) acc[m] = rec[ChunkRec::UT + r * D + jb * DB + j0 + m];
-            for (int i = 0; i < D; ++i) {
-                const float wv = Wt[r * LDK + i];
-#pragma unroll
-                for (int m = 0; m < DB / 4; ++m) acc[m] = fmaf(-wv, S[i * LDS + j0 + m], acc[m]);
-            }
-#pragma unroll
-            for (int m = 0; m < DB / 4; ++m) U[r * LDS + j0 + m] = acc[m];
+        for (int e = 0; e < CH; e += 4) {
+            const float4 x = ld4(UTg + e);
+            ut[e] = x.x; ut[e + 1] = x.y; ut[e + 2] = x.z; ut[e + 3] = x.w;
         }
-        __syncthreads();
-        // O = Qt S + P U  -> workspace
-        {
-            const int r = tid >> 2, j0 = (tid & 3) * (DB / 4);
-            float acc[DB / 4] = {};
-            for (int i = 0; i < D; ++i) {
-                const float qv = Qt[r * LDK + i];
-#pragma unroll
-                for (int m = 0; m < DB / 4; ++m) acc[m] = fmaf(qv, S[i * LDS + j0 + m], acc[m]);
-            }
-            for (int s = 0; s <= r; ++s) {
-                const float pv = P[r * LDC + s];
-#pragma unroll
-                for (int m = 0; m < DB / 4; ++m) acc[m] = fmaf(pv, U[s * LDS + j0 + m], acc[m]);
-            }
-            float *O = rec + ChunkRec::OO;
-#pragma unroll
-            for (int m = 0; m < DB / 4; ++m) O[r * D + jb * DB + j0 + m] = acc[m];
+        ok = __syncthreads_and(mbar_wait(bar_m1, par, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && c + 1 < sq.n_chunks) {  // W and Q images are consumed: stream in the next chunk's
+            mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
+            bulk_load(sm + cs::B1, rec_ptr(p, g + 1, h) + Rec::W_HI, Rec::B1_BYTES, bar_b1);
         }
-        __syncthreads();
-        // S <- Diag(gamma) S + Kt^T U   (128 x DB, 16 outputs per thread)
-        {
-            const int i = tid >> 1, j0 = (tid & 1) * (DB / 2);
-            float acc[DB / 2];
+        // U^T row j = Ut^T - (W S)^T  -> hi/lo images
+        for (int c0 = 0; c0 < CH; c0 += 16) {
+            float v[16];
+            tmem_ld16(tl + c0, v);
+            tmem_wait_ld();
 #pragma unroll
-            for (int m = 0; m < DB / 2; ++m) acc[m] = gam[i] * S[i * LDS + j0 + m];
-            for (int s = 0; s < CH; ++s) {
-                const float kv = Kt[s * LDK + i];
+            for (int half = 0; half < 2; ++half) {
+                float x[8];
 #pragma unroll
-                for (int m = 0; m < DB / 2; ++m) acc[m] = fmaf(kv, U[s * LDS + j0 + m], acc[m]);
+                for (int e = 0; e < 8; ++e) x[e] = ut[c0 + 8 * half + e] - v[8 * half + e];
+                uint4 vh, vl;
+                split8(x, vh, vl);
+                const uint32_t off = sw128_chunk(j, (c0 >> 3) + half, D);
+                *reinterpret_cast<uint4 *>(sm + cs::A2_HI + off) = vh;
+                *reinterpret_cast<uint4 *>(sm + cs::A2_LO + off) = vl;
             }
-#pragma unroll
-            for (int m = 0; m < DB / 2; ++m) S[i * LDS + j0 + m] = acc[m];
         }
+        ok = __syncthreads_and(mbar_wait(bar_b2, par, p.err));
+        if (!ok) break;
+        gcur[j] = reinterpret_cast<const float *>(sm + cs::GAM)[j];
+        fence_proxy_async_smem();
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            mma3(tm + 128, sbase + cs::A2_HI, sbase + cs::A2_LO, sbase + cs::KT_HI, sbase + cs::KT_LO, D, D, CH, id128,
+                 false);
+            mma3(tm + 64, sbase + cs::A2_HI, sbase + cs::A2_LO, sbase + cs::P_HI, sbase + cs::P_LO, D, CH, CH, id64,
+                 true);
+            mma_commit(bar_m2);
+        }
+        ok = __syncthreads_and(mbar_wait(bar_m2, par, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && c + 1 < sq.n_chunks) {  // K^T, P images and gamma consumed
+            mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
+            bulk_load(sm + cs::B2, rec_ptr(p, g + 1, h) + Rec::KT_HI, Rec::B2_BYTES, bar_b2);
+        }
+        // O column j -> record (rows r), coalesced across the warp
+        float *O = reinterpret_cast<float *>(rec + Rec::OO);
+        for (int c0 = 0; c0 < CH; c0 += 16) {
+            float v[16];
+            tmem_ld16(tl + 64 + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) O[(c0 + e) * D + j] = v[e];
+        }
+        // S^T row j <- gamma . S^T row j + (K^T U)^T row j; refresh the A1 images
         const ChunkMeta cm = p.chunks[g];
-        for (int q = 0; q < cm.ck_count; ++q) {
-            const CkptMeta ck = p.ckpts[cm.ck_begin + q];
-            float *dst = p.states + size_t(ck.dst_slot) * p.H * head_elems + size_t(h) * head_elems;
-            for (int e = tid; e < D * DB; e += 256) {
-                const int j = e / D, i = e - j * D;
-                dst[size_t(jb * DB + j) * D + i] = S[i * LDS + j];
+        for (int c0 = 0; c0 < D; c0 += 16) {
+            float s[16], ds[16];
+            tmem_ld16(tl + 256 + c0, s);
+            tmem_ld16(tl + 128 + c0, ds);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) s[e] = fmaf(gcur[c0 + e], s[e], ds[e]);
+            tmem_st16(tl + 256 + c0, s);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = s[8 * half + e];
+                uint4 vh, vl;
+                split8(x, vh, vl);
+                const uint32_t off = sw128_chunk(j, (c0 >> 3) + half, D);
+                *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
+                *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
+            }
+            for (int q = 0; q < cm.ck_count; ++q) {
+                const CkptMeta ck = p.ckpts[cm.ck_begin + q];
+                float *dst = p.states + size_t(ck.dst_slot) * p.H * head_elems + size_t(h) * head_elems + size_t(j) * D + c0;
+#pragma unroll
+                for (int e = 0; e < 16; e += 4)
+                    *reinterpret_cast<float4 *>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
             }
         }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
-    for (int e = tid; e < D * DB; e += 256) {
-        const int j = e / D, i = e - j * D;
-        slot_state[size_t(jb * DB + j) * D + i] = S[i * LDS + j];
+    // end state S^T row j -> slot
+    if (ok) {
+        for (int c0 = 0; c0 < D; c0 += 16) {
+            float s[16];
+            tmem_ld16(tl + 256 + c0, s);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4 *>(slot_state + size_t(j) * D + c0 + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+        }
     }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-// ---------------------------------------------------------------- out -----
+// ================================================================ out ====
 template <typename Act>
 __global__ void __launch_bounds__(128) prefill_out_kernel(const PrefillParams p) {
     const int g = blockIdx.x, h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const ChunkMeta cm = p.chunks[g];
-    const float *O = rec_ptr(p, g, h) + ChunkRec::OO;
+    const float *O = reinterpret_cast<const float *>(rec_ptr(p, g, h) + Rec::OO);
     const Act *gate = static_cast<const Act *>(p.gate);
     const Act *nw = static_cast<const Act *>(p.norm_w);
     Act *out = static_cast<Act *>(p.out);
     const size_t HD = size_t(p.H) * D;
     for (int t = warp; t < cm.len; t += 4) {
-        float o[4], ss = 0.f;
+        const float4 o4 = ld4(O + t * D + lane * 4);
+        const float o[4] = {o4.x, o4.y, o4.z, o4.w};
+        float ss = 0.f;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            o[m] = O[t * D + lane * 4 + m];
-            ss = fmaf(o[m], o[m], ss);
-        }
+        for (int m = 0; m < 4; ++m) ss = fmaf(o[m], o[m], ss);
         for (int s = 16; s; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
         const float r = rsqrtf(ss * (1.0f / D) + p.eps_rms);
         const size_t base = size_t(cm.row0 + t) * HD + size_t(h) * D + lane * 4;
@@ -447,7 +730,7 @@ __global__ void __launch_bounds__(128) prefill_out_kernel(const PrefillParams p)
     }
 }
 
-// ---------------------------------------------------------------- tails ---
+// ============================================================== tails ====
 // Conv tail after `pos` tokens of a segment: raw inputs at pos-3 .. pos-1
 // (before the segment: the slot's old tail, or zeros for a new sequence).
 // One block per checkpoint request when ckpt_pass, else per sequence; the
@@ -474,15 +757,16 @@ __global__ void __launch_bounds__(256) prefill_tails_kernel(const PrefillParams 
         const int s = ch / HD, rem = ch - s * HD;
         const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
         Act x[3];
-        for (int j = 0; j < 3; ++j) {
-            const int q = pos - 3 + j;
-            if (q >= 0) x[j] = src[size_t(sq.row0 + q) * HD + rem];
-            else x[j] = sq.has_init ? old[size_t(3 + q) * p.n_ch + ch] : from_f32<Act>(0.f);
+        for (int jj = 0; jj < 3; ++jj) {
+            const int q = pos - 3 + jj;
+            if (q >= 0) x[jj] = src[size_t(sq.row0 + q) * HD + rem];
+            else x[jj] = sq.has_init ? old[size_t(3 + q) * p.n_ch + ch] : from_f32<Act>(0.f);
         }
-        for (int j = 0; j < 3; ++j) nt[size_t(j) * p.n_ch + ch] = x[j];
+        for (int jj = 0; jj < 3; ++jj) nt[size_t(jj) * p.n_ch + ch] = x[jj];
     }
 }
 
+// ================================================================ host ===
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
@@ -494,8 +778,8 @@ WsLayout ws_layout(int N, long long n_chunks, long long n_reqs, int H) {
     L.seqs = 0;
     L.chunks = align256(L.seqs + sizeof(SeqMeta) * size_t(N));
     L.ckpts = align256(L.chunks + sizeof(ChunkMeta) * size_t(n_chunks));
-    L.rec = align256(L.ckpts + sizeof(CkptMeta) * size_t(std::max<long long>(n_reqs, 1)));
-    L.total = align256(L.rec + sizeof(float) * ChunkRec::FLOATS * size_t(n_chunks) * size_t(H));
+    L.rec = (L.ckpts + sizeof(CkptMeta) * size_t(std::max<long long>(n_reqs, 1)) + 1023) / 1024 * 1024;
+    L.total = L.rec + Rec::BYTES * size_t(n_chunks) * size_t(H);
     return L;
 }
 
@@ -505,6 +789,36 @@ long long count_chunks(const int32_t *cu, int N) {
     return n;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Tensor map over a token-major [n_tok][H][128] activation tensor; the box
+// is one head's 128 channels x `rows` tokens.
+bool make_map(CUtensorMap *m, const void *base, int n_tok, int H, int esize, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(H), cuuint64_t(n_tok)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * esize, cuuint64_t(H) * D * esize};
+    const cuuint32_t box[3] = {cuuint32_t(D), 1u, cuuint32_t(rows)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <typename K>
 kda_status set_smem(K kern, size_t bytes) {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) == cudaSuccess
@@ -512,22 +826,31 @@ kda_status set_smem(K kern, size_t bytes) {
                : KDA_ERR_CUDA;
 }
 
-constexpr size_t kPrepSmem = sizeof(float) * (2 * CH * D + 2 * CH);
-constexpr size_t kIntraSmem = sizeof(float) * (3 * CH * LDK + 3 * CH * LDC + D + CH + 4);
-constexpr size_t kChainSmem = sizeof(float) * (D * LDS + 3 * CH * LDK + CH * LDC + CH * LDS + D);
+template <typename Act>
+constexpr size_t prep_smem() {
+    return 1024 + 3 * size_t(CH + HALO) * D * sizeof(Act) + size_t(CH) * D * sizeof(Act);
+}
+constexpr size_t kIntraSmem = 1024 + is::BYTES;
+constexpr size_t kChainSmem = 1024 + cs::BYTES;
 
 template <typename Act>
-kda_status launch_act(const PrefillParams &p, int N, long long n_chunks, int n_reqs, cudaStream_t stream) {
+kda_status launch_act(const PrefillParams &p, const kda_io *io, int n_tok, int N, long long n_chunks, int n_reqs,
+                      cudaStream_t stream) {
     kda_status st;
-    if ((st = set_smem(prefill_prep_kernel<Act>, kPrepSmem)) != KDA_OK) return st;
+    if ((st = set_smem(prefill_prep_kernel<Act>, prep_smem<Act>())) != KDA_OK) return st;
     if ((st = set_smem(prefill_intra_kernel, kIntraSmem)) != KDA_OK) return st;
     if ((st = set_smem(prefill_chain_kernel, kChainSmem)) != KDA_OK) return st;
     if (n_chunks > 0) {
+        CUtensorMap mq, mk, mv, ma;
+        const int es = int(sizeof(Act));
+        if (!make_map(&mq, io->q, n_tok, p.H, es, CH + HALO) || !make_map(&mk, io->k, n_tok, p.H, es, CH + HALO) ||
+            !make_map(&mv, io->v, n_tok, p.H, es, CH + HALO) || !make_map(&ma, io->alpha, n_tok, p.H, es, CH))
+            return KDA_ERR_CUDA;
         const dim3 grid(unsigned(n_chunks), unsigned(p.H));
-        prefill_prep_kernel<Act><<<grid, D, kPrepSmem, stream>>>(p);
-        prefill_intra_kernel<<<grid, 256, kIntraSmem, stream>>>(p);
+        prefill_prep_kernel<Act><<<grid, 128, prep_smem<Act>(), stream>>>(p, mq, mk, mv, ma);
+        prefill_intra_kernel<<<grid, 128, kIntraSmem, stream>>>(p);
     }
-    prefill_chain_kernel<<<unsigned(N) * p.H * NB, 256, kChainSmem, stream>>>(p);
+    prefill_chain_kernel<<<unsigned(N) * p.H, 128, kChainSmem, stream>>>(p);
     if (n_chunks > 0) prefill_out_kernel<Act><<<dim3(unsigned(n_chunks), unsigned(p.H)), 128, 0, stream>>>(p);
     if (n_reqs > 0) prefill_tails_kernel<Act><<<n_reqs, 256, 0, stream>>>(p, 1);
     prefill_tails_kernel<Act><<<N, 256, 0, stream>>>(p, 0);
@@ -597,7 +920,7 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
     p.seqs = reinterpret_cast<const SeqMeta *>(ws + L.seqs);
     p.chunks = reinterpret_cast<const ChunkMeta *>(ws + L.chunks);
     p.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.ckpts);
-    p.rec = reinterpret_cast<float *>(ws + L.rec);
+    p.rec = ws + L.rec;
     p.states = pool->states;
     p.tails = pool->tails;
     p.err = pool->err;
@@ -617,8 +940,9 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
     p.n_ckpts = n_reqs;
     p.eps_l2 = w->eps_l2;
     p.eps_rms = w->eps_rms;
-    if (pool->desc.act == KDA_BF16) return launch_act<__nv_bfloat16>(p, N, n_chunks, n_reqs, stream);
-    return launch_act<float>(p, N, n_chunks, n_reqs, stream);
+    const int n_tok = cu_seqlens[N];
+    if (pool->desc.act == KDA_BF16) return launch_act<__nv_bfloat16>(p, io, n_tok, N, n_chunks, n_reqs, stream);
+    return launch_act<float>(p, io, n_tok, N, n_chunks, n_reqs, stream);
 }
 
 // ------------------------------------------------------ no-allocation entry --
