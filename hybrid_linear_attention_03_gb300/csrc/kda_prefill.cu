@@ -240,16 +240,19 @@ __global__ void __launch_bounds__(128) prefill_prep_kernel(const PrefillParams p
 
 // ============================================================== intra ====
 namespace is {  // intra shared-memory map (bytes from a 1 KiB-aligned base)
-constexpr uint32_t X_HI = 0, X_LO = 32768, KB_HI = 65536, KB_LO = 81920;           // phase 1
-constexpr uint32_t A_F32 = 0, XS_F32 = 16384, T_F32 = 81920;                        // inverse
+constexpr uint32_t X_HI = 0, X_LO = 32768, KB_HI = 65536, KB_LO = 81920;           // phase 1 images
+constexpr uint32_t A_F32 = 0, XS_F32 = 16384, T_F32 = 81920;                        // inverse (fp32)
 constexpr uint32_t T_HI = 0, T_LO = 8192, AK_HI = 16384, AK_LO = 32768, AV_HI = 49152, AV_LO = 65536;  // phase 3
-constexpr uint32_t ST_Q = 98304, ST_KT = 131072, ST_P = 163840;  // staging of images for bulk stores
-constexpr uint32_t ST_W = 98304;
-constexpr uint32_t SMALL = 180224;
+constexpr uint32_t IN0 = 98304;   // QH, then VV, then the W image staging (32 KiB)
+constexpr uint32_t KH = 131072;   // fp32 [64][128]
+constexpr uint32_t GG = 163840;   // fp32 [64][128]
+constexpr uint32_t SMALL = 196608;
 constexpr uint32_t BYTES = SMALL + 2048;
+constexpr int NT = 256;
 }  // namespace is
 
-// Fills `rows` x (8 * chunks_per_row) elements of an image pair with f(row, k0, out8).
+// Fills `rows` x (8 * chunks_per_row) elements of an image pair with f(row, k0, out8),
+// storing 16-byte chunks at their swizzled offsets (shared or global memory).
 template <typename F>
 __device__ __forceinline__ void build_image(unsigned char *hi, unsigned char *lo, int rows, int chunks_per_row,
                                             int tid, int nthreads, F f) {
@@ -261,7 +264,7 @@ __device__ __forceinline__ void build_image(unsigned char *hi, unsigned char *lo
         split8(x, vh, vl);
         const uint32_t off = sw128_chunk(r, c, rows);
         *reinterpret_cast<uint4 *>(hi + off) = vh;
-        if (lo) *reinterpret_cast<uint4 *>(lo + off) = vl;
+        *reinterpret_cast<uint4 *>(lo + off) = vl;
     }
 }
 
@@ -281,51 +284,65 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
     }
 }
 
-__global__ void __launch_bounds__(128) prefill_intra_kernel(const PrefillParams p) {
+// One CTA (8 warps) per (chunk, head).  The prep record's q, k and G arrive
+// by TMA bulk copies (v follows once q is consumed), so every operand build
+// reads shared memory.  Images the chain needs that involve no MMA (exp(G).q,
+// (exp(G_last - G).k)^T, P) go straight to the record from registers; the W
+// image is staged and bulk-stored.
+__global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *cref = reinterpret_cast<float *>(sm + is::SMALL);  // [128]
     float *beta = cref + D;                                    // [64]
     int *flag = reinterpret_cast<int *>(beta + CH);            // [1]
     uint32_t *tbase = reinterpret_cast<uint32_t *>(flag + 1);  // [1]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + is::SMALL + 1024);  // [1]
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + is::SMALL + 1024);
+    uint64_t *bar_mma = bar_ld + 1;
+    const float *QHs = reinterpret_cast<const float *>(sm + is::IN0);
+    const float *VVs = reinterpret_cast<const float *>(sm + is::IN0);
+    const float *KHs = reinterpret_cast<const float *>(sm + is::KH);
+    const float *GGs = reinterpret_cast<const float *>(sm + is::GG);
     const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     char *rec = rec_ptr(p, g, h);
-    const float *QH = at<float>(rec, Rec::QH), *KH = at<float>(rec, Rec::KH), *VV = at<float>(rec, Rec::VV),
-                *GG = at<float>(rec, Rec::GG);
     const uint32_t sbase = smem_u32(sm);
     if (tid == 0) {
         *flag = 0;
-        mbar_init(bar, 1);
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
         fence_mbar_init();
+        mbar_arrive_expect_tx(bar_ld, 3 * 32768 + CH * 4);
+        bulk_load(sm + is::IN0, rec + Rec::QH, 32768, bar_ld);
+        bulk_load(sm + is::KH, rec + Rec::KH, 32768, bar_ld);
+        bulk_load(sm + is::GG, rec + Rec::GG, 32768, bar_ld);
+        bulk_load(beta, rec + Rec::BB, CH * 4, bar_ld);
     }
     if (warp == 0) tmem_alloc(tbase, 256);
-    if (tid < CH) beta[tid] = at<float>(rec, Rec::BB)[tid];
-    {
-        const float g0 = GG[tid], gl = GG[(CH - 1) * D + tid];
-        cref[tid] = 0.5f * (g0 + gl);
-        at<float>(rec, Rec::GAM)[tid] = expf(gl);
-        if (g0 - gl > kSafeSpan) atomicOr(flag, 1);
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tbase;
+    bool ok = __syncthreads_and(mbar_wait(bar_ld, 0, p.err));
+    uint32_t mma_phase = 0;
+    if (ok && tid < D) {
+        const float g0 = GGs[tid], gl = GGs[(CH - 1) * D + tid];
+        cref[tid] = 0.5f * (g0 + gl);
+        at<float>(rec, Rec::GAM)[tid] = expf(gl);
+        if (g0 - gl > kSafeSpan) atomicOr(flag, 1);
+    }
+    __syncthreads();
     const bool exact = *flag != 0;
-    bool ok = true;
-    uint32_t phase = 0;
 
     // ---- phase 1: X = [K exp(G - c); Q exp(G - c)], Kb = K exp(c - G) -> A, P
-    if (!exact) {
-        build_image(sm + is::X_HI, sm + is::X_LO, 128, 16, tid, 128, [&](int r, int k0, float(&x)[8]) {
-            const float *src = r < CH ? KH + r * D : QH + (r - CH) * D;
-            const float *gg = GG + (r & (CH - 1)) * D;
+    if (ok && !exact) {
+        build_image(sm + is::X_HI, sm + is::X_LO, 128, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
+            const float *src = r < CH ? KHs + r * D : QHs + (r - CH) * D;
+            const float *gg = GGs + (r & (CH - 1)) * D;
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = src[k0 + e] * expf(gg[k0 + e] - cref[k0 + e]);
         });
-        build_image(sm + is::KB_HI, sm + is::KB_LO, CH, 16, tid, 128, [&](int r, int k0, float(&x)[8]) {
+        build_image(sm + is::KB_HI, sm + is::KB_LO, CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = KH[r * D + k0 + e] * expf(cref[k0 + e] - GG[r * D + k0 + e]);
+            for (int e = 0; e < 8; ++e) x[e] = KHs[r * D + k0 + e] * expf(cref[k0 + e] - GGs[r * D + k0 + e]);
         });
         fence_proxy_async_smem();
         tc_fence_before();
@@ -334,38 +351,39 @@ __global__ void __launch_bounds__(128) prefill_intra_kernel(const PrefillParams 
         if (tid == 0) {
             mma3(tm, sbase + is::X_HI, sbase + is::X_LO, sbase + is::KB_HI, sbase + is::KB_LO, 128, CH, D,
                  idesc_bf16_f32(128, CH), false);
-            mma_commit(bar);
+            mma_commit(bar_mma);
         }
     }
     // chain images that need no MMA: exp(G) . q (rows r) and (exp(G_last - G) . k)^T (rows i)
-    build_image(sm + is::ST_Q, sm + is::ST_Q + 16384, CH, 16, tid, 128, [&](int r, int k0, float(&x)[8]) {
+    if (ok) {
+        build_image(reinterpret_cast<unsigned char *>(rec + Rec::Q_HI), reinterpret_cast<unsigned char *>(rec + Rec::Q_LO),
+                    CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = QH[r * D + k0 + e] * expf(GG[r * D + k0 + e]);
-    });
-    build_image(sm + is::ST_KT, sm + is::ST_KT + 16384, D, 8, tid, 128, [&](int i, int r0, float(&x)[8]) {
-        const float gl = GG[(CH - 1) * D + i];
+                        for (int e = 0; e < 8; ++e) x[e] = QHs[r * D + k0 + e] * expf(GGs[r * D + k0 + e]);
+                    });
+        build_image(reinterpret_cast<unsigned char *>(rec + Rec::KT_HI),
+                    reinterpret_cast<unsigned char *>(rec + Rec::KT_LO), D, 8, tid, is::NT,
+                    [&](int i, int r0, float(&x)[8]) {
+                        const float gl = GGs[(CH - 1) * D + i];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = KH[(r0 + e) * D + i] * expf(gl - GG[(r0 + e) * D + i]);
-    });
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_store(rec + Rec::Q_HI, sm + is::ST_Q, 32768);
-        bulk_store(rec + Rec::KT_HI, sm + is::ST_KT, 32768);
-        bulk_commit();
+                        for (int e = 0; e < 8; ++e) x[e] = KHs[(r0 + e) * D + i] * expf(gl - GGs[(r0 + e) * D + i]);
+                    });
     }
-    // ---- A (s < r, times beta_r) -> fp32, P (s <= r) -> images
+    __syncthreads();
+    // ---- A (s < r, times beta_r) -> fp32 smem, P (s <= r) -> record images
     float *A = reinterpret_cast<float *>(sm + is::A_F32);
-    unsigned char *phi = sm + is::ST_P, *plo = sm + is::ST_P + 8192;
+    unsigned char *phi = reinterpret_cast<unsigned char *>(rec + Rec::P_HI);
+    unsigned char *plo = reinterpret_cast<unsigned char *>(rec + Rec::P_LO);
     if (!exact) {
-        ok = __syncthreads_and(mbar_wait(bar, phase, p.err));
-        phase ^= 1;
+        ok = __syncthreads_and(ok && mbar_wait(bar_mma, mma_phase, p.err));
+        mma_phase ^= 1;
         tc_fence_after();
-        const int m = warp * 32 + lane;  // TMEM lane = row of X
+        const int m = (warp & 3) * 32 + lane;  // TMEM lane = row of X; warps w and w+4 split the columns
+        const int cbase = (warp >> 2) * 32;
         if (ok) {
-            for (int c0 = 0; c0 < CH; c0 += 16) {
+            for (int c0 = cbase; c0 < cbase + 32; c0 += 16) {
                 float v[16];
-                tmem_ld16(tm + (uint32_t(warp * 32) << 16) + c0, v);
+                tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + c0, v);
                 tmem_wait_ld();
                 if (m < CH) {
 #pragma unroll
@@ -386,16 +404,16 @@ __global__ void __launch_bounds__(128) prefill_intra_kernel(const PrefillParams 
                 }
             }
         }
-    } else {
+    } else if (ok) {
         // exact per-element exponentials (chunks whose decay span is too wide)
-        for (int e = tid; e < CH * CH; e += 128) {
+        for (int e = tid; e < CH * CH; e += is::NT) {
             const int r = e / CH, s = e % CH;
             float a = 0.f, pq = 0.f;
             if (s <= r) {
                 for (int i = 0; i < D; ++i) {
-                    const float f = KH[s * D + i] * expf(GG[r * D + i] - GG[s * D + i]);
-                    a = fmaf(KH[r * D + i], f, a);
-                    pq = fmaf(QH[r * D + i], f, pq);
+                    const float f = KHs[s * D + i] * expf(GGs[r * D + i] - GGs[s * D + i]);
+                    a = fmaf(KHs[r * D + i], f, a);
+                    pq = fmaf(QHs[r * D + i], f, pq);
                 }
             }
             A[r * CH + s] = s < r ? beta[r] * a : 0.f;
@@ -407,19 +425,18 @@ __global__ void __launch_bounds__(128) prefill_intra_kernel(const PrefillParams 
             *reinterpret_cast<__nv_bfloat16 *>(plo + off) = pl;
         }
     }
-    fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_store(rec + Rec::P_HI, phi, 16384);
-        bulk_commit();
+    __syncthreads();  // q is consumed (the exact path reads it for P): v takes its place
+    if (tid == 0 && ok) {
+        mbar_arrive_expect_tx(bar_ld, 32768);
+        bulk_load(sm + is::IN0, rec + Rec::VV, 32768, bar_ld);
     }
     // ---- T = (I + A)^-1 (unit lower triangular), 16 x 16 blocks
     float *T = reinterpret_cast<float *>(sm + is::T_F32);
     float *XS = reinterpret_cast<float *>(sm + is::XS_F32);
-    for (int e = tid; e < CH * CH; e += 128) T[e] = 0.f;
+    for (int e = tid; e < CH * CH; e += is::NT) T[e] = 0.f;
     __syncthreads();
-    if (lane < 16) {
+    if (warp < 4 && lane < 16) {
         const int b0 = warp * 16, c = b0 + lane;  // each lane reads only the column it writes
         for (int r = b0; r < b0 + 16; ++r) {
             float acc = (r == c) ? 1.f : 0.f;
@@ -430,14 +447,14 @@ __global__ void __launch_bounds__(128) prefill_intra_kernel(const PrefillParams 
     __syncthreads();
     for (int d = 1; d < 4; ++d) {  // T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
         const int nblk = 4 - d;
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += is::NT) {
             const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
             float acc = 0.f;
             for (int s = b * 16; s < a * 16; ++s) acc = fmaf(A[(a * 16 + r) * CH + s], T[s * CH + b * 16 + cc], acc);
             XS[(a * 16 + r) * CH + b * 16 + cc] = acc;
         }
         __syncthreads();
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += is::NT) {
             const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
             float acc = 0.f;
             for (int s = 0; s <= r; ++s) acc = fmaf(-T[(a * 16 + r) * CH + a * 16 + s], XS[(a * 16 + s) * CH + b * 16 + cc], acc);
@@ -446,41 +463,42 @@ __global__ void __launch_bounds__(128) prefill_intra_kernel(const PrefillParams 
         __syncthreads();
     }
     // ---- phase 3: W^T = (beta exp(G) . K)^T T^T and Ut^T = (beta V)^T T^T
-    build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, 128, [&](int r, int s0, float(&x)[8]) {
+    ok = __syncthreads_and(ok && mbar_wait(bar_ld, 1, p.err));  // v has arrived
+    if (ok) {
+        build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, is::NT, [&](int r, int s0, float(&x)[8]) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = T[r * CH + s0 + e];
-    });
-    build_image(sm + is::AK_HI, sm + is::AK_LO, D, 8, tid, 128, [&](int i, int s0, float(&x)[8]) {
+            for (int e = 0; e < 8; ++e) x[e] = T[r * CH + s0 + e];
+        });
+        build_image(sm + is::AK_HI, sm + is::AK_LO, D, 8, tid, is::NT, [&](int i, int s0, float(&x)[8]) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * expf(GG[(s0 + e) * D + i]) * KH[(s0 + e) * D + i];
-    });
-    build_image(sm + is::AV_HI, sm + is::AV_LO, D, 8, tid, 128, [&](int j, int s0, float(&x)[8]) {
+            for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * expf(GGs[(s0 + e) * D + i]) * KHs[(s0 + e) * D + i];
+        });
+        build_image(sm + is::AV_HI, sm + is::AV_LO, D, 8, tid, is::NT, [&](int j, int s0, float(&x)[8]) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * VV[(s0 + e) * D + j];
-    });
+            for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * VVs[(s0 + e) * D + j];
+        });
+    }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // v is consumed: the W image staging takes its place
     tc_fence_after();
-    if (tid == 0) {
+    if (tid == 0 && ok) {
         const uint32_t id = idesc_bf16_f32(128, CH);
         mma3(tm + 64, sbase + is::AK_HI, sbase + is::AK_LO, sbase + is::T_HI, sbase + is::T_LO, D, CH, CH, id, false);
         mma3(tm + 128, sbase + is::AV_HI, sbase + is::AV_LO, sbase + is::T_HI, sbase + is::T_LO, D, CH, CH, id, false);
-        mma_commit(bar);
-        bulk_wait_read();  // the Q / K^T / P staging may be overwritten now
+        mma_commit(bar_mma);
     }
-    __syncthreads();
-    // W image staging is zeroed by the drain below (every element written)
-    ok = __syncthreads_and(ok && mbar_wait(bar, phase, p.err));
+    ok = __syncthreads_and(ok && mbar_wait(bar_mma, mma_phase, p.err));
     tc_fence_after();
-    unsigned char *whi = sm + is::ST_W, *wlo = sm + is::ST_W + 16384;
-    const int i = warp * 32 + lane;  // TMEM lane: key channel i (W^T row) / value channel j (Ut^T row)
+    unsigned char *whi = sm + is::IN0, *wlo = sm + is::IN0 + 16384;
+    const int i = (warp & 3) * 32 + lane;  // TMEM lane: key channel i (W^T row) / value channel j (Ut^T row)
+    const int cbase = (warp >> 2) * 32;
     if (ok) {
         float *UT = at<float>(rec, Rec::UT) + i * CH;
-        for (int c0 = 0; c0 < CH; c0 += 16) {
+        for (int c0 = cbase; c0 < cbase + 32; c0 += 16) {
             float v[16], u[16];
-            tmem_ld16(tm + (uint32_t(warp * 32) << 16) + 64 + c0, v);
-            tmem_ld16(tm + (uint32_t(warp * 32) << 16) + 128 + c0, u);
+            tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + 64 + c0, v);
+            tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + 128 + c0, u);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -499,7 +517,7 @@ __global__ void __launch_bounds__(128) prefill_intra_kernel(const PrefillParams 
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0 && ok) {
         bulk_store(rec + Rec::W_HI, whi, 32768);
         bulk_commit();
         bulk_wait();
@@ -848,7 +866,7 @@ kda_status launch_act(const PrefillParams &p, const kda_io *io, int n_tok, int N
             return KDA_ERR_CUDA;
         const dim3 grid(unsigned(n_chunks), unsigned(p.H));
         prefill_prep_kernel<Act><<<grid, 128, prep_smem<Act>(), stream>>>(p, mq, mk, mv, ma);
-        prefill_intra_kernel<<<grid, 128, kIntraSmem, stream>>>(p);
+        prefill_intra_kernel<<<grid, is::NT, kIntraSmem, stream>>>(p);
     }
     prefill_chain_kernel<<<unsigned(N) * p.H, 128, kChainSmem, stream>>>(p);
     if (n_chunks > 0) prefill_out_kernel<Act><<<dim3(unsigned(n_chunks), unsigned(p.H)), 128, 0, stream>>>(p);
