@@ -51,6 +51,8 @@ def args_():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
     ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "prefill"], default=None,
                     help="run one secondary case alone (for profiling) and print its numbers")
+    ap.add_argument("--prefill-tokens", type=int, default=None,
+                    help="with --only prefill: a shorter sequence of the same workload (small profiling case)")
     return ap.parse_args()
 
 
@@ -139,7 +141,7 @@ def run_ours(a, rank, world, local):
     if a.only:
         kbuild.build()
         if a.only == "prefill":
-            res = prefill_case(kda, dev, iters=a.steps, warmup=a.warmup)
+            res = prefill_case(kda, dev, iters=a.steps, warmup=a.warmup, L=a.prefill_tokens)
         else:
             res = secondary(kda, dev, hbm_peak, peak_kind, only=a.only, iters=a.steps)
         print(json.dumps(res), flush=True)
@@ -337,11 +339,12 @@ def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
     return res
 
 
-def prefill_case(kda, dev, iters=3, warmup=1):
+def prefill_case(kda, dev, iters=3, warmup=1, L=None):
     """Chunked prefill of one 32768-token sequence (H = 64, d = 128, C = 64,
     alpha = sigmoid(N(3, 1))) from a zero slot; tok/s of the whole call."""
     wl = I.PREFILL_32K
-    H, D, act, L = wl.H, wl.dk, wl.act, wl.extra["L"]
+    H, D, act = wl.H, wl.dk, wl.act
+    L = L or wl.extra["L"]
     w_dev = {k: v.to(dev) for k, v in wl.weights().items()}
     w = kda.make_weights(w_dev["conv_w"], w_dev["norm_w"], wl.eps_l2, wl.eps_rms)
     pool = kda.StatePool(wl.num_slots, H, D, D, act)
@@ -368,7 +371,7 @@ def prefill_case(kda, dev, iters=3, warmup=1):
     ms = float(np.mean(times))
     st, flags = kda.kda_poll_device_error(pool)
     assert st == 0, f"device error word {flags:#x}"
-    return {"workload": wl.name, "tok_per_s": round(L / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
+    return {"workload": wl.name if L == wl.extra["L"] else f"{wl.name} (first {L} tokens)", "tok_per_s": round(L / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
             "workspace_bytes": ws.numel(),
             "l2": "inputs (3.2 GB) and workspace exceed L2; not flushed between calls"}
 

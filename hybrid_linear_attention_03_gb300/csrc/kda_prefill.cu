@@ -84,7 +84,7 @@ struct Rec {
     static constexpr size_t P_HI = KT_LO + 16384;    // img [64 r][64 s]    P
     static constexpr size_t P_LO = P_HI + 8192;
     static constexpr size_t GAM = P_LO + 8192;       // fp32 [128] exp(G_last)
-    static constexpr size_t UT = GAM + 1024;         // fp32 [128 j][64 r]  Ut^T
+    static constexpr size_t UT = GAM + 1024;         // fp32 [64 r][128 j]  Ut
     static constexpr size_t OO = UT + 32768;         // fp32 [64 r][128 j]  O (pre-norm)
     static constexpr size_t BYTES = OO + 32768;
     static constexpr uint32_t B1_BYTES = uint32_t(KT_HI - W_HI);  // W + Q images
@@ -119,6 +119,12 @@ __device__ __forceinline__ T *at(char *base, size_t off) {
 }
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+__device__ __forceinline__ void ld8(const float *p, float (&x)[8]) {  // p 16-byte aligned
+    const float4 a = ld4(p), b = ld4(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
 
 template <typename Act>
 __device__ __forceinline__ float4 act4(const Act *p);
@@ -253,11 +259,16 @@ constexpr int NT = 256;
 
 // Fills `rows` x (8 * chunks_per_row) elements of an image pair with f(row, k0, out8),
 // storing 16-byte chunks at their swizzled offsets (shared or global memory).
-template <typename F>
+// Row-major unit order (consecutive threads walk one row's chunks) suits f
+// reading rows of a [row][K] array; chunk-major order (consecutive threads
+// take consecutive rows of one chunk) suits f reading columns of a [K][row]
+// array without shared-memory bank conflicts.
+template <bool kChunkMajor = false, typename F>
 __device__ __forceinline__ void build_image(unsigned char *hi, unsigned char *lo, int rows, int chunks_per_row,
                                             int tid, int nthreads, F f) {
     for (int u = tid; u < rows * chunks_per_row; u += nthreads) {
-        const int r = u / chunks_per_row, c = u - r * chunks_per_row;
+        const int r = kChunkMajor ? u % rows : u / chunks_per_row;
+        const int c = kChunkMajor ? u / rows : u - r * chunks_per_row;
         float x[8];
         f(r, 8 * c, x);
         uint4 vh, vl;
@@ -335,14 +346,20 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     // ---- phase 1: X = [K exp(G - c); Q exp(G - c)], Kb = K exp(c - G) -> A, P
     if (ok && !exact) {
         build_image(sm + is::X_HI, sm + is::X_LO, 128, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
-            const float *src = r < CH ? KHs + r * D : QHs + (r - CH) * D;
-            const float *gg = GGs + (r & (CH - 1)) * D;
+            float a[8], gg[8], cr[8];
+            ld8(r < CH ? KHs + r * D + k0 : QHs + (r - CH) * D + k0, a);
+            ld8(GGs + (r & (CH - 1)) * D + k0, gg);
+            ld8(cref + k0, cr);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = src[k0 + e] * expf(gg[k0 + e] - cref[k0 + e]);
+            for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(gg[e] - cr[e]);
         });
         build_image(sm + is::KB_HI, sm + is::KB_LO, CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
+            float a[8], gg[8], cr[8];
+            ld8(KHs + r * D + k0, a);
+            ld8(GGs + r * D + k0, gg);
+            ld8(cref + k0, cr);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = KHs[r * D + k0 + e] * expf(cref[k0 + e] - GGs[r * D + k0 + e]);
+            for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(cr[e] - gg[e]);
         });
         fence_proxy_async_smem();
         tc_fence_before();
@@ -358,10 +375,13 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     if (ok) {
         build_image(reinterpret_cast<unsigned char *>(rec + Rec::Q_HI), reinterpret_cast<unsigned char *>(rec + Rec::Q_LO),
                     CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
+                        float a[8], gg[8];
+                        ld8(QHs + r * D + k0, a);
+                        ld8(GGs + r * D + k0, gg);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = QHs[r * D + k0 + e] * expf(GGs[r * D + k0 + e]);
+                        for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(gg[e]);
                     });
-        build_image(reinterpret_cast<unsigned char *>(rec + Rec::KT_HI),
+        build_image<true>(reinterpret_cast<unsigned char *>(rec + Rec::KT_HI),
                     reinterpret_cast<unsigned char *>(rec + Rec::KT_LO), D, 8, tid, is::NT,
                     [&](int i, int r0, float(&x)[8]) {
                         const float gl = GGs[(CH - 1) * D + i];
@@ -466,14 +486,13 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     ok = __syncthreads_and(ok && mbar_wait(bar_ld, 1, p.err));  // v has arrived
     if (ok) {
         build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, is::NT, [&](int r, int s0, float(&x)[8]) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = T[r * CH + s0 + e];
+            ld8(T + r * CH + s0, x);
         });
-        build_image(sm + is::AK_HI, sm + is::AK_LO, D, 8, tid, is::NT, [&](int i, int s0, float(&x)[8]) {
+        build_image<true>(sm + is::AK_HI, sm + is::AK_LO, D, 8, tid, is::NT, [&](int i, int s0, float(&x)[8]) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * expf(GGs[(s0 + e) * D + i]) * KHs[(s0 + e) * D + i];
         });
-        build_image(sm + is::AV_HI, sm + is::AV_LO, D, 8, tid, is::NT, [&](int j, int s0, float(&x)[8]) {
+        build_image<true>(sm + is::AV_HI, sm + is::AV_LO, D, 8, tid, is::NT, [&](int j, int s0, float(&x)[8]) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * VVs[(s0 + e) * D + j];
         });
@@ -494,7 +513,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     const int i = (warp & 3) * 32 + lane;  // TMEM lane: key channel i (W^T row) / value channel j (Ut^T row)
     const int cbase = (warp >> 2) * 32;
     if (ok) {
-        float *UT = at<float>(rec, Rec::UT) + i * CH;
+        float *UT = at<float>(rec, Rec::UT) + i;  // column j = i of Ut [r][j]
         for (int c0 = cbase; c0 < cbase + 32; c0 += 16) {
             float v[16], u[16];
             tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + 64 + c0, v);
@@ -510,8 +529,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
                 *reinterpret_cast<__nv_bfloat16 *>(wlo + off) = wl;
             }
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4 *>(UT + c0 + e) = make_float4(u[e], u[e + 1], u[e + 2], u[e + 3]);
+            for (int e = 0; e < 16; ++e) UT[(c0 + e) * D] = u[e];  // coalesced across the warp
         }
     }
     fence_proxy_async_smem();
@@ -520,7 +538,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     if (tid == 0 && ok) {
         bulk_store(rec + Rec::W_HI, whi, 32768);
         bulk_commit();
-        bulk_wait();
+        bulk_wait_read();  // shared memory may go; the write lands before the kernel completes
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
@@ -612,12 +630,9 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         }
         // Ut^T row j while the MMAs run
         float ut[CH];
-        const float *UTg = reinterpret_cast<const float *>(rec + Rec::UT) + size_t(j) * CH;
+        const float *UTg = reinterpret_cast<const float *>(rec + Rec::UT) + j;  // column j, coalesced
 #pragma unroll
-        for (int e = 0; e < CH; e += 4) {
-            const float4 x = ld4(UTg + e);
-            ut[e] = x.x; ut[e + 1] = x.y; ut[e + 2] = x.z; ut[e + 3] = x.w;
-        }
+        for (int e = 0; e < CH; ++e) ut[e] = UTg[e * D];
         ok = __syncthreads_and(mbar_wait(bar_m1, par, p.err));
         if (!ok) break;
         tc_fence_after();
@@ -625,19 +640,20 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
             mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
             bulk_load(sm + cs::B1, rec_ptr(p, g + 1, h) + Rec::W_HI, Rec::B1_BYTES, bar_b1);
         }
-        // U^T row j = Ut^T - (W S)^T  -> hi/lo images
-        for (int c0 = 0; c0 < CH; c0 += 16) {
-            float v[16];
-            tmem_ld16(tl + c0, v);
+        // U^T row j = Ut^T - (W S)^T  -> hi/lo images (all 64 columns in one TMEM round trip)
+        {
+            float v[4][16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(tl + 16 * q, v[q]);
             tmem_wait_ld();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            for (int cc = 0; cc < 8; ++cc) {
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = ut[c0 + 8 * half + e] - v[8 * half + e];
+                for (int e = 0; e < 8; ++e) x[e] = ut[8 * cc + e] - v[cc >> 1][8 * (cc & 1) + e];
                 uint4 vh, vl;
                 split8(x, vh, vl);
-                const uint32_t off = sw128_chunk(j, (c0 >> 3) + half, D);
+                const uint32_t off = sw128_chunk(j, cc, D);
                 *reinterpret_cast<uint4 *>(sm + cs::A2_HI + off) = vh;
                 *reinterpret_cast<uint4 *>(sm + cs::A2_LO + off) = vl;
             }
@@ -665,40 +681,50 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         }
         // O column j -> record (rows r), coalesced across the warp
         float *O = reinterpret_cast<float *>(rec + Rec::OO);
-        for (int c0 = 0; c0 < CH; c0 += 16) {
-            float v[16];
-            tmem_ld16(tl + 64 + c0, v);
+        {
+            float v[4][16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(tl + 64 + 16 * q, v[q]);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) O[(c0 + e) * D + j] = v[e];
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int e = 0; e < 16; ++e) O[(16 * q + e) * D + j] = v[q][e];
         }
         // S^T row j <- gamma . S^T row j + (K^T U)^T row j; refresh the A1 images
         const ChunkMeta cm = p.chunks[g];
-        for (int c0 = 0; c0 < D; c0 += 16) {
-            float s[16], ds[16];
-            tmem_ld16(tl + 256 + c0, s);
-            tmem_ld16(tl + 128 + c0, ds);
+        for (int c0 = 0; c0 < D; c0 += 32) {  // 32 columns per TMEM round trip
+            float s[2][16], ds[2][16];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                tmem_ld16(tl + 256 + c0 + 16 * q, s[q]);
+                tmem_ld16(tl + 128 + c0 + 16 * q, ds[q]);
+            }
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) s[e] = fmaf(gcur[c0 + e], s[e], ds[e]);
-            tmem_st16(tl + 256 + c0, s);
+            for (int q = 0; q < 2; ++q) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float x[8];
+                for (int e = 0; e < 16; ++e) s[q][e] = fmaf(gcur[c0 + 16 * q + e], s[q][e], ds[q][e]);
+                tmem_st16(tl + 256 + c0 + 16 * q, s[q]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = s[8 * half + e];
-                uint4 vh, vl;
-                split8(x, vh, vl);
-                const uint32_t off = sw128_chunk(j, (c0 >> 3) + half, D);
-                *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
-                *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
-            }
-            for (int q = 0; q < cm.ck_count; ++q) {
-                const CkptMeta ck = p.ckpts[cm.ck_begin + q];
-                float *dst = p.states + size_t(ck.dst_slot) * p.H * head_elems + size_t(h) * head_elems + size_t(j) * D + c0;
+                for (int half = 0; half < 2; ++half) {
+                    float x[8];
 #pragma unroll
-                for (int e = 0; e < 16; e += 4)
-                    *reinterpret_cast<float4 *>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+                    for (int e = 0; e < 8; ++e) x[e] = s[q][8 * half + e];
+                    uint4 vh, vl;
+                    split8(x, vh, vl);
+                    const uint32_t off = sw128_chunk(j, ((c0 + 16 * q) >> 3) + half, D);
+                    *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
+                    *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
+                }
+                for (int k = 0; k < cm.ck_count; ++k) {
+                    const CkptMeta ck = p.ckpts[cm.ck_begin + k];
+                    float *dst = p.states + size_t(ck.dst_slot) * p.H * head_elems + size_t(h) * head_elems +
+                                 size_t(j) * D + c0 + 16 * q;
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(dst + e) = make_float4(s[q][e], s[q][e + 1], s[q][e + 2], s[q][e + 3]);
+                }
             }
         }
         tmem_wait_st();
