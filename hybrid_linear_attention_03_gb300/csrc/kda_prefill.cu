@@ -75,20 +75,19 @@ struct Rec {
     static constexpr size_t VV = KH + 32768;         // fp32 [64][128] conv'd v
     static constexpr size_t GG = VV + 32768;         // fp32 [64][128] cumulative log decay
     static constexpr size_t BB = GG + 32768;         // fp32 [64] beta (0 on padding rows)
-    static constexpr size_t W_HI = BB + 1024;        // img [64 r][128 i]   W
-    static constexpr size_t W_LO = W_HI + 16384;
-    static constexpr size_t Q_HI = W_LO + 16384;     // img [64 r][128 i]   exp(G) . q
-    static constexpr size_t Q_LO = Q_HI + 16384;
-    static constexpr size_t KT_HI = Q_LO + 16384;    // img [128 i][64 r]   (exp(G_last - G) . k)^T
-    static constexpr size_t KT_LO = KT_HI + 16384;
-    static constexpr size_t P_HI = KT_LO + 16384;    // img [64 r][64 s]    P
-    static constexpr size_t P_LO = P_HI + 8192;
-    static constexpr size_t GAM = P_LO + 8192;       // fp32 [128] exp(G_last)
+    // [W; exp(G) . q]: one 128-row image [r | 64 + r][128 i] (W rows 0..63, Q rows 64..127)
+    static constexpr size_t WQ_HI = BB + 1024;
+    static constexpr size_t WQ_LO = WQ_HI + 32768;
+    // [(exp(G_last - G) . k)^T; P]: one 192-row image [i | 128 + r][64] (K^T rows 0..127, P rows 128..191)
+    static constexpr size_t KP_HI = WQ_LO + 32768;
+    static constexpr size_t KP_LO = KP_HI + 24576;
+    static constexpr size_t P_OFF = 16384;           // P rows start 16 KiB into a KP image
+    static constexpr size_t GAM = KP_LO + 24576;     // fp32 [128] exp(G_last)
     static constexpr size_t UT = GAM + 1024;         // fp32 [64 r][128 j]  Ut
     static constexpr size_t OO = UT + 32768;         // fp32 [64 r][128 j]  O (pre-norm)
     static constexpr size_t BYTES = OO + 32768;
-    static constexpr uint32_t B1_BYTES = uint32_t(KT_HI - W_HI);  // W + Q images
-    static constexpr uint32_t B2_BYTES = uint32_t(UT - KT_HI);    // K^T + P images + gamma
+    static constexpr uint32_t B1_BYTES = uint32_t(KP_HI - WQ_HI);  // [W; Q] images
+    static constexpr uint32_t B2_BYTES = uint32_t(UT - KP_HI);     // [K^T; P] images + gamma
 };
 static_assert(Rec::BYTES % 1024 == 0, "record keeps 1 KiB alignment");
 
@@ -265,7 +264,8 @@ constexpr int NT = 256;
 // array without shared-memory bank conflicts.
 template <bool kChunkMajor = false, typename F>
 __device__ __forceinline__ void build_image(unsigned char *hi, unsigned char *lo, int rows, int chunks_per_row,
-                                            int tid, int nthreads, F f) {
+                                            int tid, int nthreads, F f, int row0 = 0, int total_rows = 0) {
+    if (total_rows == 0) total_rows = rows;
     for (int u = tid; u < rows * chunks_per_row; u += nthreads) {
         const int r = kChunkMajor ? u % rows : u / chunks_per_row;
         const int c = kChunkMajor ? u / rows : u - r * chunks_per_row;
@@ -273,7 +273,7 @@ __device__ __forceinline__ void build_image(unsigned char *hi, unsigned char *lo
         f(r, 8 * c, x);
         uint4 vh, vl;
         split8(x, vh, vl);
-        const uint32_t off = sw128_chunk(r, c, rows);
+        const uint32_t off = sw128_chunk(row0 + r, c, total_rows);
         *reinterpret_cast<uint4 *>(hi + off) = vh;
         *reinterpret_cast<uint4 *>(lo + off) = vl;
     }
@@ -373,16 +373,16 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     }
     // chain images that need no MMA: exp(G) . q (rows r) and (exp(G_last - G) . k)^T (rows i)
     if (ok) {
-        build_image(reinterpret_cast<unsigned char *>(rec + Rec::Q_HI), reinterpret_cast<unsigned char *>(rec + Rec::Q_LO),
+        build_image(reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI), reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO),
                     CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
                         float a[8], gg[8];
                         ld8(QHs + r * D + k0, a);
                         ld8(GGs + r * D + k0, gg);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(gg[e]);
-                    });
-        build_image<true>(reinterpret_cast<unsigned char *>(rec + Rec::KT_HI),
-                    reinterpret_cast<unsigned char *>(rec + Rec::KT_LO), D, 8, tid, is::NT,
+                    }, CH, 2 * CH);
+        build_image<true>(reinterpret_cast<unsigned char *>(rec + Rec::KP_HI),
+                    reinterpret_cast<unsigned char *>(rec + Rec::KP_LO), D, 8, tid, is::NT,
                     [&](int i, int r0, float(&x)[8]) {
                         const float gl = GGs[(CH - 1) * D + i];
 #pragma unroll
@@ -392,8 +392,8 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     __syncthreads();
     // ---- A (s < r, times beta_r) -> fp32 smem, P (s <= r) -> record images
     float *A = reinterpret_cast<float *>(sm + is::A_F32);
-    unsigned char *phi = reinterpret_cast<unsigned char *>(rec + Rec::P_HI);
-    unsigned char *plo = reinterpret_cast<unsigned char *>(rec + Rec::P_LO);
+    unsigned char *phi = reinterpret_cast<unsigned char *>(rec + Rec::KP_HI + Rec::P_OFF);
+    unsigned char *plo = reinterpret_cast<unsigned char *>(rec + Rec::KP_LO + Rec::P_OFF);
     if (!exact) {
         ok = __syncthreads_and(ok && mbar_wait(bar_mma, mma_phase, p.err));
         mma_phase ^= 1;
@@ -536,7 +536,11 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok) {
-        bulk_store(rec + Rec::W_HI, whi, 32768);
+        // a 64-row image's K-block b holds the same bytes as rows 0..63 of K-block b of WQ
+        bulk_store(rec + Rec::WQ_HI, whi, 8192);
+        bulk_store(rec + Rec::WQ_HI + 16384, whi + 8192, 8192);
+        bulk_store(rec + Rec::WQ_LO, wlo, 8192);
+        bulk_store(rec + Rec::WQ_LO + 16384, wlo + 8192, 8192);
         bulk_commit();
         bulk_wait_read();  // shared memory may go; the write lands before the kernel completes
     }
@@ -547,10 +551,10 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
 // ============================================================== chain ====
 namespace cs {  // chain shared-memory map
 constexpr uint32_t A1_HI = 0, A1_LO = 32768;             // S^T images [128 j][128 i]
-constexpr uint32_t B1 = 65536;                            // W hi/lo, Q hi/lo images (64 KiB)
-constexpr uint32_t W_HI = B1, W_LO = B1 + 16384, Q_HI = B1 + 32768, Q_LO = B1 + 49152;
-constexpr uint32_t B2 = 131072;                           // K^T hi/lo, P hi/lo, gamma
-constexpr uint32_t KT_HI = B2, KT_LO = B2 + 16384, P_HI = B2 + 32768, P_LO = B2 + 40960, GAM = B2 + 49152;
+constexpr uint32_t B1 = 65536;                            // [W; Q] hi/lo images (64 KiB)
+constexpr uint32_t WQ_HI = B1, WQ_LO = B1 + 32768;
+constexpr uint32_t B2 = 131072;                           // [K^T; P] hi/lo images, gamma
+constexpr uint32_t KP_HI = B2, KP_LO = B2 + 24576, GAM = B2 + 49152;
 constexpr uint32_t A2_HI = 181248, A2_LO = 181248 + 16384;  // U^T images [128 j][64 r]
 constexpr uint32_t GCUR = A2_LO + 16384;                   // gamma of the current chunk
 constexpr uint32_t BARS = GCUR + 512;
@@ -558,7 +562,7 @@ constexpr uint32_t BYTES = BARS + 512;
 }  // namespace cs
 static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
 
-// TMEM columns: (W S)^T [0,64), O^T [64,128), (K^T U)^T [128,256), S^T [256,384)
+// TMEM columns: [(W S)^T | (Q S)^T] [0,128), [(K^T U)^T | (P U)^T] [128,320), S^T [320,448)
 __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -584,9 +588,9 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
     if (tid == 0 && sq.n_chunks > 0) {
         const char *r0 = rec_ptr(p, sq.chunk0, h);
         mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
-        bulk_load(sm + cs::B1, r0 + Rec::W_HI, Rec::B1_BYTES, bar_b1);
+        bulk_load(sm + cs::B1, r0 + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
         mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
-        bulk_load(sm + cs::B2, r0 + Rec::KT_HI, Rec::B2_BYTES, bar_b2);
+        bulk_load(sm + cs::B2, r0 + Rec::KP_HI, Rec::B2_BYTES, bar_b2);
     }
     // S^T row j: fp32 into TMEM, hi/lo into the A1 images
     for (int c0 = 0; c0 < D; c0 += 16) {
@@ -596,7 +600,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
             const float4 x = sq.has_init ? ld4(slot_state + size_t(j) * D + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
             v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
         }
-        tmem_st16(tl + 256 + c0, v);
+        tmem_st16(tl + 320 + c0, v);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float x[8];
@@ -615,7 +619,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
     __syncthreads();
     tc_fence_after();
     bool ok = true;
-    const uint32_t id64 = idesc_bf16_f32(128, CH), id128 = idesc_bf16_f32(128, D);
+    const uint32_t id128 = idesc_bf16_f32(128, 2 * CH), id192 = idesc_bf16_f32(128, D + CH);
     for (int c = 0; c < sq.n_chunks && ok; ++c) {
         const int g = sq.chunk0 + c;
         char *rec = rec_ptr(p, g, h);
@@ -624,8 +628,8 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         if (!ok) break;
         if (tid == 0) {
             tc_fence_after();
-            mma3(tm + 0, sbase + cs::A1_HI, sbase + cs::A1_LO, sbase + cs::W_HI, sbase + cs::W_LO, D, CH, D, id64, false);
-            mma3(tm + 64, sbase + cs::A1_HI, sbase + cs::A1_LO, sbase + cs::Q_HI, sbase + cs::Q_LO, D, CH, D, id64, false);
+            mma3(tm + 0, sbase + cs::A1_HI, sbase + cs::A1_LO, sbase + cs::WQ_HI, sbase + cs::WQ_LO, D, 2 * CH, D,
+                 id128, false);
             mma_commit(bar_m1);
         }
         // Ut^T row j while the MMAs run
@@ -638,7 +642,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         tc_fence_after();
         if (tid == 0 && c + 1 < sq.n_chunks) {  // W and Q images are consumed: stream in the next chunk's
             mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
-            bulk_load(sm + cs::B1, rec_ptr(p, g + 1, h) + Rec::W_HI, Rec::B1_BYTES, bar_b1);
+            bulk_load(sm + cs::B1, rec_ptr(p, g + 1, h) + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
         }
         // U^T row j = Ut^T - (W S)^T  -> hi/lo images (all 64 columns in one TMEM round trip)
         {
@@ -666,10 +670,8 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            mma3(tm + 128, sbase + cs::A2_HI, sbase + cs::A2_LO, sbase + cs::KT_HI, sbase + cs::KT_LO, D, D, CH, id128,
-                 false);
-            mma3(tm + 64, sbase + cs::A2_HI, sbase + cs::A2_LO, sbase + cs::P_HI, sbase + cs::P_LO, D, CH, CH, id64,
-                 true);
+            mma3(tm + 128, sbase + cs::A2_HI, sbase + cs::A2_LO, sbase + cs::KP_HI, sbase + cs::KP_LO, D, D + CH, CH,
+                 id192, false);
             mma_commit(bar_m2);
         }
         ok = __syncthreads_and(mbar_wait(bar_m2, par, p.err));
@@ -677,19 +679,22 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         tc_fence_after();
         if (tid == 0 && c + 1 < sq.n_chunks) {  // K^T, P images and gamma consumed
             mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
-            bulk_load(sm + cs::B2, rec_ptr(p, g + 1, h) + Rec::KT_HI, Rec::B2_BYTES, bar_b2);
+            bulk_load(sm + cs::B2, rec_ptr(p, g + 1, h) + Rec::KP_HI, Rec::B2_BYTES, bar_b2);
         }
         // O column j -> record (rows r), coalesced across the warp
         float *O = reinterpret_cast<float *>(rec + Rec::OO);
-        {
-            float v[4][16];
+        for (int h2 = 0; h2 < 2; ++h2) {  // O = (Q S)^T + (P U)^T
+            float v[2][16], w2[2][16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tl + 64 + 16 * q, v[q]);
+            for (int q = 0; q < 2; ++q) {
+                tmem_ld16(tl + 64 + 32 * h2 + 16 * q, v[q]);
+                tmem_ld16(tl + 256 + 32 * h2 + 16 * q, w2[q]);
+            }
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 2; ++q)
 #pragma unroll
-                for (int e = 0; e < 16; ++e) O[(16 * q + e) * D + j] = v[q][e];
+                for (int e = 0; e < 16; ++e) O[(32 * h2 + 16 * q + e) * D + j] = v[q][e] + w2[q][e];
         }
         // S^T row j <- gamma . S^T row j + (K^T U)^T row j; refresh the A1 images
         const ChunkMeta cm = p.chunks[g];
@@ -697,7 +702,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
             float s[2][16], ds[2][16];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                tmem_ld16(tl + 256 + c0 + 16 * q, s[q]);
+                tmem_ld16(tl + 320 + c0 + 16 * q, s[q]);
                 tmem_ld16(tl + 128 + c0 + 16 * q, ds[q]);
             }
             tmem_wait_ld();
@@ -705,7 +710,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
             for (int q = 0; q < 2; ++q) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) s[q][e] = fmaf(gcur[c0 + 16 * q + e], s[q][e], ds[q][e]);
-                tmem_st16(tl + 256 + c0 + 16 * q, s[q]);
+                tmem_st16(tl + 320 + c0 + 16 * q, s[q]);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float x[8];
@@ -737,7 +742,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
     if (ok) {
         for (int c0 = 0; c0 < D; c0 += 16) {
             float s[16];
-            tmem_ld16(tl + 256 + c0, s);
+            tmem_ld16(tl + 320 + c0, s);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; e += 4)
