@@ -49,7 +49,7 @@ def args_():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
-    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "prefill"], default=None,
+    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "prefill", "mixed"], default=None,
                     help="run one secondary case alone (for profiling) and print its numbers")
     ap.add_argument("--prefill-tokens", type=int, default=None,
                     help="with --only prefill: a shorter sequence of the same workload (small profiling case)")
@@ -142,6 +142,8 @@ def run_ours(a, rank, world, local):
         kbuild.build()
         if a.only == "prefill":
             res = prefill_case(kda, dev, iters=a.steps, warmup=a.warmup, L=a.prefill_tokens)
+        elif a.only == "mixed":
+            res = mixed_case(kda, dev, iters=a.steps, warmup=a.warmup)
         else:
             res = secondary(kda, dev, hbm_peak, peak_kind, only=a.only, iters=a.steps)
         print(json.dumps(res), flush=True)
@@ -274,10 +276,13 @@ def run_ours(a, rank, world, local):
     }
     if not a.no_secondary:
         sec = secondary(kda, dev, hbm_peak, peak_kind)
-        try:
-            sec["prefill"] = prefill_case(kda, dev, iters=3, warmup=1)
-        except Exception as e:  # reported, not hidden: the line says why prefill is absent
-            sec["prefill"] = {"error": f"{type(e).__name__}: {e}"}
+        for name, fn in (("prefill", lambda: prefill_case(kda, dev, iters=3, warmup=1)),
+                         ("mixed", lambda: mixed_case(kda, dev, iters=3, warmup=1))):
+            try:
+                sec[name] = fn()
+            except Exception as e:  # reported, not hidden: the line says why the entry is absent
+                sec[name] = {"error": f"{type(e).__name__}: {e}"}
+            torch.cuda.empty_cache()
         line["secondary"] = sec
     if rank == 0:
         if not a.no_cpu_baseline:
@@ -374,6 +379,59 @@ def prefill_case(kda, dev, iters=3, warmup=1, L=None):
     return {"workload": wl.name if L == wl.extra["L"] else f"{wl.name} (first {L} tokens)", "tok_per_s": round(L / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
             "workspace_bytes": ws.numel(),
             "l2": "inputs (3.2 GB) and workspace exceed L2; not flushed between calls"}
+
+
+def mixed_case(kda, dev, iters=3, warmup=1):
+    """The mixed step: one chunked-prefill call over 8 varlen sequences
+    (log-uniform 1K..64K tokens, checkpoints every 32768 tokens and at each
+    end into fresh slots) plus one decode call for 56 sequences warmed by 512
+    tokens, over a 1024-slot pool.  tok/s = (prefill tokens + 56) / time."""
+    wl = I.MIXED
+    plan = I.mixed_plan(wl)
+    H, D, act = wl.H, wl.dk, wl.act
+    w_dev = {k: v.to(dev) for k, v in wl.weights().items()}
+    w = kda.make_weights(w_dev["conv_w"], w_dev["norm_w"], wl.eps_l2, wl.eps_rms)
+    pool = kda.StatePool(wl.num_slots, H, D, D, act)
+    nd, warm_n, lens = wl.extra["n_decode"], wl.extra["warm"], plan["lens"]
+    warm = {k: v.to(dev) for k, v in I.concat_inputs([wl.tokens(b, warm_n) for b in range(nd)]).items()}
+    cu_w = [warm_n * i for i in range(nd + 1)]
+    ws_w = torch.empty(kda.kda_prefill_workspace_bytes(pool, cu_w), dtype=torch.uint8, device=dev)
+    wout = torch.empty(nd * warm_n, H, D, dtype=act, device=dev)
+    kda.kda_prefill_chunked(pool, w, kda.make_io(warm, wout), cu_w, plan["dec_slots"], [0] * nd, 64, (), ws_w)
+    del ws_w, wout, warm
+    pf = {k: v.to(dev) for k, v in I.concat_inputs([wl.tokens(300 + n, L) for n, L in enumerate(lens)]).items()}
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(pool, cu), dtype=torch.uint8, device=dev)
+    out_pf = torch.empty(cu[-1], H, D, dtype=act, device=dev)
+    dec = {k: v.to(dev) for k, v in wl.tokens(400, nd).items()}
+    out_dec = torch.empty(nd, H, D, dtype=act, device=dev)
+    dslots = torch.tensor(plan["dec_slots"], dtype=torch.int32, device=dev)
+    io_pf, io_dec = kda.make_io(pf, out_pf), kda.make_io(dec, out_dec)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.kda_prefill_chunked(pool, w, io_pf, cu, plan["pf_slots"], [0] * len(lens), 64, plan["reqs"], ws)
+        kda.kda_decode(pool, w, io_dec, dslots, nd)
+
+    for _ in range(warmup):
+        step()
+    times = []
+    for _ in range(iters):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        step()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    ms = float(np.mean(times))
+    st, flags = kda.kda_poll_device_error(pool)
+    assert st == 0, f"device error word {flags:#x}"
+    n_tok = cu[-1] + nd
+    return {"workload": wl.name, "tok_per_s": round(n_tok / (ms / 1e3), 1), "ms_per_step": round(ms, 3),
+            "prefill_tokens": cu[-1], "decode_tokens": nd, "checkpoints": len(plan["reqs"]),
+            "workspace_bytes": ws.numel()}
 
 
 # ----------------------------------------------------------------------- oracle

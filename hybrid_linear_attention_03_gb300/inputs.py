@@ -146,3 +146,21 @@ def mixed_prefill_lengths(wl: Workload = MIXED) -> list[int]:
     (log-uniform in [1K, 64K])."""
     u = uniforms(wl.seed, 0, wl.extra["n_prefill"])
     return [int(np.floor(1024.0 * 64.0 ** x)) for x in u]
+
+
+def mixed_plan(wl: Workload = MIXED) -> dict:
+    """Slots and checkpoint requests of the mixed workload: decodes in slots
+    0..n_decode-1, prefills next, then one fresh slot per checkpoint request
+    (every `interval` tokens from the sequence start, and each sequence end)."""
+    lens = mixed_prefill_lengths(wl)
+    nd, npf, iv = wl.extra["n_decode"], wl.extra["n_prefill"], wl.extra["interval"]
+    dec_slots = list(range(nd))
+    pf_slots = list(range(nd, nd + npf))
+    reqs, nxt = [], nd + npf
+    for n, L in enumerate(lens):
+        for pos in sorted(set(list(range(iv, L, iv)) + [L])):
+            reqs.append((n, pos, nxt))
+            nxt += 1
+    resume = [int(x) for x in permutation(wl.seed, 5, npf)[:wl.extra["resume"]]]
+    return {"lens": lens, "dec_slots": dec_slots, "pf_slots": pf_slots, "reqs": reqs, "next_free": nxt,
+            "resume": resume}

@@ -51,3 +51,20 @@ def to_device(inp: dict, device="cuda") -> dict:
 
 def out_tol(act: torch.dtype) -> float:
     return OUT_TOL_BF16 if act == torch.bfloat16 else OUT_TOL_F32
+
+
+def head_subset(inp: dict, w: dict, heads, H: int, dk: int, dv: int):
+    """Slices per-token inputs and weights down to `heads` (heads are
+    independent, so the oracle can check a sample of them at full length)."""
+    heads = list(heads)
+    sub = {k: v[:, heads] for k, v in inp.items()}
+    chans = conv_channels(heads, H, dk, dv)
+    return sub, {"conv_w": w["conv_w"][chans], "norm_w": w["norm_w"]}
+
+
+def conv_channels(heads, H: int, dk: int, dv: int) -> np.ndarray:
+    """Conv-channel indices (q, then k, then v) of the given heads."""
+    q = [h * dk + i for h in heads for i in range(dk)]
+    k = [H * dk + h * dk + i for h in heads for i in range(dk)]
+    v = [2 * H * dk + h * dv + j for h in heads for j in range(dv)]
+    return np.array(q + k + v)
