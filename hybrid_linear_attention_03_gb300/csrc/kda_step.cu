@@ -131,18 +131,14 @@ kda_step_kernel(const StepParams p) {
         if (threadIdx.x == 0) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
         return;
     }
+    // Programmatic dependent launch: the next step-kernel launch on this
+    // stream may start now and run its own prologue up to its
+    // griddepcontrol.wait, which waits for this grid to complete.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // Issue the state loads first; the conv prologue runs while they fly.
     const int sub = lane / C::LPR, c4 = lane % C::LPR;
-    const float *Sin = p.states + size_t(in_slot) * slot_elems + size_t(h) * head_elems;
-    float4 S[C::NV];
-#pragma unroll
-    for (int n = 0; n < C::NV; ++n) {
-        const int row = warp * 16 + n * C::RPL + sub;
-        S[n] = load4(Sin + size_t(row) * D + 4 * c4);
-    }
-
-    // Per-token inputs of the first token, fetched before the prologue.
+    // Per-token inputs of the first token (not written by a preceding step
+    // launch), fetched before the wait.
     const int n_own = c4 / C::OWN;
     const bool owner = (c4 % C::OWN) == 0;
     const int own_row = n_own * C::RPL + sub;  // 0..15 within the warp
@@ -170,10 +166,28 @@ kda_step_kernel(const StepParams p) {
             const int ch = s * p.H * D + h * D + c;
             const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
             wv[u] = load4(cw + size_t(ch) * 4);
+            xv[u][3] = src[size_t(b) * T * p.H * D + size_t(h) * D + c];
+        }
+    }
+    // The pool's state and tail may have been written by the preceding step
+    // launch: wait for it to complete before reading them.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float *Sin = p.states + size_t(in_slot) * slot_elems + size_t(h) * head_elems;
+    float4 S[C::NV];
+#pragma unroll
+    for (int n = 0; n < C::NV; ++n) {
+        const int row = warp * 16 + n * C::RPL + sub;
+        S[n] = load4(Sin + size_t(row) * D + 4 * c4);
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int idx = threadIdx.x + u * C::NT;
+        if (idx < 3 * D) {
+            const int s = idx / D, c = idx - s * D;
+            const int ch = s * p.H * D + h * D + c;
             xv[u][0] = tail_in[ch];
             xv[u][1] = tail_in[p.n_ch + ch];
             xv[u][2] = tail_in[2 * p.n_ch + ch];
-            xv[u][3] = src[size_t(b) * T * p.H * D + size_t(h) * D + c];
         }
     }
 #pragma unroll
@@ -309,8 +323,17 @@ kda_status launch_d(const StepParams &p, cudaStream_t stream) {
                                         int(step_smem_bytes<D, Act>(kMaxVerifyT)));
     });
     if (attr_err != cudaSuccess) return KDA_ERR_CUDA;
-    kern<<<unsigned(p.B) * unsigned(p.H), C::NT, step_smem_bytes<D, Act>(p.T), stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(p.B) * unsigned(p.H), 1, 1);
+    cfg.blockDim = dim3(C::NT, 1, 1);
+    cfg.dynamicSmemBytes = step_smem_bytes<D, Act>(p.T);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 template <typename Act>

@@ -165,6 +165,11 @@ KDA_API kda_status kda_check_slots(const kda_pool *pool, const int32_t *in_slots
  * pool sets KDA_DEVERR_SLOT_RANGE and that sequence is skipped.  Slots must be
  * distinct (check with kda_check_slots).  B = 0 is a no-op.
  * One launch: conv, L2, update, readout and gated norm are fused.
+ * Consecutive kda_decode / kda_verify launches on one stream overlap by
+ * programmatic dependent launch: a launch reads its slot tables, weights and
+ * token inputs while the previous one finishes, and reads the pool only
+ * after it has completed.  So token inputs must not be written by the
+ * immediately preceding kda_decode / kda_verify launch on the stream.
  * Source: "vLLM Kimi K3 지원", section "Fused Kernels 및 메타데이터 최적화",
  * KDA Decode bullet. */
 KDA_API kda_status kda_decode(kda_pool *pool, const kda_weights *w, const kda_io *io,
