@@ -131,10 +131,6 @@ kda_step_kernel(const StepParams p) {
         if (threadIdx.x == 0) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
         return;
     }
-    // Programmatic dependent launch: the next step-kernel launch on this
-    // stream may start now and run its own prologue up to its
-    // griddepcontrol.wait, which waits for this grid to complete.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int sub = lane / C::LPR, c4 = lane % C::LPR;
     // Per-token inputs of the first token (not written by a preceding step
@@ -296,6 +292,12 @@ kda_step_kernel(const StepParams p) {
 
     // Gated RMSNorm of every token over the head's D value channels.
     __syncthreads();
+    // Programmatic dependent launch: the next step-kernel launch on this
+    // stream may start now and run its own prologue up to its
+    // griddepcontrol.wait, which waits for this grid to complete.  Measured
+    // at batch 1 (graph of 1000 steps, same GPU): 5.3 us per step with the
+    // trigger here, 6.2 us with it at kernel start, 6.0 us without it.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const float wn = to_f32(static_cast<const Act *>(p.norm_w)[own_j]);
     for (int t = 0; t < T; ++t) {
         float tot = 0.f;
