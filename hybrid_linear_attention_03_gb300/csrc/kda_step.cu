@@ -32,6 +32,7 @@
 // was measured slower at every batch size tried (batch 1..16, T = 1 and 8):
 // the cluster barriers cost more than the shorter per-CTA state stream saved.
 #include "kda_internal.h"
+#include "kda_sm100.cuh"
 
 #include <mutex>
 
@@ -92,10 +93,17 @@ struct RowReduce {
     }
 };
 
+// Snapshot staging (multi-token launches only): 16 rows x D floats per warp,
+// placed first in dynamic shared memory so every warp's block starts on a
+// 16-byte boundary (bulk copies need it); D*D*4 bytes is a multiple of 16.
+template <int D>
+__host__ __device__ constexpr size_t stage_floats(int T) { return T > 1 ? size_t(D) * D : 0; }
+
 template <int D, typename Act>
 __host__ __device__ constexpr size_t step_smem_bytes(int T) {
     constexpr int WPC = D / 16;
-    return sizeof(float) * (size_t(T) * 3 * D     // conv outputs
+    return sizeof(float) * (stage_floats<D>(T)    // snapshot staging
+                            + size_t(T) * 3 * D   // conv outputs
                             + WPC * 16            // u row buffer
                             + size_t(T) * D       // o per token
                             + size_t(T) * D       // gate logits per token
@@ -109,7 +117,8 @@ kda_step_kernel(const StepParams p) {
     using C = StepCfg<D>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int T = p.T;
-    float *conv = reinterpret_cast<float *>(smem_raw);  // [T][3][D]
+    float *stage_all = reinterpret_cast<float *>(smem_raw);  // [D][D] if T > 1 (16 rows per warp)
+    float *conv = stage_all + stage_floats<D>(T);            // [T][3][D]
     float *ubuf = conv + size_t(T) * 3 * D;              // [WPC][16]
     float *obuf = ubuf + C::WPC * 16;                    // [T][D]
     float *gbuf = obuf + size_t(T) * D;                  // [T][D]
@@ -273,13 +282,35 @@ kda_step_kernel(const StepParams p) {
             sq[t * C::WPC + warp] = a;
         }
 
-        // Snapshot: this warp's state rows and its share of the conv tail.
+        // Snapshot.  A single-token launch stores its rows directly (in
+        // place).  With several drafts the snapshot stream dominates: this
+        // warp's 16 state rows are one contiguous 16*D*4-byte block in HBM,
+        // staged in shared memory and handed to the TMA engine as one bulk
+        // store, which keeps the warp's load/store pipe free (batch 64 x 8
+        // drafts: 613 -> 527 us per launch on GB300; a single token got
+        // slower, so it keeps direct stores).  The staging buffer is reused
+        // once the previous bulk store has finished reading it.
         const int snap = p.snap_slots[b * T + t];
         float *Sout = p.states + size_t(snap) * slot_elems + size_t(h) * head_elems;
+        if (T == 1) {
 #pragma unroll
-        for (int n = 0; n < C::NV; ++n) {
-            float4 *dst = reinterpret_cast<float4 *>(Sout + size_t(warp * 16 + n * C::RPL + sub) * D + 4 * c4);
-            if (T > 1) __stcs(dst, S[n]); else *dst = S[n];
+            for (int n = 0; n < C::NV; ++n)
+                *reinterpret_cast<float4 *>(Sout + size_t(warp * 16 + n * C::RPL + sub) * D + 4 * c4) = S[n];
+        } else {
+            float *stage = stage_all + size_t(warp) * 16 * D;
+            if (t > 0) {
+                if (lane == 0) sm100::bulk_wait_read();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int n = 0; n < C::NV; ++n)
+                *reinterpret_cast<float4 *>(stage + (n * C::RPL + sub) * D + 4 * c4) = S[n];
+            sm100::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                sm100::bulk_store(Sout + size_t(warp) * 16 * D, stage, 16 * D * sizeof(float));
+                sm100::bulk_commit();
+            }
         }
         Act *tail_out = tails + size_t(snap) * 3 * p.n_ch;
         for (int idx = lane; idx < 9 * 16; idx += 32) {  // 3 taps x 3 streams x this warp's 16 channels
@@ -290,6 +321,9 @@ kda_step_kernel(const StepParams p) {
         __syncwarp();  // ubuf is rewritten by the next token
     }
 
+    // The staging buffers must stay valid until the bulk stores have read
+    // them (their writes land before the grid completes).
+    if (T > 1 && lane == 0) sm100::bulk_wait_read();
     // Gated RMSNorm of every token over the head's D value channels.
     __syncthreads();
     // Programmatic dependent launch: the next step-kernel launch on this
