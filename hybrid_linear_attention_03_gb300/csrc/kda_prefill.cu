@@ -56,6 +56,8 @@ constexpr int CH = 64;   // chunk length
 constexpr int HALO = 3;  // previous raw inputs the width-4 conv needs
 constexpr float kLogAlphaMin = -100.0f;  // log(alpha) floor: alpha below e^-100 acts as e^-100
 constexpr float kSafeSpan = 160.0f;      // max per-channel log-decay span for the split exponent
+constexpr int kMaxWindows = 8;           // chunk windows overlapped across two streams
+constexpr int kMinWindowChunks = 32;     // smallest window worth a separate chain launch
 
 struct SeqMeta {
     int32_t row0, len, slot, has_init, chunk0, n_chunks;
@@ -103,6 +105,8 @@ struct PrefillParams {
     void *out;
     const void *conv_w, *norm_w;
     int32_t H, n_ch, n_seqs, n_chunks, n_ckpts;
+    int32_t chunk_base;      // prep / intra: global index of blockIdx.x == 0
+    int32_t win_lo, win_hi;  // chain: global chunk range of this launch
     float eps_l2, eps_rms;
 };
 
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(128) prefill_prep_kernel(const PrefillParams p
     Act *tv = reinterpret_cast<Act *>(sm + 2 * TILE);
     Act *ta = reinterpret_cast<Act *>(sm + 3 * TILE);
     __shared__ uint64_t bar;
-    const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const ChunkMeta cm = p.chunks[g];
     const SeqMeta sq = p.seqs[cm.seq];
     char *rec = rec_ptr(p, g, h);
@@ -252,7 +256,7 @@ constexpr uint32_t IN0 = 98304;   // QH, then VV, then the W image staging (32 K
 constexpr uint32_t KH = 131072;   // fp32 [64][128]
 constexpr uint32_t GG = 163840;   // fp32 [64][128]
 constexpr uint32_t SMALL = 196608;
-constexpr uint32_t BYTES = SMALL + 2048;
+constexpr uint32_t BYTES = SMALL + 2560;
 constexpr int NT = 256;
 }  // namespace is
 
@@ -303,9 +307,11 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
 __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *cref = reinterpret_cast<float *>(sm + is::SMALL);  // [128]
+    float *cref = reinterpret_cast<float *>(sm + is::SMALL);  // [128] c = mid of the log-decay range
     float *beta = cref + D;                                    // [64]
     int *flag = reinterpret_cast<int *>(beta + CH);            // [1]
+    float *ec = reinterpret_cast<float *>(sm + is::SMALL + 1536);  // [128] exp(c)
+    float *elc = ec + D;                                           // [128] exp(G_last - c)
     uint32_t *tbase = reinterpret_cast<uint32_t *>(flag + 1);  // [1]
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + is::SMALL + 1024);
     uint64_t *bar_mma = bar_ld + 1;
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     const float *VVs = reinterpret_cast<const float *>(sm + is::IN0);
     const float *KHs = reinterpret_cast<const float *>(sm + is::KH);
     const float *GGs = reinterpret_cast<const float *>(sm + is::GG);
-    const int g = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     char *rec = rec_ptr(p, g, h);
     const uint32_t sbase = smem_u32(sm);
     if (tid == 0) {
@@ -336,30 +342,48 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     uint32_t mma_phase = 0;
     if (ok && tid < D) {
         const float g0 = GGs[tid], gl = GGs[(CH - 1) * D + tid];
-        cref[tid] = 0.5f * (g0 + gl);
+        const float c = 0.5f * (g0 + gl);
+        cref[tid] = c;
+        ec[tid] = expf(c);
+        elc[tid] = expf(gl - c);
         at<float>(rec, Rec::GAM)[tid] = expf(gl);
         if (g0 - gl > kSafeSpan) atomicOr(flag, 1);
     }
     __syncthreads();
     const bool exact = *flag != 0;
+    // Within the safe span every decay factor of the chunk derives from one
+    // exponential per element, E = exp(G - c) in [e^-80, e^80]:
+    //   exp(G_r - c), exp(c - G_s) = 1/E, exp(G) = E e^c, exp(G_last - G) = e^(G_last - c) / E.
+    // G is replaced by E in place.  The exact path keeps G.
+    float *EE = reinterpret_cast<float *>(sm + is::GG);
+    if (ok && !exact) {
+        for (int e4 = tid; e4 < CH * D / 4; e4 += is::NT) {
+            const int i0 = (e4 * 4) % D;
+            float4 g = ld4(GGs + 4 * e4);
+            g.x = expf(g.x - cref[i0]);
+            g.y = expf(g.y - cref[i0 + 1]);
+            g.z = expf(g.z - cref[i0 + 2]);
+            g.w = expf(g.w - cref[i0 + 3]);
+            *reinterpret_cast<float4 *>(EE + 4 * e4) = g;
+        }
+        __syncthreads();
+    }
 
     // ---- phase 1: X = [K exp(G - c); Q exp(G - c)], Kb = K exp(c - G) -> A, P
     if (ok && !exact) {
         build_image(sm + is::X_HI, sm + is::X_LO, 128, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
-            float a[8], gg[8], cr[8];
+            float a[8], ee[8];
             ld8(r < CH ? KHs + r * D + k0 : QHs + (r - CH) * D + k0, a);
-            ld8(GGs + (r & (CH - 1)) * D + k0, gg);
-            ld8(cref + k0, cr);
+            ld8(EE + (r & (CH - 1)) * D + k0, ee);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(gg[e] - cr[e]);
+            for (int e = 0; e < 8; ++e) x[e] = a[e] * ee[e];
         });
         build_image(sm + is::KB_HI, sm + is::KB_LO, CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
-            float a[8], gg[8], cr[8];
+            float a[8], ee[8];
             ld8(KHs + r * D + k0, a);
-            ld8(GGs + r * D + k0, gg);
-            ld8(cref + k0, cr);
+            ld8(EE + r * D + k0, ee);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(cr[e] - gg[e]);
+            for (int e = 0; e < 8; ++e) x[e] = a[e] / ee[e];
         });
         fence_proxy_async_smem();
         tc_fence_before();
@@ -375,18 +399,22 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     if (ok) {
         build_image(reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI), reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO),
                     CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
-                        float a[8], gg[8];
+                        float a[8], gg[8], cc[8];
                         ld8(QHs + r * D + k0, a);
-                        ld8(GGs + r * D + k0, gg);
+                        ld8(GGs + r * D + k0, gg);  // E when !exact, G when exact
+                        ld8(ec + k0, cc);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(gg[e]);
+                        for (int e = 0; e < 8; ++e) x[e] = a[e] * (exact ? expf(gg[e]) : gg[e] * cc[e]);
                     }, CH, 2 * CH);
         build_image<true>(reinterpret_cast<unsigned char *>(rec + Rec::KP_HI),
                     reinterpret_cast<unsigned char *>(rec + Rec::KP_LO), D, 8, tid, is::NT,
                     [&](int i, int r0, float(&x)[8]) {
-                        const float gl = GGs[(CH - 1) * D + i];
+                        const float gl = GGs[(CH - 1) * D + i], l = elc[i];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = KHs[(r0 + e) * D + i] * expf(gl - GGs[(r0 + e) * D + i]);
+                        for (int e = 0; e < 8; ++e) {
+                            const float gv = GGs[(r0 + e) * D + i];
+                            x[e] = KHs[(r0 + e) * D + i] * (exact ? expf(gl - gv) : l / gv);
+                        }
                     });
     }
     __syncthreads();
@@ -489,8 +517,12 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
             ld8(T + r * CH + s0, x);
         });
         build_image<true>(sm + is::AK_HI, sm + is::AK_LO, D, 8, tid, is::NT, [&](int i, int s0, float(&x)[8]) {
+            const float cc = ec[i];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * expf(GGs[(s0 + e) * D + i]) * KHs[(s0 + e) * D + i];
+            for (int e = 0; e < 8; ++e) {
+                const float gv = GGs[(s0 + e) * D + i];
+                x[e] = beta[s0 + e] * (exact ? expf(gv) : gv * cc) * KHs[(s0 + e) * D + i];
+            }
         });
         build_image<true>(sm + is::AV_HI, sm + is::AV_LO, D, 8, tid, is::NT, [&](int j, int s0, float(&x)[8]) {
 #pragma unroll
@@ -573,6 +605,14 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
     const int tid = threadIdx.x, warp = tid >> 5, j = tid;  // j: value channel = TMEM lane
     const int h = blockIdx.x % p.H, n = blockIdx.x / p.H;
     const SeqMeta sq = p.seqs[n];
+    // The chunks of this sequence inside the launch's window [win_lo, win_hi).
+    // A sequence with no chunks is settled by the window that starts at 0.
+    const int c_lo = max(sq.chunk0, p.win_lo) - sq.chunk0;
+    const int c_hi = min(sq.chunk0 + sq.n_chunks, p.win_hi) - sq.chunk0;
+    if (c_hi <= c_lo && !(sq.n_chunks == 0 && p.win_lo == 0)) return;
+    // A window that continues a sequence reads the state the previous window
+    // left in the slot.
+    const bool load_state = sq.has_init || c_lo > 0;
     const size_t head_elems = size_t(D) * D;
     float *slot_state = p.states + size_t(sq.slot) * p.H * head_elems + size_t(h) * head_elems;  // S^T [j][i]
     const uint32_t sbase = smem_u32(sm);
@@ -585,8 +625,8 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tbase, tl = tm + (uint32_t(warp * 32) << 16);
-    if (tid == 0 && sq.n_chunks > 0) {
-        const char *r0 = rec_ptr(p, sq.chunk0, h);
+    if (tid == 0 && c_hi > c_lo) {
+        const char *r0 = rec_ptr(p, sq.chunk0 + c_lo, h);
         mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
         bulk_load(sm + cs::B1, r0 + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
         mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
@@ -597,7 +637,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         float v[16];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
-            const float4 x = sq.has_init ? ld4(slot_state + size_t(j) * D + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 x = load_state ? ld4(slot_state + size_t(j) * D + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
             v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
         }
         tmem_st16(tl + 320 + c0, v);
@@ -620,10 +660,10 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
     tc_fence_after();
     bool ok = true;
     const uint32_t id128 = idesc_bf16_f32(128, 2 * CH), id192 = idesc_bf16_f32(128, D + CH);
-    for (int c = 0; c < sq.n_chunks && ok; ++c) {
+    for (int c = c_lo; c < c_hi && ok; ++c) {
         const int g = sq.chunk0 + c;
         char *rec = rec_ptr(p, g, h);
-        const uint32_t par = uint32_t(c & 1);
+        const uint32_t par = uint32_t((c - c_lo) & 1);
         ok = __syncthreads_and(mbar_wait(bar_b1, par, p.err));
         if (!ok) break;
         if (tid == 0) {
@@ -640,7 +680,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         ok = __syncthreads_and(mbar_wait(bar_m1, par, p.err));
         if (!ok) break;
         tc_fence_after();
-        if (tid == 0 && c + 1 < sq.n_chunks) {  // W and Q images are consumed: stream in the next chunk's
+        if (tid == 0 && c + 1 < c_hi) {  // W and Q images are consumed: stream in the next chunk's
             mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
             bulk_load(sm + cs::B1, rec_ptr(p, g + 1, h) + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
         }
@@ -677,7 +717,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         ok = __syncthreads_and(mbar_wait(bar_m2, par, p.err));
         if (!ok) break;
         tc_fence_after();
-        if (tid == 0 && c + 1 < sq.n_chunks) {  // K^T, P images and gamma consumed
+        if (tid == 0 && c + 1 < c_hi) {  // K^T, P images and gamma consumed
             mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
             bulk_load(sm + cs::B2, rec_ptr(p, g + 1, h) + Rec::KP_HI, Rec::B2_BYTES, bar_b2);
         }
@@ -882,24 +922,90 @@ constexpr size_t prep_smem() {
 constexpr size_t kIntraSmem = 1024 + is::BYTES;
 constexpr size_t kChainSmem = 1024 + cs::BYTES;
 
+// Per-device side stream (highest priority) and events for the windowed
+// overlap of the chain with the per-chunk kernels.  Not memory: nothing here
+// allocates device memory.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t ev[2 * kMaxWindows + 1] = {};
+    bool ok = false;
+};
+
+SideStream *side_stream() {
+    static SideStream per_dev[64];
+    static std::once_flag once[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::call_once(once[dev], [dev] {
+        SideStream &x = per_dev[dev];
+        int lo = 0, hi = 0;
+        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return;
+        if (cudaStreamCreateWithPriority(&x.s, cudaStreamNonBlocking, hi) != cudaSuccess) return;
+        for (auto &e : x.ev)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return;
+        x.ok = true;
+    });
+    return per_dev[dev].ok ? &per_dev[dev] : nullptr;
+}
+
 template <typename Act>
-kda_status launch_act(const PrefillParams &p, const kda_io *io, int n_tok, int N, long long n_chunks, int n_reqs,
+kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int N, long long n_chunks, int n_reqs,
                       cudaStream_t stream) {
     kda_status st;
     if ((st = set_smem(prefill_prep_kernel<Act>, prep_smem<Act>())) != KDA_OK) return st;
     if ((st = set_smem(prefill_intra_kernel, kIntraSmem)) != KDA_OK) return st;
     if ((st = set_smem(prefill_chain_kernel, kChainSmem)) != KDA_OK) return st;
+    PrefillParams p = p0;
+    CUtensorMap mq, mk, mv, ma;
     if (n_chunks > 0) {
-        CUtensorMap mq, mk, mv, ma;
         const int es = int(sizeof(Act));
         if (!make_map(&mq, io->q, n_tok, p.H, es, CH + HALO) || !make_map(&mk, io->k, n_tok, p.H, es, CH + HALO) ||
             !make_map(&mv, io->v, n_tok, p.H, es, CH + HALO) || !make_map(&ma, io->alpha, n_tok, p.H, es, CH))
             return KDA_ERR_CUDA;
-        const dim3 grid(unsigned(n_chunks), unsigned(p.H));
-        prefill_prep_kernel<Act><<<grid, 128, prep_smem<Act>(), stream>>>(p, mq, mk, mv, ma);
-        prefill_intra_kernel<<<grid, is::NT, kIntraSmem, stream>>>(p);
     }
-    prefill_chain_kernel<<<unsigned(N) * p.H, 128, kChainSmem, stream>>>(p);
+    // Windows of chunks: the chain of window w (one CTA per sequence and
+    // head, on the side stream) runs while prep and intra of window w + 1
+    // fill the other SMs; events order each chain launch after its window's
+    // records and the final join returns everything to the caller's stream.
+    // The side stream's events are shared by every caller of this device:
+    // one call's record / wait sequence is enqueued as a whole.
+    static std::mutex enqueue_mu;
+    std::lock_guard<std::mutex> lock(enqueue_mu);
+    SideStream *side = nullptr;
+    int n_win = 1;
+    if (n_chunks >= 2 * kMinWindowChunks) {
+        side = side_stream();
+        if (side) n_win = int(std::min<long long>(kMaxWindows, n_chunks / kMinWindowChunks));
+    }
+    const long long per = (n_chunks + n_win - 1) / n_win;
+    cudaStream_t cs = side ? side->s : stream;
+    if (side) {  // the side stream starts after everything already on the caller's stream
+        if (cudaEventRecord(side->ev[2 * kMaxWindows], stream) != cudaSuccess ||
+            cudaStreamWaitEvent(cs, side->ev[2 * kMaxWindows], 0) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    for (int w = 0; w < n_win; ++w) {
+        const long long lo = std::min(n_chunks, w * per), hi = std::min(n_chunks, (w + 1) * per);
+        if (hi > lo) {
+            p.chunk_base = int(lo);
+            const dim3 grid(unsigned(hi - lo), unsigned(p.H));
+            prefill_prep_kernel<Act><<<grid, 128, prep_smem<Act>(), stream>>>(p, mq, mk, mv, ma);
+            prefill_intra_kernel<<<grid, is::NT, kIntraSmem, stream>>>(p);
+        }
+        p.win_lo = int(lo);
+        p.win_hi = (w + 1 == n_win) ? int(n_chunks) : int(hi);
+        if (side) {
+            if (cudaEventRecord(side->ev[w], stream) != cudaSuccess || cudaStreamWaitEvent(cs, side->ev[w], 0) != cudaSuccess)
+                return KDA_ERR_CUDA;
+        }
+        prefill_chain_kernel<<<unsigned(N) * p.H, 128, kChainSmem, cs>>>(p);
+    }
+    if (side) {
+        if (cudaEventRecord(side->ev[kMaxWindows], cs) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, side->ev[kMaxWindows], 0) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    p.chunk_base = 0;
     if (n_chunks > 0) prefill_out_kernel<Act><<<dim3(unsigned(n_chunks), unsigned(p.H)), 128, 0, stream>>>(p);
     if (n_reqs > 0) prefill_tails_kernel<Act><<<n_reqs, 256, 0, stream>>>(p, 1);
     prefill_tails_kernel<Act><<<N, 256, 0, stream>>>(p, 0);
@@ -966,6 +1072,9 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
                                         cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
     PrefillParams p;
+    p.chunk_base = 0;
+    p.win_lo = 0;
+    p.win_hi = int(n_chunks);
     p.seqs = reinterpret_cast<const SeqMeta *>(ws + L.seqs);
     p.chunks = reinterpret_cast<const ChunkMeta *>(ws + L.chunks);
     p.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.ckpts);

@@ -138,3 +138,17 @@ def test_prefill_host_errors():
     assert e.value.status == kda.KDA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.all(m.gpu.states() == 0)
+
+
+def test_prefill_across_chunk_windows_matches_oracle():
+    """72 chunks (3 sequences) run as two chunk windows whose chain launches
+    overlap the next window's per-chunk kernels; sequence 1 straddles the
+    window boundary and continues from its slot.  Checkpoints on both sides."""
+    H, act = 2, torch.bfloat16
+    lens = [2000, 1500, 1000]
+    m = Mirror(16, H, D, act, I.layer_weights(59, H, D, D, 4, act))
+    inp = I.token_inputs(59, 0, sum(lens), H, D, D, 3.0, act)
+    reqs = [(0, 1024, 8), (1, 192, 9), (1, 1408, 10), (1, 1500, 11), (2, 1000, 12)]
+    out = prefill_gpu(m, hp.to_device(inp), lens, [0, 1, 2], [0, 0, 0], reqs)
+    ref = prefill_oracle(m, inp, lens, [0, 1, 2], [0, 0, 0], reqs)
+    _check(m, out, ref, [0, 1, 2], reqs)
