@@ -299,6 +299,29 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
     }
 }
 
+// One level of the blocked inverse of I + A: the 4 - d blocks at distance d
+// below the diagonal, with fixed-length (unrolled) dot products.
+template <int d>
+__device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS, int tid) {
+    constexpr int nblk = 4 - d;
+    for (int e = tid; e < nblk * 256; e += is::NT) {
+        const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < 16 * d; ++s) acc = fmaf(A[(a * 16 + r) * CH + b * 16 + s], T[(b * 16 + s) * CH + b * 16 + cc], acc);
+        XS[(a * 16 + r) * CH + b * 16 + cc] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < nblk * 256; e += is::NT) {
+        const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < 16; ++s) acc = fmaf(-T[(a * 16 + r) * CH + a * 16 + s], XS[(a * 16 + s) * CH + b * 16 + cc], acc);
+        T[(a * 16 + r) * CH + b * 16 + cc] = acc;
+    }
+    __syncthreads();
+}
+
 // One CTA (8 warps) per (chunk, head).  The prep record's q, k and G arrive
 // by TMA bulk copies (v follows once q is consumed), so every operand build
 // reads shared memory.  Images the chain needs that involve no MMA (exp(G).q,
@@ -383,7 +406,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
             ld8(KHs + r * D + k0, a);
             ld8(EE + r * D + k0, ee);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = a[e] / ee[e];
+            for (int e = 0; e < 8; ++e) x[e] = __fdividef(a[e], ee[e]);  // ee in [e^-80, e^80]
         });
         fence_proxy_async_smem();
         tc_fence_before();
@@ -413,7 +436,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const float gv = GGs[(r0 + e) * D + i];
-                            x[e] = KHs[(r0 + e) * D + i] * (exact ? expf(gl - gv) : l / gv);
+                            x[e] = KHs[(r0 + e) * D + i] * (exact ? expf(gl - gv) : __fdividef(l, gv));
                         }
                     });
     }
@@ -482,34 +505,30 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     // ---- T = (I + A)^-1 (unit lower triangular), 16 x 16 blocks
     float *T = reinterpret_cast<float *>(sm + is::T_F32);
     float *XS = reinterpret_cast<float *>(sm + is::XS_F32);
-    for (int e = tid; e < CH * CH; e += is::NT) T[e] = 0.f;
+    for (int e = tid; e < CH * CH; e += is::NT) T[e] = 0.f;  // the blocks above the diagonal stay 0
     __syncthreads();
-    if (warp < 4 && lane < 16) {
-        const int b0 = warp * 16, c = b0 + lane;  // each lane reads only the column it writes
-        for (int r = b0; r < b0 + 16; ++r) {
+    // Diagonal 16 x 16 blocks by forward substitution, a lane per column with
+    // the column in registers (fully unrolled): lanes 0-15 of warp w take
+    // block 2w, lanes 16-31 block 2w + 1.  Rows above the lane's column come
+    // out 0 by themselves (every earlier entry of the column is 0).
+    if (warp < 2) {
+        const int b0 = (warp * 2 + (lane >> 4)) * 16, c = lane & 15;
+        float tc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
             float acc = (r == c) ? 1.f : 0.f;
-            for (int s = c; s < r; ++s) acc = fmaf(-A[r * CH + s], T[s * CH + c], acc);
-            T[r * CH + c] = (r >= c) ? acc : 0.f;
+#pragma unroll
+            for (int s = 0; s < r; ++s) acc = fmaf(-A[(b0 + r) * CH + b0 + s], tc[s], acc);
+            tc[r] = acc;
         }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) T[(b0 + r) * CH + b0 + c] = tc[r];
     }
     __syncthreads();
-    for (int d = 1; d < 4; ++d) {  // T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
-        const int nblk = 4 - d;
-        for (int e = tid; e < nblk * 256; e += is::NT) {
-            const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
-            float acc = 0.f;
-            for (int s = b * 16; s < a * 16; ++s) acc = fmaf(A[(a * 16 + r) * CH + s], T[s * CH + b * 16 + cc], acc);
-            XS[(a * 16 + r) * CH + b * 16 + cc] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < nblk * 256; e += is::NT) {
-            const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
-            float acc = 0.f;
-            for (int s = 0; s <= r; ++s) acc = fmaf(-T[(a * 16 + r) * CH + a * 16 + s], XS[(a * 16 + s) * CH + b * 16 + cc], acc);
-            T[(a * 16 + r) * CH + b * 16 + cc] = acc;
-        }
-        __syncthreads();
-    }
+    // Blocks below the diagonal, by distance d: T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
+    tri_offdiag<1>(A, T, XS, tid);
+    tri_offdiag<2>(A, T, XS, tid);
+    tri_offdiag<3>(A, T, XS, tid);
     // ---- phase 3: W^T = (beta exp(G) . K)^T T^T and Ut^T = (beta V)^T T^T
     ok = __syncthreads_and(ok && mbar_wait(bar_ld, 1, p.err));  // v has arrived
     if (ok) {
@@ -595,14 +614,17 @@ constexpr uint32_t BYTES = BARS + 512;
 static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
 
 // TMEM columns: [(W S)^T | (Q S)^T] [0,128), [(K^T U)^T | (P U)^T] [128,320), S^T [320,448)
-__global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar_b1 = reinterpret_cast<uint64_t *>(sm + cs::BARS);
     uint64_t *bar_b2 = bar_b1 + 1, *bar_m1 = bar_b1 + 2, *bar_m2 = bar_b1 + 3;
     uint32_t *tbase = reinterpret_cast<uint32_t *>(bar_b1 + 4);
     float *gcur = reinterpret_cast<float *>(sm + cs::GCUR);
-    const int tid = threadIdx.x, warp = tid >> 5, j = tid;  // j: value channel = TMEM lane
+    // 8 warps: warps w and w + 4 share TMEM lanes 32*(w % 4) .. +31 (value
+    // channel j = TMEM lane) and split every row's columns between them.
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j = (warp & 3) * 32 + lane, half = warp >> 2;
     const int h = blockIdx.x % p.H, n = blockIdx.x / p.H;
     const SeqMeta sq = p.seqs[n];
     // The chunks of this sequence inside the launch's window [win_lo, win_hi).
@@ -624,7 +646,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tm = *tbase, tl = tm + (uint32_t(warp * 32) << 16);
+    const uint32_t tm = *tbase, tl = tm + (uint32_t((warp & 3) * 32) << 16);
     if (tid == 0 && c_hi > c_lo) {
         const char *r0 = rec_ptr(p, sq.chunk0 + c_lo, h);
         mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
@@ -632,8 +654,9 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
         bulk_load(sm + cs::B2, r0 + Rec::KP_HI, Rec::B2_BYTES, bar_b2);
     }
+    const int sc0 = half * 64;  // this thread's 64 columns of the S^T row
     // S^T row j: fp32 into TMEM, hi/lo into the A1 images
-    for (int c0 = 0; c0 < D; c0 += 16) {
+    for (int c0 = sc0; c0 < sc0 + 64; c0 += 16) {
         float v[16];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
@@ -642,13 +665,13 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         }
         tmem_st16(tl + 320 + c0, v);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int hh = 0; hh < 2; ++hh) {
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = v[8 * half + e];
+            for (int e = 0; e < 8; ++e) x[e] = v[8 * hh + e];
             uint4 vh, vl;
             split8(x, vh, vl);
-            const uint32_t off = sw128_chunk(j, (c0 >> 3) + half, D);
+            const uint32_t off = sw128_chunk(j, (c0 >> 3) + hh, D);
             *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
             *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
         }
@@ -660,6 +683,7 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
     tc_fence_after();
     bool ok = true;
     const uint32_t id128 = idesc_bf16_f32(128, 2 * CH), id192 = idesc_bf16_f32(128, D + CH);
+    const int uc0 = half * 32;  // this thread's 32 columns of the U / O rows
     for (int c = c_lo; c < c_hi && ok; ++c) {
         const int g = sq.chunk0 + c;
         char *rec = rec_ptr(p, g, h);
@@ -672,11 +696,11 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
                  id128, false);
             mma_commit(bar_m1);
         }
-        // Ut^T row j while the MMAs run
-        float ut[CH];
+        // Ut row entries (r = uc0 .. uc0 + 31, column j) while the MMAs run
+        float ut[32];
         const float *UTg = reinterpret_cast<const float *>(rec + Rec::UT) + j;  // column j, coalesced
 #pragma unroll
-        for (int e = 0; e < CH; ++e) ut[e] = UTg[e * D];
+        for (int e = 0; e < 32; ++e) ut[e] = UTg[(uc0 + e) * D];
         ok = __syncthreads_and(mbar_wait(bar_m1, par, p.err));
         if (!ok) break;
         tc_fence_after();
@@ -684,27 +708,27 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
             mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
             bulk_load(sm + cs::B1, rec_ptr(p, g + 1, h) + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
         }
-        // U^T row j = Ut^T - (W S)^T  -> hi/lo images (all 64 columns in one TMEM round trip)
+        // U^T row j = Ut^T - (W S)^T  -> hi/lo images (this thread's 32 columns)
         {
-            float v[4][16];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld16(tl + 16 * q, v[q]);
+            float v[2][16];
+            tmem_ld16(tl + uc0, v[0]);
+            tmem_ld16(tl + uc0 + 16, v[1]);
             tmem_wait_ld();
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
+            for (int cc = 0; cc < 4; ++cc) {
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = ut[8 * cc + e] - v[cc >> 1][8 * (cc & 1) + e];
                 uint4 vh, vl;
                 split8(x, vh, vl);
-                const uint32_t off = sw128_chunk(j, cc, D);
+                const uint32_t off = sw128_chunk(j, (uc0 >> 3) + cc, D);
                 *reinterpret_cast<uint4 *>(sm + cs::A2_HI + off) = vh;
                 *reinterpret_cast<uint4 *>(sm + cs::A2_LO + off) = vl;
             }
         }
         ok = __syncthreads_and(mbar_wait(bar_b2, par, p.err));
         if (!ok) break;
-        gcur[j] = reinterpret_cast<const float *>(sm + cs::GAM)[j];
+        if (half == 0) gcur[j] = reinterpret_cast<const float *>(sm + cs::GAM)[j];
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -721,24 +745,24 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
             mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
             bulk_load(sm + cs::B2, rec_ptr(p, g + 1, h) + Rec::KP_HI, Rec::B2_BYTES, bar_b2);
         }
-        // O column j -> record (rows r), coalesced across the warp
-        float *O = reinterpret_cast<float *>(rec + Rec::OO);
-        for (int h2 = 0; h2 < 2; ++h2) {  // O = (Q S)^T + (P U)^T
+        // O column j (rows uc0 .. uc0 + 31) = (Q S)^T + (P U)^T -> record, coalesced across the warp
+        {
+            float* O = reinterpret_cast<float *>(rec + Rec::OO);
             float v[2][16], w2[2][16];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                tmem_ld16(tl + 64 + 32 * h2 + 16 * q, v[q]);
-                tmem_ld16(tl + 256 + 32 * h2 + 16 * q, w2[q]);
+                tmem_ld16(tl + 64 + uc0 + 16 * q, v[q]);
+                tmem_ld16(tl + 256 + uc0 + 16 * q, w2[q]);
             }
             tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 2; ++q)
 #pragma unroll
-                for (int e = 0; e < 16; ++e) O[(32 * h2 + 16 * q + e) * D + j] = v[q][e] + w2[q][e];
+                for (int e = 0; e < 16; ++e) O[(uc0 + 16 * q + e) * D + j] = v[q][e] + w2[q][e];
         }
         // S^T row j <- gamma . S^T row j + (K^T U)^T row j; refresh the A1 images
         const ChunkMeta cm = p.chunks[g];
-        for (int c0 = 0; c0 < D; c0 += 32) {  // 32 columns per TMEM round trip
+        for (int c0 = sc0; c0 < sc0 + 64; c0 += 32) {  // 32 columns per TMEM round trip
             float s[2][16], ds[2][16];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -752,13 +776,13 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
                 for (int e = 0; e < 16; ++e) s[q][e] = fmaf(gcur[c0 + 16 * q + e], s[q][e], ds[q][e]);
                 tmem_st16(tl + 320 + c0 + 16 * q, s[q]);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int hh = 0; hh < 2; ++hh) {
                     float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = s[q][8 * half + e];
+                    for (int e = 0; e < 8; ++e) x[e] = s[q][8 * hh + e];
                     uint4 vh, vl;
                     split8(x, vh, vl);
-                    const uint32_t off = sw128_chunk(j, ((c0 + 16 * q) >> 3) + half, D);
+                    const uint32_t off = sw128_chunk(j, ((c0 + 16 * q) >> 3) + hh, D);
                     *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
                     *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
                 }
@@ -778,9 +802,9 @@ __global__ void __launch_bounds__(128) prefill_chain_kernel(const PrefillParams 
         __syncthreads();
         tc_fence_after();
     }
-    // end state S^T row j -> slot
+    // end state S^T row j (this thread's 64 columns) -> slot
     if (ok) {
-        for (int c0 = 0; c0 < D; c0 += 16) {
+        for (int c0 = sc0; c0 < sc0 + 64; c0 += 16) {
             float s[16];
             tmem_ld16(tl + 320 + c0, s);
             tmem_wait_ld();
@@ -998,7 +1022,7 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
             if (cudaEventRecord(side->ev[w], stream) != cudaSuccess || cudaStreamWaitEvent(cs, side->ev[w], 0) != cudaSuccess)
                 return KDA_ERR_CUDA;
         }
-        prefill_chain_kernel<<<unsigned(N) * p.H, 128, kChainSmem, cs>>>(p);
+        prefill_chain_kernel<<<unsigned(N) * p.H, 256, kChainSmem, cs>>>(p);
     }
     if (side) {
         if (cudaEventRecord(side->ev[kMaxWindows], cs) != cudaSuccess ||
