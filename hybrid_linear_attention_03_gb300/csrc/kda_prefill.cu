@@ -300,24 +300,40 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
 }
 
 // One level of the blocked inverse of I + A: the 4 - d blocks at distance d
-// below the diagonal, with fixed-length (unrolled) dot products.
+// below the diagonal, with fixed-length (unrolled) dot products; a thread
+// owns 4 adjacent columns of one row, so each A value it loads feeds 4 FMAs
+// and the T / X values arrive as 16-byte vectors.
 template <int d>
 __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS, int tid) {
     constexpr int nblk = 4 - d;
-    for (int e = tid; e < nblk * 256; e += is::NT) {
-        const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
-        float acc = 0.f;
+    for (int e = tid; e < nblk * 64; e += is::NT) {
+        const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4, a = blk + d, b = blk;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s = 0; s < 16 * d; ++s) acc = fmaf(A[(a * 16 + r) * CH + b * 16 + s], T[(b * 16 + s) * CH + b * 16 + cc], acc);
-        XS[(a * 16 + r) * CH + b * 16 + cc] = acc;
+        for (int s = 0; s < 16 * d; ++s) {
+            const float av = A[(a * 16 + r) * CH + b * 16 + s];
+            const float4 tv = ld4(T + (b * 16 + s) * CH + b * 16 + c4);
+            acc.x = fmaf(av, tv.x, acc.x);
+            acc.y = fmaf(av, tv.y, acc.y);
+            acc.z = fmaf(av, tv.z, acc.z);
+            acc.w = fmaf(av, tv.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(XS + (a * 16 + r) * CH + b * 16 + c4) = acc;
     }
     __syncthreads();
-    for (int e = tid; e < nblk * 256; e += is::NT) {
-        const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15, a = blk + d, b = blk;
-        float acc = 0.f;
+    for (int e = tid; e < nblk * 64; e += is::NT) {
+        const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4, a = blk + d, b = blk;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s = 0; s < 16; ++s) acc = fmaf(-T[(a * 16 + r) * CH + a * 16 + s], XS[(a * 16 + s) * CH + b * 16 + cc], acc);
-        T[(a * 16 + r) * CH + b * 16 + cc] = acc;
+        for (int s = 0; s < 16; ++s) {
+            const float tv = -T[(a * 16 + r) * CH + a * 16 + s];
+            const float4 xv = ld4(XS + (a * 16 + s) * CH + b * 16 + c4);
+            acc.x = fmaf(tv, xv.x, acc.x);
+            acc.y = fmaf(tv, xv.y, acc.y);
+            acc.z = fmaf(tv, xv.z, acc.z);
+            acc.w = fmaf(tv, xv.w, acc.w);
+        }
+        *reinterpret_cast<float4 *>(T + (a * 16 + r) * CH + b * 16 + c4) = acc;
     }
     __syncthreads();
 }

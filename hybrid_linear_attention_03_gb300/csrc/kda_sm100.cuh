@@ -199,16 +199,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 }
 
 // Splits 8 fp32 values into bf16 hi = rn(x) and lo = rn(x - hi), packed as
-// two 16-byte vectors (x ~= hi + lo to about 16 mantissa bits).
+// two 16-byte vectors (x ~= hi + lo to about 16 mantissa bits).  Pairs are
+// converted with the packed bf16x2 round-to-nearest conversion.
 __device__ __forceinline__ void split8(const float (&x)[8], uint4 &hi, uint4 &lo) {
     uint32_t h[4], l[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * i]), h1 = __float2bfloat16_rn(x[2 * i + 1]);
-        const __nv_bfloat16 l0 = __float2bfloat16_rn(x[2 * i] - __bfloat162float(h0));
-        const __nv_bfloat16 l1 = __float2bfloat16_rn(x[2 * i + 1] - __bfloat162float(h1));
-        h[i] = uint32_t(__bfloat16_as_ushort(h0)) | (uint32_t(__bfloat16_as_ushort(h1)) << 16);
-        l[i] = uint32_t(__bfloat16_as_ushort(l0)) | (uint32_t(__bfloat16_as_ushort(l1)) << 16);
+        const __nv_bfloat162 hp = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        const float2 hf = __bfloat1622float2(hp);
+        const __nv_bfloat162 lp = __floats2bfloat162_rn(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);
+        h[i] = *reinterpret_cast<const uint32_t *>(&hp);
+        l[i] = *reinterpret_cast<const uint32_t *>(&lp);
     }
     hi = make_uint4(h[0], h[1], h[2], h[3]);
     lo = make_uint4(l[0], l[1], l[2], l[3]);
