@@ -19,8 +19,10 @@ For N > 1 launch under torchrun; each rank runs an independent replica
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -38,7 +40,42 @@ from hybrid_linear_attention_03_gb300 import inputs as I  # noqa: E402
 METRIC = "KDA decode tok/s (batch 1, H=64, d=128, 1000 chained steps)"
 UNIT = "tok/s"
 STEP_KERNEL = "kda_step_kernel"
+STEP_SOURCES = ("hybrid_linear_attention_03_gb300/csrc/kda_step.cu",
+                "hybrid_linear_attention_03_gb300/csrc/kda_sm100.cuh",
+                "hybrid_linear_attention_03_gb300/csrc/kda_internal.h")
 L2_FLUSH_BYTES = 512 << 20
+L2_NOTE = ("flushed before every timed launch: a 512 MiB buffer is written, then read, so the kernel "
+           "finds none of its data in L2 and no dirty line of the flush is left for it to write back")
+
+
+def flush_l2(buf):
+    """Evicts L2 by writing a buffer 4x its size, then reading it back (the
+    read makes the flush's own write-backs happen before the timed region)."""
+    buf.zero_()
+    return buf.view(torch.int64).sum()
+
+
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile):
+    """DRAM bytes per launch that an ncu summary under profiles/ records for
+    the step kernel, or None if the kernel's sources changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", profile)) as f:
+            text = f.read()
+    except OSError:
+        return None
+    sha = re.search(r"^source_sha256_16: ([0-9a-f]{16})", text, re.M)
+    tr = re.search(r"^traffic_bytes_per_launch: (\d+)", text, re.M)
+    if not sha or not tr or sha.group(1) != source_sha(STEP_SOURCES):
+        return None
+    return int(tr.group(1))
 
 
 def args_():
@@ -192,7 +229,7 @@ def run_ours(a, rank, world, local):
     def one_step():
         with torch.cuda.stream(stream):
             kda.kda_state_checkpoint(pool, [spare], [slot])
-            flush.zero_()
+            flush_l2(flush)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             graph.replay()
@@ -235,7 +272,7 @@ def run_ours(a, rank, world, local):
     def e2e_step():
         with torch.cuda.stream(stream):
             kda.kda_state_checkpoint(pool, [spare], [slot])
-            flush.zero_()
+            flush_l2(flush)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             for k, v in host_in.items():
@@ -261,12 +298,13 @@ def run_ours(a, rank, world, local):
         "config": {"workload": wl.name, "batch": 1, "heads": H, "d_k": D, "d_v": D, "io_dtype": "bf16",
                    "state_dtype": "f32", "pool_slots": wl.num_slots, "warm_tokens": wl.extra["warm"],
                    "decode_steps_per_bench_step": n_steps, "cuda_graph": True,
-                   "l2": "flushed (512 MiB write) between timed steps; within a step the 4 MiB state of the "
-                         "single sequence stays L2-resident across its 1000 chained decodes",
+                   "l2": "flushed between timed steps (512 MiB written, then read); within a step the 4 MiB "
+                         "state of the single sequence stays L2-resident across its 1000 chained decodes",
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": a.steps * n_steps,
         "roofline": {"bound": "hbm", "kernel": STEP_KERNEL, "achieved": round(achieved, 1), "peak": hbm_peak,
-                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": profiled_traffic("kda_step_decode_b1_dram.md"),
                      "bytes_per_launch": bytes_b1, "launch_us": round(launch_us, 3),
                      "note": f"peak = {peak_kind} HBM copy bandwidth; at batch 1 the state stays in L2 and the "
                              "launch is latency-bound; the HBM rooflines of this kernel are the batch-64 entries "
@@ -304,7 +342,8 @@ def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
     perm = torch.from_numpy(I.permutation(wl.seed, 0, wl.num_slots)).to(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    for name, T in (("decode_b64", 1), ("verify_b64_t8", 8)):
+    for name, T, profile in (("decode_b64", 1, "kda_step_decode_b64_full.md"),
+                             ("verify_b64_t8", 8, "kda_step_verify_b64_t8_dram.md")):
         if only is not None and name != only:
             continue
         toks = {k: v.to(dev) for k, v in wl.tokens(200, B * T).items()}
@@ -323,7 +362,7 @@ def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
             launch()
         times = []
         for _ in range(iters):
-            flush.zero_()
+            flush_l2(flush)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             launch()
@@ -337,8 +376,9 @@ def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
                      "gpu_launches": iters,
                      "roofline": {"bound": "hbm", "kernel": STEP_KERNEL, "achieved": round(ach, 1),
                                   "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
-                                  "traffic": None, "bytes_per_launch": byts, "peak_kind": peak_kind},
-                     "l2": "flushed before every timed launch"}
+                                  "traffic": profiled_traffic(profile), "bytes_per_launch": byts,
+                                  "peak_kind": peak_kind},
+                     "l2": L2_NOTE}
     st, flags = kda.kda_poll_device_error(pool)
     assert st == 0, f"device error word {flags:#x}"
     return res

@@ -24,11 +24,11 @@
 // operands in the 128-byte-swizzle K-major layout (kda_sm100.cuh).
 //
 // Kernels (one stream, in order):
-//   prep   (chunk, head): TMA loads the raw q, k, v, alpha tiles (with the
-//          3-token conv halo); conv + SiLU, L2 of q and k, G, beta.
-//   intra  (chunk, head): [K exp(G-c); Q exp(G-c)] x (K exp(c-G))^T -> A, P
-//          (one M=128 MMA); T = (I + A)^-1 on CUDA cores; W^T and Ut^T as
-//          M=128 MMAs; writes the chain's operand images.
+//   intra  (chunk, head): TMA loads the raw q, k, v, alpha tiles (with the
+//          3-token conv halo); conv + SiLU, L2 of q and k, G, beta in shared
+//          memory; [K exp(G-c); Q exp(G-c)] x (K exp(c-G))^T -> A, P (one
+//          M=128 MMA); T = (I + A)^-1 on CUDA cores; W^T and Ut^T as M=128
+//          MMAs; writes the chain's operand images.
 //   chain  (sequence, head): sequential over chunks; S^T (fp32) lives in
 //          TMEM; (W S)^T, (Q S)^T, (K^T U)^T and (P U)^T are MMAs; the next
 //          chunk's operand images stream in by TMA bulk copies while the
@@ -72,13 +72,8 @@ struct CkptMeta {
 // Per (chunk, head) workspace record (bytes).  "img" = bf16 operand image in
 // the 128-byte-swizzle K-major layout, [rows][K].
 struct Rec {
-    static constexpr size_t QH = 0;                  // fp32 [64][128] L2-normalised q
-    static constexpr size_t KH = QH + 32768;         // fp32 [64][128] L2-normalised k
-    static constexpr size_t VV = KH + 32768;         // fp32 [64][128] conv'd v
-    static constexpr size_t GG = VV + 32768;         // fp32 [64][128] cumulative log decay
-    static constexpr size_t BB = GG + 32768;         // fp32 [64] beta (0 on padding rows)
     // [W; exp(G) . q]: one 128-row image [r | 64 + r][128 i] (W rows 0..63, Q rows 64..127)
-    static constexpr size_t WQ_HI = BB + 1024;
+    static constexpr size_t WQ_HI = 0;
     static constexpr size_t WQ_LO = WQ_HI + 32768;
     // [(exp(G_last - G) . k)^T; P]: one 192-row image [i | 128 + r][64] (K^T rows 0..127, P rows 128..191)
     static constexpr size_t KP_HI = WQ_LO + 32768;
@@ -105,12 +100,15 @@ struct PrefillParams {
     void *out;
     const void *conv_w, *norm_w;
     int32_t H, n_ch, n_seqs, n_chunks, n_ckpts;
-    int32_t chunk_base;      // prep / intra: global index of blockIdx.x == 0
+    int32_t chunk_base;      // intra: global index of blockIdx.x == 0
     int32_t win_lo, win_hi;  // chain: global chunk range of this launch
     float eps_l2, eps_rms;
 };
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+// sigma(x) with the hardware exp2 / reciprocal approximations (relative error
+// a few 1e-7; 0 for x below about -88, where exp(-x) overflows to inf).
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ char *rec_ptr(const PrefillParams &p, int g, int h) {
     return p.rec + (size_t(g) * p.H + h) * Rec::BYTES;
@@ -143,108 +141,42 @@ __device__ __forceinline__ float4 act4<__nv_bfloat16>(const __nv_bfloat16 *p) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
-// ============================================================== prep =====
-// One CTA (4 warps) per (chunk, head).  TMA brings the q, k, v tiles of the
-// chunk's 64 tokens plus the 3 before them, and the alpha tile; the halo
-// rows that fall before the segment are replaced by the slot's conv tail (or
-// zeros).  Warp w handles tokens w, w+4, ...; lane l channels 4l..4l+3.
+// ======================================================= conv helper ====
+// Causal conv (width 4, last tap on the current token) + SiLU of token t of a
+// chunk for the lane's 4 channels, from a raw tile whose row t + 3 is token t.
+// Tile rows before the segment start come from the slot's conv tail (oldest
+// first) when the sequence resumes (tail_s != nullptr), else they are zero.
+// Tokens past the segment end give 0.
 template <typename Act>
-__global__ void __launch_bounds__(128) prefill_prep_kernel(const PrefillParams p,
-                                                           const __grid_constant__ CUtensorMap tm_q,
-                                                           const __grid_constant__ CUtensorMap tm_k,
-                                                           const __grid_constant__ CUtensorMap tm_v,
-                                                           const __grid_constant__ CUtensorMap tm_a) {
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr size_t TILE = size_t(CH + HALO) * D * sizeof(Act);
-    Act *tq = reinterpret_cast<Act *>(sm);
-    Act *tk = reinterpret_cast<Act *>(sm + TILE);
-    Act *tv = reinterpret_cast<Act *>(sm + 2 * TILE);
-    Act *ta = reinterpret_cast<Act *>(sm + 3 * TILE);
-    __shared__ uint64_t bar;
-    const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const ChunkMeta cm = p.chunks[g];
-    const SeqMeta sq = p.seqs[cm.seq];
-    char *rec = rec_ptr(p, g, h);
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(&bar, uint32_t(3 * TILE + size_t(CH) * D * sizeof(Act)));
-        tma_load_3d(tq, &tm_q, &bar, 0, h, cm.row0 - HALO);
-        tma_load_3d(tk, &tm_k, &bar, 0, h, cm.row0 - HALO);
-        tma_load_3d(tv, &tm_v, &bar, 0, h, cm.row0 - HALO);
-        tma_load_3d(ta, &tm_a, &bar, 0, h, cm.row0);
+__device__ __forceinline__ void conv_silu4(const Act *tile, const float4 (&w)[4], int t, int lane, int pos0, int len,
+                                           const Act *tail_s, int n_ch, float (&y)[4]) {
+    float4 x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int row = t + j, pos = pos0 - HALO + row;
+        if (row < HALO && pos < 0)
+            x[j] = tail_s ? act4(tail_s + size_t(HALO + pos) * n_ch + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        else
+            x[j] = act4(tile + row * D + 4 * lane);
     }
-    // conv taps of this lane's channels while the tiles fly
+    const float xs[4][4] = {{x[0].x, x[1].x, x[2].x, x[3].x}, {x[0].y, x[1].y, x[2].y, x[3].y},
+                            {x[0].z, x[1].z, x[2].z, x[3].z}, {x[0].w, x[1].w, x[2].w, x[3].w}};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        float acc = w[m].x * xs[m][0];
+        acc = fmaf(w[m].y, xs[m][1], acc);
+        acc = fmaf(w[m].z, xs[m][2], acc);
+        acc = fmaf(w[m].w, xs[m][3], acc);
+        y[m] = t < len ? acc * sigmoid_fast(acc) : 0.f;
+    }
+}
+
+// The lane's 4 channels' conv taps of stream s (0 q, 1 k, 2 v) of head h.
+template <typename Act>
+__device__ __forceinline__ void conv_taps(const PrefillParams &p, int s, int h, int lane, float4 (&w)[4]) {
     const Act *cw = static_cast<const Act *>(p.conv_w);
-    float4 w[3][4];
 #pragma unroll
-    for (int s = 0; s < 3; ++s)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) w[s][m] = act4(cw + size_t(s * p.H * D + h * D + 4 * lane + m) * 4);
-    __syncthreads();
-    // a timed-out wait is seen by every thread, so all of them leave together
-    if (!__syncthreads_and(mbar_wait(&bar, 0, p.err))) return;
-    // halo rows before the segment start: the slot's conv tail, or zeros
-    if (cm.pos0 < HALO) {
-        const Act *tail = static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch;
-        for (int e = tid; e < 3 * HALO * D; e += 128) {
-            const int s = e / (HALO * D), j = (e / D) % HALO, c = e % D;
-            const int pos = cm.pos0 - HALO + j;
-            if (pos < 0) {
-                Act *tile = s == 0 ? tq : (s == 1 ? tk : tv);
-                tile[j * D + c] = sq.has_init ? tail[size_t(HALO + pos) * p.n_ch + s * p.H * D + h * D + c]
-                                              : from_f32<Act>(0.f);
-            }
-        }
-    }
-    __syncthreads();
-    float *QH = at<float>(rec, Rec::QH), *KH = at<float>(rec, Rec::KH), *VV = at<float>(rec, Rec::VV);
-    for (int t = warp; t < CH; t += 4) {
-        float y[3][4];
-#pragma unroll
-        for (int s = 0; s < 3; ++s) {
-            const Act *tile = s == 0 ? tq : (s == 1 ? tk : tv);
-            float4 x[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = act4(tile + (t + j) * D + 4 * lane);
-            const float xs[4][4] = {{x[0].x, x[1].x, x[2].x, x[3].x}, {x[0].y, x[1].y, x[2].y, x[3].y},
-                                    {x[0].z, x[1].z, x[2].z, x[3].z}, {x[0].w, x[1].w, x[2].w, x[3].w}};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                float acc = w[s][m].x * xs[m][0];
-                acc = fmaf(w[s][m].y, xs[m][1], acc);
-                acc = fmaf(w[s][m].z, xs[m][2], acc);
-                acc = fmaf(w[s][m].w, xs[m][3], acc);
-                y[s][m] = t < cm.len ? acc * sigmoid_f(acc) : 0.f;
-            }
-        }
-        float a = 0.f, b = 0.f;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            a = fmaf(y[0][m], y[0][m], a);
-            b = fmaf(y[1][m], y[1][m], b);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            a += __shfl_xor_sync(0xffffffffu, a, o);
-            b += __shfl_xor_sync(0xffffffffu, b, o);
-        }
-        const float rq = rsqrtf(a + p.eps_l2), rk = rsqrtf(b + p.eps_l2);
-        *reinterpret_cast<float4 *>(QH + t * D + 4 * lane) = make_float4(y[0][0] * rq, y[0][1] * rq, y[0][2] * rq, y[0][3] * rq);
-        *reinterpret_cast<float4 *>(KH + t * D + 4 * lane) = make_float4(y[1][0] * rk, y[1][1] * rk, y[1][2] * rk, y[1][3] * rk);
-        *reinterpret_cast<float4 *>(VV + t * D + 4 * lane) = make_float4(y[2][0], y[2][1], y[2][2], y[2][3]);
-    }
-    // cumulative log decay: thread = channel
-    float *GG = at<float>(rec, Rec::GG);
-    float G = 0.f;
-    for (int t = 0; t < CH; ++t) {
-        if (t < cm.len) G += fmaxf(logf(to_f32(ta[t * D + tid])), kLogAlphaMin);
-        GG[t * D + tid] = G;
-    }
-    if (tid < CH)
-        at<float>(rec, Rec::BB)[tid] =
-            tid < cm.len ? to_f32(static_cast<const Act *>(p.beta)[size_t(cm.row0 + tid) * p.H + h]) : 0.f;
+    for (int m = 0; m < 4; ++m) w[m] = act4(cw + size_t(s * p.H * D + h * D + 4 * lane + m) * 4);
 }
 
 // ============================================================== intra ====
@@ -252,12 +184,32 @@ namespace is {  // intra shared-memory map (bytes from a 1 KiB-aligned base)
 constexpr uint32_t X_HI = 0, X_LO = 32768, KB_HI = 65536, KB_LO = 81920;           // phase 1 images
 constexpr uint32_t A_F32 = 0, XS_F32 = 16384, T_F32 = 81920;                        // inverse (fp32)
 constexpr uint32_t T_HI = 0, T_LO = 8192, AK_HI = 16384, AK_LO = 32768, AV_HI = 49152, AV_LO = 65536;  // phase 3
-constexpr uint32_t IN0 = 98304;   // QH, then VV, then the W image staging (32 KiB)
-constexpr uint32_t KH = 131072;   // fp32 [64][128]
-constexpr uint32_t GG = 163840;   // fp32 [64][128]
+constexpr uint32_t RQ = 0;        // raw q tile (67 rows), then raw k; both give way to the phase-1 images
+constexpr uint32_t IN0 = 98304;   // raw alpha tile, then q^, then v, then the W image staging (32 KiB)
+constexpr uint32_t KH = 131072;   // fp32 [64][128] k^
+constexpr uint32_t GG = 163840;   // fp32 [64][128] G, then E = exp(G - c)
 constexpr uint32_t SMALL = 196608;
-constexpr uint32_t BYTES = SMALL + 2560;
+constexpr uint32_t RV_LATE = 32768;         // raw v tile of a 4-byte activation (free while T is formed)
+constexpr uint32_t RV_EARLY = SMALL + 2560; // raw v tile of a 2-byte activation (loaded with the others)
 constexpr int NT = 256;
+template <typename Act>
+__host__ __device__ constexpr uint32_t tile_bytes() { return uint32_t((CH + HALO) * D * sizeof(Act)); }
+// A 2-byte activation's v tile fits beside everything else and arrives with
+// q, k and alpha; a 4-byte one is loaded once A and P have freed the images.
+template <typename Act>
+__host__ __device__ constexpr bool v_early() { return sizeof(Act) == 2; }
+template <typename Act>
+__host__ __device__ constexpr uint32_t RK() { return RQ + tile_bytes<Act>(); }
+template <typename Act>
+__host__ __device__ constexpr uint32_t RV() { return v_early<Act>() ? RV_EARLY : RV_LATE; }
+template <typename Act>
+__host__ __device__ constexpr uint32_t BYTES() { return v_early<Act>() ? RV_EARLY + tile_bytes<Act>() : SMALL + 2560; }
+template <typename Act>
+__host__ __device__ constexpr bool map_ok() {
+    return RK<Act>() + tile_bytes<Act>() <= IN0 && CH * D * sizeof(Act) <= KH - IN0 &&
+           (v_early<Act>() || (RV_LATE >= XS_F32 + 16384 && RV_LATE + tile_bytes<Act>() <= T_F32)) &&
+           BYTES<Act>() + 1024 <= 232448 && tile_bytes<Act>() % 128 == 0;
+}
 }  // namespace is
 
 // Fills `rows` x (8 * chunks_per_row) elements of an image pair with f(row, k0, out8),
@@ -338,12 +290,20 @@ __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS,
     __syncthreads();
 }
 
-// One CTA (8 warps) per (chunk, head).  The prep record's q, k and G arrive
-// by TMA bulk copies (v follows once q is consumed), so every operand build
-// reads shared memory.  Images the chain needs that involve no MMA (exp(G).q,
-// (exp(G_last - G).k)^T, P) go straight to the record from registers; the W
-// image is staged and bulk-stored.
-__global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillParams p) {
+// One CTA (8 warps) per (chunk, head).  TMA brings the raw q, k, v tiles of
+// the chunk's 64 tokens plus the 3 before them (the conv halo) and the alpha
+// tile; the kernel forms G, q^, k^ (conv + SiLU + L2) and v (conv + SiLU) in
+// shared memory, so every operand build reads shared memory.  Images the
+// chain needs that involve no MMA (exp(G).q, (exp(G_last - G).k)^T, P) go
+// straight to the record from registers; the W image is staged and
+// bulk-stored.
+template <typename Act>
+__global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillParams p,
+                                                               const __grid_constant__ CUtensorMap tm_q,
+                                                               const __grid_constant__ CUtensorMap tm_k,
+                                                               const __grid_constant__ CUtensorMap tm_v,
+                                                               const __grid_constant__ CUtensorMap tm_a) {
+    static_assert(is::map_ok<Act>(), "intra shared-memory map overlaps");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *cref = reinterpret_cast<float *>(sm + is::SMALL);  // [128] c = mid of the log-decay range
@@ -354,24 +314,43 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     uint32_t *tbase = reinterpret_cast<uint32_t *>(flag + 1);  // [1]
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + is::SMALL + 1024);
     uint64_t *bar_mma = bar_ld + 1;
+    uint64_t *bar_v = bar_ld + 2;
+    constexpr uint32_t TILE = is::tile_bytes<Act>();
+    const Act *rq = reinterpret_cast<const Act *>(sm + is::RQ);
+    const Act *rk = reinterpret_cast<const Act *>(sm + is::RK<Act>());
+    const Act *rv = reinterpret_cast<const Act *>(sm + is::RV<Act>());
+    const Act *ra = reinterpret_cast<const Act *>(sm + is::IN0);
     const float *QHs = reinterpret_cast<const float *>(sm + is::IN0);
     const float *VVs = reinterpret_cast<const float *>(sm + is::IN0);
     const float *KHs = reinterpret_cast<const float *>(sm + is::KH);
     const float *GGs = reinterpret_cast<const float *>(sm + is::GG);
     const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const ChunkMeta cm = p.chunks[g];
+    const SeqMeta sq = p.seqs[cm.seq];
     char *rec = rec_ptr(p, g, h);
     const uint32_t sbase = smem_u32(sm);
     if (tid == 0) {
         *flag = 0;
         mbar_init(bar_ld, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_v, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_ld, 3 * 32768 + CH * 4);
-        bulk_load(sm + is::IN0, rec + Rec::QH, 32768, bar_ld);
-        bulk_load(sm + is::KH, rec + Rec::KH, 32768, bar_ld);
-        bulk_load(sm + is::GG, rec + Rec::GG, 32768, bar_ld);
-        bulk_load(beta, rec + Rec::BB, CH * 4, bar_ld);
+        mbar_arrive_expect_tx(bar_ld, 2 * TILE + uint32_t(CH * D * sizeof(Act)));
+        tma_load_3d(sm + is::RQ, &tm_q, bar_ld, 0, h, cm.row0 - HALO);
+        tma_load_3d(sm + is::RK<Act>(), &tm_k, bar_ld, 0, h, cm.row0 - HALO);
+        tma_load_3d(sm + is::IN0, &tm_a, bar_ld, 0, h, cm.row0);
+        if constexpr (is::v_early<Act>()) {
+            mbar_arrive_expect_tx(bar_v, TILE);
+            tma_load_3d(sm + is::RV<Act>(), &tm_v, bar_v, 0, h, cm.row0 - HALO);
+        }
     }
+    if (tid < CH)
+        beta[tid] = tid < cm.len ? to_f32(static_cast<const Act *>(p.beta)[size_t(cm.row0 + tid) * p.H + h]) : 0.f;
+    // conv tail rows of this head (resumed sequences), per stream
+    const Act *tail = sq.has_init ? static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch + h * D : nullptr;
+    float4 wq[4], wk[4];
+    conv_taps<Act>(p, 0, h, lane, wq);
+    conv_taps<Act>(p, 1, h, lane, wk);
     if (warp == 0) tmem_alloc(tbase, 256);
     tc_fence_before();
     __syncthreads();
@@ -379,6 +358,49 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     const uint32_t tm = *tbase;
     bool ok = __syncthreads_and(mbar_wait(bar_ld, 0, p.err));
     uint32_t mma_phase = 0;
+    // G = cumulative log decay: thread = (channel, half of the chunk); the
+    // second half adds the first half's total below
+    float *GGw = reinterpret_cast<float *>(sm + is::GG);
+    const int gi = tid & (D - 1), gt0 = (tid >> 7) * (CH / 2);
+    if (ok) {
+        float G = 0.f;
+#pragma unroll 4
+        for (int t = gt0; t < gt0 + CH / 2; ++t) {
+            if (t < cm.len) G += fmaxf(logf(to_f32(ra[t * D + gi])), kLogAlphaMin);
+            GGw[t * D + gi] = G;
+        }
+    }
+    __syncthreads();  // alpha is consumed: q^ takes its place
+    if (ok) {
+        if (gt0 > 0) {
+            const float g31 = GGw[(gt0 - 1) * D + gi];
+            for (int t = gt0; t < CH; ++t) GGw[t * D + gi] += g31;
+        }
+        // q^, k^: warp per token, lane per 4 channels
+        float *QHw = reinterpret_cast<float *>(sm + is::IN0), *KHw = reinterpret_cast<float *>(sm + is::KH);
+#pragma unroll 2
+        for (int it = 0; it < CH / (is::NT / 32); ++it) {
+            const int t = warp + it * (is::NT / 32);
+            float yq[4], yk[4];
+            conv_silu4<Act>(rq, wq, t, lane, cm.pos0, cm.len, tail, p.n_ch, yq);
+            conv_silu4<Act>(rk, wk, t, lane, cm.pos0, cm.len, tail ? tail + p.H * D : nullptr, p.n_ch, yk);
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                a = fmaf(yq[m], yq[m], a);
+                b = fmaf(yk[m], yk[m], b);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, o);
+                b += __shfl_xor_sync(0xffffffffu, b, o);
+            }
+            const float nq = rsqrtf(a + p.eps_l2), nk = rsqrtf(b + p.eps_l2);
+            *reinterpret_cast<float4 *>(QHw + t * D + 4 * lane) = make_float4(yq[0] * nq, yq[1] * nq, yq[2] * nq, yq[3] * nq);
+            *reinterpret_cast<float4 *>(KHw + t * D + 4 * lane) = make_float4(yk[0] * nk, yk[1] * nk, yk[2] * nk, yk[3] * nk);
+        }
+    }
+    __syncthreads();
     if (ok && tid < D) {
         const float g0 = GGs[tid], gl = GGs[(CH - 1) * D + tid];
         const float c = 0.5f * (g0 + gl);
@@ -513,10 +535,12 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
         }
     }
     tc_fence_before();
-    __syncthreads();  // q is consumed (the exact path reads it for P): v takes its place
-    if (tid == 0 && ok) {
-        mbar_arrive_expect_tx(bar_ld, 32768);
-        bulk_load(sm + is::IN0, rec + Rec::VV, 32768, bar_ld);
+    __syncthreads();  // q^ is consumed (the exact path reads it for P): v takes its place
+    if constexpr (!is::v_early<Act>()) {
+        if (tid == 0 && ok) {  // the phase-1 images are consumed: the raw v tile may land there
+            mbar_arrive_expect_tx(bar_v, TILE);
+            tma_load_3d(sm + is::RV<Act>(), &tm_v, bar_v, 0, h, cm.row0 - HALO);
+        }
     }
     // ---- T = (I + A)^-1 (unit lower triangular), 16 x 16 blocks
     float *T = reinterpret_cast<float *>(sm + is::T_F32);
@@ -540,13 +564,32 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[(b0 + r) * CH + b0 + c] = tc[r];
     }
-    __syncthreads();
+    // meanwhile warps 2..7 form v = SiLU(conv(v raw)) in the q^ buffer
+    bool vok = true;
+    if (warp >= 2) {
+        // a late tile is only requested while ok; an early one is always in flight
+        vok = (is::v_early<Act>() || ok) ? mbar_wait(bar_v, 0, p.err) : false;
+        if (ok && vok) {
+            float4 wv[4];
+            conv_taps<Act>(p, 2, h, lane, wv);
+            float *VVw = reinterpret_cast<float *>(sm + is::IN0);
+            constexpr int NW = is::NT / 32 - 2;
+#pragma unroll 2
+            for (int it = 0; it < (CH + NW - 1) / NW; ++it) {
+                const int t = warp - 2 + it * NW;
+                if (t >= CH) break;
+                float y[4];
+                conv_silu4<Act>(rv, wv, t, lane, cm.pos0, cm.len, tail ? tail + 2 * p.H * D : nullptr, p.n_ch, y);
+                *reinterpret_cast<float4 *>(VVw + t * D + 4 * lane) = make_float4(y[0], y[1], y[2], y[3]);
+            }
+        }
+    }
+    ok = __syncthreads_and(ok && vok);
     // Blocks below the diagonal, by distance d: T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
     tri_offdiag<1>(A, T, XS, tid);
     tri_offdiag<2>(A, T, XS, tid);
     tri_offdiag<3>(A, T, XS, tid);
     // ---- phase 3: W^T = (beta exp(G) . K)^T T^T and Ut^T = (beta V)^T T^T
-    ok = __syncthreads_and(ok && mbar_wait(bar_ld, 1, p.err));  // v has arrived
     if (ok) {
         build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, is::NT, [&](int r, int s0, float(&x)[8]) {
             ld8(T + r * CH + s0, x);
@@ -956,10 +999,9 @@ kda_status set_smem(K kern, size_t bytes) {
 }
 
 template <typename Act>
-constexpr size_t prep_smem() {
-    return 1024 + 3 * size_t(CH + HALO) * D * sizeof(Act) + size_t(CH) * D * sizeof(Act);
+constexpr size_t intra_smem() {
+    return 1024 + is::BYTES<Act>();
 }
-constexpr size_t kIntraSmem = 1024 + is::BYTES;
 constexpr size_t kChainSmem = 1024 + cs::BYTES;
 
 // Per-device side stream (highest priority) and events for the windowed
@@ -992,8 +1034,7 @@ template <typename Act>
 kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int N, long long n_chunks, int n_reqs,
                       cudaStream_t stream) {
     kda_status st;
-    if ((st = set_smem(prefill_prep_kernel<Act>, prep_smem<Act>())) != KDA_OK) return st;
-    if ((st = set_smem(prefill_intra_kernel, kIntraSmem)) != KDA_OK) return st;
+    if ((st = set_smem(prefill_intra_kernel<Act>, intra_smem<Act>())) != KDA_OK) return st;
     if ((st = set_smem(prefill_chain_kernel, kChainSmem)) != KDA_OK) return st;
     PrefillParams p = p0;
     CUtensorMap mq, mk, mv, ma;
@@ -1004,7 +1045,7 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
             return KDA_ERR_CUDA;
     }
     // Windows of chunks: the chain of window w (one CTA per sequence and
-    // head, on the side stream) runs while prep and intra of window w + 1
+    // head, on the side stream) runs while intra of window w + 1
     // fill the other SMs; events order each chain launch after its window's
     // records and the final join returns everything to the caller's stream.
     // The side stream's events are shared by every caller of this device:
@@ -1029,8 +1070,7 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
         if (hi > lo) {
             p.chunk_base = int(lo);
             const dim3 grid(unsigned(hi - lo), unsigned(p.H));
-            prefill_prep_kernel<Act><<<grid, 128, prep_smem<Act>(), stream>>>(p, mq, mk, mv, ma);
-            prefill_intra_kernel<<<grid, is::NT, kIntraSmem, stream>>>(p);
+            prefill_intra_kernel<Act><<<grid, is::NT, intra_smem<Act>(), stream>>>(p, mq, mk, mv, ma);
         }
         p.win_lo = int(lo);
         p.win_hi = (w + 1 == n_win) ? int(n_chunks) : int(hi);

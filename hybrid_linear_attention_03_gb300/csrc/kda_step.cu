@@ -20,9 +20,12 @@
 //     products over d_k: 4 FMAs per lane, then a transpose-reduce across the
 //     row's lanes that halves the number of live partial sums at each shuffle
 //     stage (16 shuffles for 16 rows instead of 80).
-//   * Conv + SiLU + L2 for all T tokens are computed once up front while the
-//     state loads are in flight; every load of that prologue is issued before
-//     its first use.
+//   * The per-token inputs of all T tokens (q, k, v, alpha, gate, beta, the
+//     snapshot slots) are copied into shared memory asynchronously as the
+//     very first thing, the old conv tail right after the state loads are
+//     issued; conv + SiLU + L2 for all T tokens then run from shared memory
+//     while the state loads are in flight.  The prologue costs one memory
+//     latency whatever T is.
 //   * Inside the token loop warps synchronise only with themselves, so each
 //     warp streams its snapshot rows as soon as they are ready.  The gated
 //     RMSNorm needs sum_j o_j^2 over the whole head: every warp keeps its
@@ -99,16 +102,19 @@ struct RowReduce {
 template <int D>
 __host__ __device__ constexpr size_t stage_floats(int T) { return T > 1 ? size_t(D) * D : 0; }
 
+__host__ __device__ constexpr size_t pad4(size_t n) { return (n + 3) / 4 * 4; }
+
+// Dynamic shared memory, in order (every part starts on a 16-byte boundary):
+// staging, conv outputs [T][3][D], u rows [WPC][16], o [T][D], per-warp sums
+// of squares [T][WPC], beta [T], snapshot slots [T], then in the activation
+// type the raw conv window [T+3][3][D] (old tail + tokens), alpha [T][D] and
+// the gate logits [T][D].
 template <int D, typename Act>
 __host__ __device__ constexpr size_t step_smem_bytes(int T) {
     constexpr int WPC = D / 16;
-    return sizeof(float) * (stage_floats<D>(T)    // snapshot staging
-                            + size_t(T) * 3 * D   // conv outputs
-                            + WPC * 16            // u row buffer
-                            + size_t(T) * D       // o per token
-                            + size_t(T) * D       // gate logits per token
-                            + size_t(T) * WPC)    // per-token, per-warp sum of squares
-           + sizeof(Act) * size_t(T + 3) * 3 * D;  // raw window (tail + tokens)
+    return sizeof(float) * (stage_floats<D>(T) + size_t(T) * 3 * D + WPC * 16 + size_t(T) * D +
+                            pad4(size_t(T) * WPC) + 2 * pad4(size_t(T))) +
+           sizeof(Act) * (size_t(T + 3) * 3 * D + 2 * size_t(T) * D);
 }
 
 template <int D, typename Act>
@@ -119,59 +125,68 @@ kda_step_kernel(const StepParams p) {
     const int T = p.T;
     float *stage_all = reinterpret_cast<float *>(smem_raw);  // [D][D] if T > 1 (16 rows per warp)
     float *conv = stage_all + stage_floats<D>(T);            // [T][3][D]
-    float *ubuf = conv + size_t(T) * 3 * D;              // [WPC][16]
-    float *obuf = ubuf + C::WPC * 16;                    // [T][D]
-    float *gbuf = obuf + size_t(T) * D;                  // [T][D]
-    float *sq = gbuf + size_t(T) * D;                    // [T][WPC]
-    Act *raw = reinterpret_cast<Act *>(sq + size_t(T) * C::WPC);  // [T+3][3][D]
+    float *ubuf = conv + size_t(T) * 3 * D;                  // [WPC][16]
+    float *obuf = ubuf + C::WPC * 16;                        // [T][D]
+    float *sq = obuf + size_t(T) * D;                        // [T][WPC]
+    float *bsm = sq + pad4(size_t(T) * C::WPC);              // [T] beta
+    int *snap_sm = reinterpret_cast<int *>(bsm + pad4(T));   // [T] snapshot slots
+    Act *raw = reinterpret_cast<Act *>(snap_sm + pad4(T));   // [T+3][3][D]
+    Act *araw = raw + size_t(T + 3) * 3 * D;                 // [T][D] alpha
+    Act *graw = araw + size_t(T) * D;                        // [T][D] gate logits
 
     const int b = blockIdx.x / p.H, h = blockIdx.x - b * p.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t head_elems = size_t(D) * D;
     const size_t slot_elems = size_t(p.H) * head_elems;
+    const Act *beta = static_cast<const Act *>(p.beta);
+
+    // Per-token inputs of all T tokens (never written by the preceding step
+    // launch): 16-byte asynchronous copies into shared memory, issued first
+    // so the whole prologue costs one memory latency.  Every (token, head)
+    // row of D activations starts on a 16-byte boundary (16-byte aligned
+    // bases, D * sizeof(Act) a multiple of 16).
+    constexpr int CPR = int(D * sizeof(Act) / 16);  // 16-byte chunks per row
+    constexpr int EPC = int(16 / sizeof(Act));      // elements per chunk
+    for (int i = threadIdx.x; i < T * 5 * CPR; i += C::NT) {
+        const int row = i / CPR, cc = i - row * CPR;
+        const int t = row / 5, r = row - t * 5;
+        const size_t src_off = ((size_t(b) * T + t) * p.H + h) * D + size_t(cc) * EPC;
+        const Act *src = static_cast<const Act *>(r == 0 ? p.q : r == 1 ? p.k : r == 2 ? p.v : r == 3 ? p.alpha : p.gate);
+        Act *dst = r < 3 ? raw + size_t((t + 3) * 3 + r) * D : (r == 3 ? araw : graw) + size_t(t) * D;
+        sm100::cp_async16(dst + cc * EPC, src + src_off);
+    }
+    sm100::cp_async_commit();
+    if (threadIdx.x < T) bsm[threadIdx.x] = to_f32(beta[(size_t(b) * T + threadIdx.x) * p.H + h]);
 
     const int in_slot = p.in_slots[b];
     bool bad = in_slot < 0 || in_slot >= p.num_slots;
     for (int t = 0; t < T; ++t) {
         const int s = p.snap_slots[b * T + t];
         bad |= (s < 0 || s >= p.num_slots);
+        if (threadIdx.x == t) snap_sm[t] = s;
     }
     if (bad) {
         if (threadIdx.x == 0) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
+        sm100::cp_async_wait_all();  // no copy may land after the CTA is gone
         return;
     }
 
     const int sub = lane / C::LPR, c4 = lane % C::LPR;
-    // Per-token inputs of the first token (not written by a preceding step
-    // launch), fetched before the wait.
     const int n_own = c4 / C::OWN;
     const bool owner = (c4 % C::OWN) == 0;
     const int own_row = n_own * C::RPL + sub;  // 0..15 within the warp
     const int own_j = warp * 16 + own_row;     // value channel this lane reports
-    const Act *alpha = static_cast<const Act *>(p.alpha);
-    const Act *beta = static_cast<const Act *>(p.beta);
-    const Act *gate = static_cast<const Act *>(p.gate);
-    float4 av_next = load4(alpha + (size_t(b) * T * p.H + h) * D + 4 * c4);
-    float bt_next = to_f32(beta[size_t(b) * T * p.H + h]);
-    float gj_next = to_f32(gate[(size_t(b) * T * p.H + h) * D + own_j]);
 
-    // ---- conv + SiLU for the head's 3*D channels over the T tokens --------
-    // All loads of a thread's channels (taps, old tail, first token) are
-    // issued before any use, so the prologue costs one memory latency.
-    const Act *tail_in = static_cast<const Act *>(p.tails) + size_t(in_slot) * 3 * p.n_ch;
+    // conv taps of this thread's channels
     const Act *cw = static_cast<const Act *>(p.conv_w);
     constexpr int PER = (3 * D + C::NT - 1) / C::NT;
     float4 wv[PER];
-    Act xv[PER][4];
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
         const int idx = threadIdx.x + u * C::NT;
         if (idx < 3 * D) {
             const int s = idx / D, c = idx - s * D;
-            const int ch = s * p.H * D + h * D + c;
-            const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
-            wv[u] = load4(cw + size_t(ch) * 4);
-            xv[u][3] = src[size_t(b) * T * p.H * D + size_t(h) * D + c];
+            wv[u] = load4(cw + size_t(s * p.H * D + h * D + c) * 4);
         }
     }
     // The pool's state and tail may have been written by the preceding step
@@ -184,34 +199,32 @@ kda_step_kernel(const StepParams p) {
         const int row = warp * 16 + n * C::RPL + sub;
         S[n] = load4(Sin + size_t(row) * D + 4 * c4);
     }
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int idx = threadIdx.x + u * C::NT;
-        if (idx < 3 * D) {
-            const int s = idx / D, c = idx - s * D;
-            const int ch = s * p.H * D + h * D + c;
-            xv[u][0] = tail_in[ch];
-            xv[u][1] = tail_in[p.n_ch + ch];
-            xv[u][2] = tail_in[2 * p.n_ch + ch];
-        }
+    // old tail rows (3 taps x 3 streams, D channels of this head each)
+    const Act *tail_in = static_cast<const Act *>(p.tails) + size_t(in_slot) * 3 * p.n_ch;
+    for (int i = threadIdx.x; i < 9 * CPR; i += C::NT) {
+        const int row = i / CPR, cc = i - row * CPR;
+        const int j = row / 3, st = row - j * 3;
+        sm100::cp_async16(raw + size_t(j * 3 + st) * D + cc * EPC,
+                          tail_in + size_t(j) * p.n_ch + size_t(st) * p.H * D + size_t(h) * D + cc * EPC);
     }
+    sm100::cp_async_commit();
+    sm100::cp_async_wait_all();
+    __syncthreads();
+
+    // ---- conv + SiLU for the head's 3*D channels over the T tokens --------
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
         const int idx = threadIdx.x + u * C::NT;
         if (idx < 3 * D) {
             const int s = idx / D, c = idx - s * D;
-            const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
-            Act x0 = xv[u][0], x1 = xv[u][1], x2 = xv[u][2];
-            raw[(0 * 3 + s) * D + c] = x0;
-            raw[(1 * 3 + s) * D + c] = x1;
-            raw[(2 * 3 + s) * D + c] = x2;
+            float x0 = to_f32(raw[(0 * 3 + s) * D + c]), x1 = to_f32(raw[(1 * 3 + s) * D + c]);
+            float x2 = to_f32(raw[(2 * 3 + s) * D + c]);
             for (int t = 0; t < T; ++t) {
-                const Act xt = t == 0 ? xv[u][3] : src[(size_t(b) * T + t) * p.H * D + size_t(h) * D + c];
-                raw[((t + 3) * 3 + s) * D + c] = xt;
-                float acc = wv[u].x * to_f32(x0);
-                acc = fmaf(wv[u].y, to_f32(x1), acc);
-                acc = fmaf(wv[u].z, to_f32(x2), acc);
-                acc = fmaf(wv[u].w, to_f32(xt), acc);
+                const float xt = to_f32(raw[((t + 3) * 3 + s) * D + c]);
+                float acc = wv[u].x * x0;
+                acc = fmaf(wv[u].y, x1, acc);
+                acc = fmaf(wv[u].z, x2, acc);
+                acc = fmaf(wv[u].w, xt, acc);
                 conv[(t * 3 + s) * D + c] = acc * sigmoid_f(acc);
                 x0 = x1;
                 x1 = x2;
@@ -237,17 +250,10 @@ kda_step_kernel(const StepParams p) {
     Act *tails = static_cast<Act *>(p.tails);
 
     for (int t = 0; t < T; ++t) {
-        const size_t tok = size_t(b) * T + t;
         const float4 qv = load4(conv + (t * 3 + 0) * D + 4 * c4);
         const float4 kv = load4(conv + (t * 3 + 1) * D + 4 * c4);
-        const float4 av = av_next;
-        const float bt = bt_next;
-        if (owner) gbuf[t * D + own_j] = gj_next;
-        if (t + 1 < T) {
-            av_next = load4(alpha + ((tok + 1) * p.H + h) * D + 4 * c4);
-            bt_next = to_f32(beta[(tok + 1) * p.H + h]);
-            gj_next = to_f32(gate[((tok + 1) * p.H + h) * D + own_j]);
-        }
+        const float4 av = load4(araw + size_t(t) * D + 4 * c4);
+        const float bt = bsm[t];
         const float4 ka = make_float4(kv.x * av.x, kv.y * av.y, kv.z * av.z, kv.w * av.w);
         const float4 bk = make_float4(bt * kv.x, bt * kv.y, bt * kv.z, bt * kv.w);
 
@@ -290,7 +296,7 @@ kda_step_kernel(const StepParams p) {
         // drafts: 613 -> 527 us per launch on GB300; a single token got
         // slower, so it keeps direct stores).  The staging buffer is reused
         // once the previous bulk store has finished reading it.
-        const int snap = p.snap_slots[b * T + t];
+        const int snap = snap_sm[t];
         float *Sout = p.states + size_t(snap) * slot_elems + size_t(h) * head_elems;
         if (T == 1) {
 #pragma unroll
@@ -341,7 +347,7 @@ kda_step_kernel(const StepParams p) {
         if (owner) {
             const float o = obuf[t * D + own_j];
             out[((size_t(b) * T + t) * p.H + h) * D + own_j] =
-                from_f32<Act>(wn * (o * r) * sigmoid_f(gbuf[t * D + own_j]));
+                from_f32<Act>(wn * (o * r) * sigmoid_f(to_f32(graw[t * D + own_j])));
         }
     }
 }

@@ -228,7 +228,7 @@ KDA_API kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, con
  * compiled into the library: every GPU that loads the library holds it
  * until the process exits, and no call allocates or frees device memory.
  * A call that needs more scratch than that (its kda_prefill_workspace_bytes
- * figure for its own requests; with d = 128 about 210 (chunk, head) pairs of
+ * figure for its own requests; with d = 128 about 370 (chunk, head) pairs of
  * 64 tokens) returns KDA_ERR_WORKSPACE and enqueues nothing.
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.

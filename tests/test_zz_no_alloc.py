@@ -68,7 +68,7 @@ def test_noalloc_prefill_matches_workspace_prefill_twice():
 
 def test_noalloc_prefill_refuses_requests_beyond_the_scratch():
     pool, w, wgt = _pool_and_weights()
-    L = 64 * 200  # 200 chunks x 2 heads of records: more than 64 MiB
+    L = 64 * 300  # 300 chunks x 2 heads of records: more than 64 MiB
     assert kda.kda_prefill_workspace_bytes(pool, [0, L]) > kda.KDA_NOALLOC_SCRATCH_BYTES
     inp = {k: v.cuda() for k, v in I.token_inputs(61, 9, L, H, D, D, 3.0, act).items()}
     out = torch.zeros(L, H, D, dtype=act, device="cuda")
