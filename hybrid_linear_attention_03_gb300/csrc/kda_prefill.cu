@@ -142,41 +142,46 @@ __device__ __forceinline__ float4 act4<__nv_bfloat16>(const __nv_bfloat16 *p) {
 }
 
 // ======================================================= conv helper ====
-// Causal conv (width 4, last tap on the current token) + SiLU of token t of a
-// chunk for the lane's 4 channels, from a raw tile whose row t + 3 is token t.
-// Tile rows before the segment start come from the slot's conv tail (oldest
-// first) when the sequence resumes (tail_s != nullptr), else they are zero.
-// Tokens past the segment end give 0.
+// Causal conv (width 4, last tap on the current token) + SiLU of one channel
+// c over the chunk's 64 tokens, from a raw tile whose row t + 3 is token t
+// (row stride D).  Tile rows before the segment start come from the slot's
+// conv tail (tail_c points at channel c's oldest tap; rows n_ch apart) when
+// the sequence resumes, else they are zero.  Tokens past the segment end
+// give 0.  out[t * D + c] receives token t.  Raw values are loaded 8 tokens
+// at a time so their latencies overlap.
 template <typename Act>
-__device__ __forceinline__ void conv_silu4(const Act *tile, const float4 (&w)[4], int t, int lane, int pos0, int len,
-                                           const Act *tail_s, int n_ch, float (&y)[4]) {
-    float4 x[4];
+__device__ __forceinline__ void conv_silu_channel(const Act *__restrict__ tile, int c, float4 w, int pos0, int len,
+                                                  const Act *__restrict__ tail_c, int n_ch, float *__restrict__ out) {
+    float x[3];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int row = t + j, pos = pos0 - HALO + row;
-        if (row < HALO && pos < 0)
-            x[j] = tail_s ? act4(tail_s + size_t(HALO + pos) * n_ch + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-        else
-            x[j] = act4(tile + row * D + 4 * lane);
+    for (int j = 0; j < HALO; ++j) {
+        const int pos = pos0 - HALO + j;
+        x[j] = pos >= 0 ? to_f32(tile[j * D + c]) : (tail_c ? to_f32(tail_c[size_t(HALO + pos) * n_ch]) : 0.f);
     }
-    const float xs[4][4] = {{x[0].x, x[1].x, x[2].x, x[3].x}, {x[0].y, x[1].y, x[2].y, x[3].y},
-                            {x[0].z, x[1].z, x[2].z, x[3].z}, {x[0].w, x[1].w, x[2].w, x[3].w}};
+    float x0 = x[0], x1 = x[1], x2 = x[2];
+#pragma unroll 1
+    for (int t0 = 0; t0 < CH; t0 += 8) {
+        float xs[8];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        float acc = w[m].x * xs[m][0];
-        acc = fmaf(w[m].y, xs[m][1], acc);
-        acc = fmaf(w[m].z, xs[m][2], acc);
-        acc = fmaf(w[m].w, xs[m][3], acc);
-        y[m] = t < len ? acc * sigmoid_fast(acc) : 0.f;
+        for (int e = 0; e < 8; ++e) xs[e] = to_f32(tile[(t0 + e + HALO) * D + c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float acc = w.x * x0;
+            acc = fmaf(w.y, x1, acc);
+            acc = fmaf(w.z, x2, acc);
+            acc = fmaf(w.w, xs[e], acc);
+            out[(t0 + e) * D + c] = t0 + e < len ? acc * sigmoid_fast(acc) : 0.f;
+            x0 = x1;
+            x1 = x2;
+            x2 = xs[e];
+        }
     }
 }
 
-// The lane's 4 channels' conv taps of stream s (0 q, 1 k, 2 v) of head h.
+// Conv taps of channel c of stream s (0 q, 1 k, 2 v) of head h.
 template <typename Act>
-__device__ __forceinline__ void conv_taps(const PrefillParams &p, int s, int h, int lane, float4 (&w)[4]) {
-    const Act *cw = static_cast<const Act *>(p.conv_w);
-#pragma unroll
-    for (int m = 0; m < 4; ++m) w[m] = act4(cw + size_t(s * p.H * D + h * D + 4 * lane + m) * 4);
+__device__ __forceinline__ float4 conv_taps(const PrefillParams &p, int s, int h, int c) {
+    return act4(static_cast<const Act *>(p.conv_w) + size_t(s * p.H * D + h * D + c) * 4);
 }
 
 // ============================================================== intra ====
@@ -217,11 +222,14 @@ __host__ __device__ constexpr bool map_ok() {
 // Row-major unit order (consecutive threads walk one row's chunks) suits f
 // reading rows of a [row][K] array; chunk-major order (consecutive threads
 // take consecutive rows of one chunk) suits f reading columns of a [K][row]
-// array without shared-memory bank conflicts.
+// array without shared-memory bank conflicts.  A thread gathers the inputs of
+// 4 units before it stores any, so their load latencies overlap (the stores
+// could alias the inputs as far as the compiler knows).
 template <bool kChunkMajor = false, typename F>
 __device__ __forceinline__ void build_image(unsigned char *hi, unsigned char *lo, int rows, int chunks_per_row,
                                             int tid, int nthreads, F f, int row0 = 0, int total_rows = 0) {
     if (total_rows == 0) total_rows = rows;
+#pragma unroll 1
     for (int u = tid; u < rows * chunks_per_row; u += nthreads) {
         const int r = kChunkMajor ? u % rows : u / chunks_per_row;
         const int c = kChunkMajor ? u / rows : u - r * chunks_per_row;
@@ -251,19 +259,18 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
     }
 }
 
-// One level of the blocked inverse of I + A: the 4 - d blocks at distance d
-// below the diagonal, with fixed-length (unrolled) dot products; a thread
+// One level of the blocked inverse of I + A (A stored transposed: A[s * CH +
+// r] = A_rs): the 4 - d blocks at distance d below the diagonal; a thread
 // owns 4 adjacent columns of one row, so each A value it loads feeds 4 FMAs
 // and the T / X values arrive as 16-byte vectors.
-template <int d>
-__device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS, int tid) {
-    constexpr int nblk = 4 - d;
+__device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS, int tid, int d) {
+    const int nblk = 4 - d;
     for (int e = tid; e < nblk * 64; e += is::NT) {
         const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4, a = blk + d, b = blk;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
+#pragma unroll 8
         for (int s = 0; s < 16 * d; ++s) {
-            const float av = A[(a * 16 + r) * CH + b * 16 + s];
+            const float av = A[(b * 16 + s) * CH + a * 16 + r];
             const float4 tv = ld4(T + (b * 16 + s) * CH + b * 16 + c4);
             acc.x = fmaf(av, tv.x, acc.x);
             acc.y = fmaf(av, tv.y, acc.y);
@@ -276,7 +283,7 @@ __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS,
     for (int e = tid; e < nblk * 64; e += is::NT) {
         const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4, a = blk + d, b = blk;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
+#pragma unroll 8
         for (int s = 0; s < 16; ++s) {
             const float tv = -T[(a * 16 + r) * CH + a * 16 + s];
             const float4 xv = ld4(XS + (a * 16 + s) * CH + b * 16 + c4);
@@ -346,11 +353,13 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     }
     if (tid < CH)
         beta[tid] = tid < cm.len ? to_f32(static_cast<const Act *>(p.beta)[size_t(cm.row0 + tid) * p.H + h]) : 0.f;
-    // conv tail rows of this head (resumed sequences), per stream
+    // conv tail of this head (resumed sequences), and the conv taps of the
+    // channel this thread convolves: q (threads 0..127) or k (128..255), and
+    // v (threads 64..191, while T is formed)
     const Act *tail = sq.has_init ? static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch + h * D : nullptr;
-    float4 wq[4], wk[4];
-    conv_taps<Act>(p, 0, h, lane, wq);
-    conv_taps<Act>(p, 1, h, lane, wk);
+    const int qk = tid >> 7, cc = tid & (D - 1), vc = tid - 64;
+    const float4 w_qk = conv_taps<Act>(p, qk, h, cc);
+    const float4 w_v = (vc >= 0 && vc < D) ? conv_taps<Act>(p, 2, h, vc) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == 0) tmem_alloc(tbase, 256);
     tc_fence_before();
     __syncthreads();
@@ -364,40 +373,59 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     const int gi = tid & (D - 1), gt0 = (tid >> 7) * (CH / 2);
     if (ok) {
         float G = 0.f;
-#pragma unroll 4
-        for (int t = gt0; t < gt0 + CH / 2; ++t) {
-            if (t < cm.len) G += fmaxf(logf(to_f32(ra[t * D + gi])), kLogAlphaMin);
-            GGw[t * D + gi] = G;
+#pragma unroll 1
+        for (int t0 = gt0; t0 < gt0 + CH / 2; t0 += 8) {  // 8 logarithms in flight, compact code
+            float lg[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) lg[e] = to_f32(ra[(t0 + e) * D + gi]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) lg[e] = fmaxf(logf(lg[e]), kLogAlphaMin);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (t0 + e < cm.len) G += lg[e];
+                GGw[(t0 + e) * D + gi] = G;
+            }
         }
     }
     __syncthreads();  // alpha is consumed: q^ takes its place
+    float *QHw = reinterpret_cast<float *>(sm + is::IN0), *KHw = reinterpret_cast<float *>(sm + is::KH);
     if (ok) {
         if (gt0 > 0) {
             const float g31 = GGw[(gt0 - 1) * D + gi];
-            for (int t = gt0; t < CH; ++t) GGw[t * D + gi] += g31;
+            float gv[CH / 2];
+#pragma unroll
+            for (int e = 0; e < CH / 2; ++e) gv[e] = GGw[(gt0 + e) * D + gi];
+#pragma unroll
+            for (int e = 0; e < CH / 2; ++e) GGw[(gt0 + e) * D + gi] = gv[e] + g31;
         }
-        // q^, k^: warp per token, lane per 4 channels
-        float *QHw = reinterpret_cast<float *>(sm + is::IN0), *KHw = reinterpret_cast<float *>(sm + is::KH);
-#pragma unroll 2
-        for (int it = 0; it < CH / (is::NT / 32); ++it) {
-            const int t = warp + it * (is::NT / 32);
-            float yq[4], yk[4];
-            conv_silu4<Act>(rq, wq, t, lane, cm.pos0, cm.len, tail, p.n_ch, yq);
-            conv_silu4<Act>(rk, wk, t, lane, cm.pos0, cm.len, tail ? tail + p.H * D : nullptr, p.n_ch, yk);
-            float a = 0.f, b = 0.f;
+        // SiLU(conv(q)) -> q^ buffer, SiLU(conv(k)) -> k^ buffer (normalised below)
+        conv_silu_channel<Act>(qk ? rk : rq, cc, w_qk, cm.pos0, cm.len, tail ? tail + qk * p.H * D + cc : nullptr, p.n_ch,
+                               qk ? KHw : QHw);
+    }
+    __syncthreads();
+    // L2 norm of the 64 q rows and 64 k rows: a warp per row, 2 rows at a time
+    if (ok) {
+#pragma unroll 1
+        for (int r0 = warp * 2; r0 < 2 * CH; r0 += is::NT / 32 * 2) {
+            float4 v[2];
+            float ss[2];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                a = fmaf(yq[m], yq[m], a);
-                b = fmaf(yk[m], yk[m], b);
+            for (int i = 0; i < 2; ++i) {
+                const int row = r0 + i;
+                v[i] = ld4((row < CH ? QHw + row * D : KHw + (row - CH) * D) + 4 * lane);
+                ss[i] = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, v[i].w * v[i].w)));
             }
 #pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                a += __shfl_xor_sync(0xffffffffu, a, o);
-                b += __shfl_xor_sync(0xffffffffu, b, o);
+            for (int o = 16; o; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int row = r0 + i;
+                const float n = rsqrtf(ss[i] + p.eps_l2);
+                *reinterpret_cast<float4 *>((row < CH ? QHw + row * D : KHw + (row - CH) * D) + 4 * lane) =
+                    make_float4(v[i].x * n, v[i].y * n, v[i].z * n, v[i].w * n);
             }
-            const float nq = rsqrtf(a + p.eps_l2), nk = rsqrtf(b + p.eps_l2);
-            *reinterpret_cast<float4 *>(QHw + t * D + 4 * lane) = make_float4(yq[0] * nq, yq[1] * nq, yq[2] * nq, yq[3] * nq);
-            *reinterpret_cast<float4 *>(KHw + t * D + 4 * lane) = make_float4(yk[0] * nk, yk[1] * nk, yk[2] * nk, yk[3] * nk);
         }
     }
     __syncthreads();
@@ -418,14 +446,21 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     // G is replaced by E in place.  The exact path keeps G.
     float *EE = reinterpret_cast<float *>(sm + is::GG);
     if (ok && !exact) {
-        for (int e4 = tid; e4 < CH * D / 4; e4 += is::NT) {
-            const int i0 = (e4 * 4) % D;
-            float4 g = ld4(GGs + 4 * e4);
-            g.x = expf(g.x - cref[i0]);
-            g.y = expf(g.y - cref[i0 + 1]);
-            g.z = expf(g.z - cref[i0 + 2]);
-            g.w = expf(g.w - cref[i0 + 3]);
-            *reinterpret_cast<float4 *>(EE + 4 * e4) = g;
+        // a thread's float4s all sit at channels 4 * tid mod D: all loads first
+        const float4 c4 = ld4(cref + (4 * tid) % D);
+#pragma unroll 1
+        for (int k0 = 0; k0 < CH * D / 4 / is::NT; k0 += 2) {
+            float4 g[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) g[k] = ld4(GGs + 4 * (tid + (k0 + k) * is::NT));
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                g[k].x = expf(g[k].x - c4.x);
+                g[k].y = expf(g[k].y - c4.y);
+                g[k].z = expf(g[k].z - c4.z);
+                g[k].w = expf(g[k].w - c4.w);
+                *reinterpret_cast<float4 *>(EE + 4 * (tid + (k0 + k) * is::NT)) = g[k];
+            }
         }
         __syncthreads();
     }
@@ -479,7 +514,8 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
                     });
     }
     __syncthreads();
-    // ---- A (s < r, times beta_r) -> fp32 smem, P (s <= r) -> record images
+    // ---- A (s < r, times beta_r) -> fp32 smem, stored transposed (A[s * CH + r]
+    // = A_rs), P (s <= r) -> record images
     float *A = reinterpret_cast<float *>(sm + is::A_F32);
     unsigned char *phi = reinterpret_cast<unsigned char *>(rec + Rec::KP_HI + Rec::P_OFF);
     unsigned char *plo = reinterpret_cast<unsigned char *>(rec + Rec::KP_LO + Rec::P_OFF);
@@ -490,13 +526,15 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
         const int m = (warp & 3) * 32 + lane;  // TMEM lane = row of X; warps w and w+4 split the columns
         const int cbase = (warp >> 2) * 32;
         if (ok) {
+#pragma unroll 1
             for (int c0 = cbase; c0 < cbase + 32; c0 += 16) {
                 float v[16];
                 tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + c0, v);
                 tmem_wait_ld();
-                if (m < CH) {
+                if (m < CH) {  // A^T: the warp's lanes (rows r = m) store consecutive words
+                    const float bm = beta[m];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) A[m * CH + c0 + e] = (c0 + e < m) ? beta[m] * v[e] : 0.f;
+                    for (int e = 0; e < 16; ++e) A[(c0 + e) * CH + m] = (c0 + e < m) ? bm * v[e] : 0.f;
                 } else {
                     const int r = m - CH;
 #pragma unroll
@@ -525,7 +563,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
                     pq = fmaf(QHs[r * D + i], f, pq);
                 }
             }
-            A[r * CH + s] = s < r ? beta[r] * a : 0.f;
+            A[s * CH + r] = s < r ? beta[r] * a : 0.f;
             const float pv = s <= r ? pq : 0.f;
             const __nv_bfloat16 ph = __float2bfloat16_rn(pv);
             const __nv_bfloat16 pl = __float2bfloat16_rn(pv - __bfloat162float(ph));
@@ -558,37 +596,25 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
         for (int r = 0; r < 16; ++r) {
             float acc = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc = fmaf(-A[(b0 + r) * CH + b0 + s], tc[s], acc);
+            for (int s = 0; s < r; ++s) acc = fmaf(-A[(b0 + s) * CH + b0 + r], tc[s], acc);
             tc[r] = acc;
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[(b0 + r) * CH + b0 + c] = tc[r];
     }
-    // meanwhile warps 2..7 form v = SiLU(conv(v raw)) in the q^ buffer
+    // meanwhile threads 64..191 form v = SiLU(conv(v raw)) in the q^ buffer
     bool vok = true;
-    if (warp >= 2) {
+    if (vc >= 0 && vc < D) {
         // a late tile is only requested while ok; an early one is always in flight
         vok = (is::v_early<Act>() || ok) ? mbar_wait(bar_v, 0, p.err) : false;
-        if (ok && vok) {
-            float4 wv[4];
-            conv_taps<Act>(p, 2, h, lane, wv);
-            float *VVw = reinterpret_cast<float *>(sm + is::IN0);
-            constexpr int NW = is::NT / 32 - 2;
-#pragma unroll 2
-            for (int it = 0; it < (CH + NW - 1) / NW; ++it) {
-                const int t = warp - 2 + it * NW;
-                if (t >= CH) break;
-                float y[4];
-                conv_silu4<Act>(rv, wv, t, lane, cm.pos0, cm.len, tail ? tail + 2 * p.H * D : nullptr, p.n_ch, y);
-                *reinterpret_cast<float4 *>(VVw + t * D + 4 * lane) = make_float4(y[0], y[1], y[2], y[3]);
-            }
-        }
+        if (ok && vok)
+            conv_silu_channel<Act>(rv, vc, w_v, cm.pos0, cm.len, tail ? tail + 2 * p.H * D + vc : nullptr, p.n_ch,
+                                   reinterpret_cast<float *>(sm + is::IN0));
     }
     ok = __syncthreads_and(ok && vok);
     // Blocks below the diagonal, by distance d: T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
-    tri_offdiag<1>(A, T, XS, tid);
-    tri_offdiag<2>(A, T, XS, tid);
-    tri_offdiag<3>(A, T, XS, tid);
+#pragma unroll 1
+    for (int d = 1; d < 4; ++d) tri_offdiag(A, T, XS, tid, d);
     // ---- phase 3: W^T = (beta exp(G) . K)^T T^T and Ut^T = (beta V)^T T^T
     if (ok) {
         build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, is::NT, [&](int r, int s0, float(&x)[8]) {
@@ -624,6 +650,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     const int cbase = (warp >> 2) * 32;
     if (ok) {
         float *UT = at<float>(rec, Rec::UT) + i;  // column j = i of Ut [r][j]
+#pragma unroll 1
         for (int c0 = cbase; c0 < cbase + 32; c0 += 16) {
             float v[16], u[16];
             tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + 64 + c0, v);
