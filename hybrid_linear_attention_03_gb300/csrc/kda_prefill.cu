@@ -189,14 +189,15 @@ namespace is {  // intra shared-memory map (bytes from a 1 KiB-aligned base)
 constexpr uint32_t X_HI = 0, X_LO = 32768, KB_HI = 65536, KB_LO = 81920;           // phase 1 images
 constexpr uint32_t A_F32 = 0, XS_F32 = 16384, T_F32 = 81920;                        // inverse (fp32)
 constexpr uint32_t T_HI = 0, T_LO = 8192, AK_HI = 16384, AK_LO = 32768, AV_HI = 49152, AV_LO = 65536;  // phase 3
-constexpr uint32_t RQ = 0;        // raw q tile (67 rows), then raw k; both give way to the phase-1 images
-constexpr uint32_t IN0 = 98304;   // raw alpha tile, then q^, then v, then the W image staging (32 KiB)
+constexpr uint32_t RQ = 0;        // raw q, k (67 rows each) and, 2-byte, alpha tiles; then the phase-1 images
+constexpr uint32_t IN0 = 98304;   // q^, then v, then the W image staging (32 KiB)
 constexpr uint32_t KH = 131072;   // fp32 [64][128] k^
 constexpr uint32_t GG = 163840;   // fp32 [64][128] G, then E = exp(G - c)
 constexpr uint32_t SMALL = 196608;
 constexpr uint32_t RV_LATE = 32768;         // raw v tile of a 4-byte activation (free while T is formed)
 constexpr uint32_t RV_EARLY = SMALL + 2560; // raw v tile of a 2-byte activation (loaded with the others)
-constexpr int NT = 256;
+constexpr int NT = 512;
+constexpr int QW = NT / 128;  // warps per TMEM lane quarter (a warp reaches lanes 32 (w % 4) .. + 31)
 template <typename Act>
 __host__ __device__ constexpr uint32_t tile_bytes() { return uint32_t((CH + HALO) * D * sizeof(Act)); }
 // A 2-byte activation's v tile fits beside everything else and arrives with
@@ -207,11 +208,15 @@ template <typename Act>
 __host__ __device__ constexpr uint32_t RK() { return RQ + tile_bytes<Act>(); }
 template <typename Act>
 __host__ __device__ constexpr uint32_t RV() { return v_early<Act>() ? RV_EARLY : RV_LATE; }
+// alpha: a 2-byte tile sits beside raw q and k; a 4-byte one lands in the G
+// buffer itself (same [64][128] 4-byte layout), where G is formed in place
+template <typename Act>
+__host__ __device__ constexpr uint32_t RA() { return sizeof(Act) == 2 ? RK<Act>() + tile_bytes<Act>() : GG; }
 template <typename Act>
 __host__ __device__ constexpr uint32_t BYTES() { return v_early<Act>() ? RV_EARLY + tile_bytes<Act>() : SMALL + 2560; }
 template <typename Act>
 __host__ __device__ constexpr bool map_ok() {
-    return RK<Act>() + tile_bytes<Act>() <= IN0 && CH * D * sizeof(Act) <= KH - IN0 &&
+    return RK<Act>() + tile_bytes<Act>() <= IN0 && (sizeof(Act) != 2 || RA<Act>() + CH * D * sizeof(Act) <= IN0) &&
            (v_early<Act>() || (RV_LATE >= XS_F32 + 16384 && RV_LATE + tile_bytes<Act>() <= T_F32)) &&
            BYTES<Act>() + 1024 <= 232448 && tile_bytes<Act>() % 128 == 0;
 }
@@ -311,6 +316,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
                                                                const __grid_constant__ CUtensorMap tm_v,
                                                                const __grid_constant__ CUtensorMap tm_a) {
     static_assert(is::map_ok<Act>(), "intra shared-memory map overlaps");
+    static_assert(CH % (16 * is::QW) == 0 && is::NT >= 4 * D, "drain split / thread roles need these");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *cref = reinterpret_cast<float *>(sm + is::SMALL);  // [128] c = mid of the log-decay range
@@ -326,7 +332,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     const Act *rq = reinterpret_cast<const Act *>(sm + is::RQ);
     const Act *rk = reinterpret_cast<const Act *>(sm + is::RK<Act>());
     const Act *rv = reinterpret_cast<const Act *>(sm + is::RV<Act>());
-    const Act *ra = reinterpret_cast<const Act *>(sm + is::IN0);
+    const Act *ra = reinterpret_cast<const Act *>(sm + is::RA<Act>());
     const float *QHs = reinterpret_cast<const float *>(sm + is::IN0);
     const float *VVs = reinterpret_cast<const float *>(sm + is::IN0);
     const float *KHs = reinterpret_cast<const float *>(sm + is::KH);
@@ -345,7 +351,7 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
         mbar_arrive_expect_tx(bar_ld, 2 * TILE + uint32_t(CH * D * sizeof(Act)));
         tma_load_3d(sm + is::RQ, &tm_q, bar_ld, 0, h, cm.row0 - HALO);
         tma_load_3d(sm + is::RK<Act>(), &tm_k, bar_ld, 0, h, cm.row0 - HALO);
-        tma_load_3d(sm + is::IN0, &tm_a, bar_ld, 0, h, cm.row0);
+        tma_load_3d(sm + is::RA<Act>(), &tm_a, bar_ld, 0, h, cm.row0);
         if constexpr (is::v_early<Act>()) {
             mbar_arrive_expect_tx(bar_v, TILE);
             tma_load_3d(sm + is::RV<Act>(), &tm_v, bar_v, 0, h, cm.row0 - HALO);
@@ -355,10 +361,10 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
         beta[tid] = tid < cm.len ? to_f32(static_cast<const Act *>(p.beta)[size_t(cm.row0 + tid) * p.H + h]) : 0.f;
     // conv tail of this head (resumed sequences), and the conv taps of the
     // channel this thread convolves: q (threads 0..127) or k (128..255), and
-    // v (threads 64..191, while T is formed)
+    // v (threads 64..191, while T is formed); threads 256..511 form G
     const Act *tail = sq.has_init ? static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch + h * D : nullptr;
     const int qk = tid >> 7, cc = tid & (D - 1), vc = tid - 64;
-    const float4 w_qk = conv_taps<Act>(p, qk, h, cc);
+    const float4 w_qk = qk < 2 ? conv_taps<Act>(p, qk, h, cc) : make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 w_v = (vc >= 0 && vc < D) ? conv_taps<Act>(p, 2, h, vc) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == 0) tmem_alloc(tbase, 256);
     tc_fence_before();
@@ -367,11 +373,17 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     const uint32_t tm = *tbase;
     bool ok = __syncthreads_and(mbar_wait(bar_ld, 0, p.err));
     uint32_t mma_phase = 0;
-    // G = cumulative log decay: thread = (channel, half of the chunk); the
-    // second half adds the first half's total below
+    // Threads 0..255: SiLU(conv(q)) -> q^ buffer, SiLU(conv(k)) -> k^ buffer
+    // (normalised below).  Threads 256..511 at the same time: G = cumulative
+    // log decay, thread = (channel, half of the chunk); the second half adds
+    // the first half's total below.
     float *GGw = reinterpret_cast<float *>(sm + is::GG);
-    const int gi = tid & (D - 1), gt0 = (tid >> 7) * (CH / 2);
-    if (ok) {
+    float *QHw = reinterpret_cast<float *>(sm + is::IN0), *KHw = reinterpret_cast<float *>(sm + is::KH);
+    const int gi = tid & (D - 1), gt0 = ((tid >> 7) & 1) * (CH / 2);
+    if (ok && qk < 2) {
+        conv_silu_channel<Act>(qk ? rk : rq, cc, w_qk, cm.pos0, cm.len, tail ? tail + qk * p.H * D + cc : nullptr, p.n_ch,
+                               qk ? KHw : QHw);
+    } else if (ok) {
         float G = 0.f;
 #pragma unroll 1
         for (int t0 = gt0; t0 < gt0 + CH / 2; t0 += 8) {  // 8 logarithms in flight, compact code
@@ -381,28 +393,21 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
 #pragma unroll
             for (int e = 0; e < 8; ++e) lg[e] = fmaxf(logf(lg[e]), kLogAlphaMin);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < 8; ++e) {  // (a 4-byte alpha tile is the G buffer: element in, element out)
                 if (t0 + e < cm.len) G += lg[e];
                 GGw[(t0 + e) * D + gi] = G;
             }
         }
     }
-    __syncthreads();  // alpha is consumed: q^ takes its place
-    float *QHw = reinterpret_cast<float *>(sm + is::IN0), *KHw = reinterpret_cast<float *>(sm + is::KH);
-    if (ok) {
-        if (gt0 > 0) {
-            const float g31 = GGw[(gt0 - 1) * D + gi];
-            float gv[CH / 2];
-#pragma unroll
-            for (int e = 0; e < CH / 2; ++e) gv[e] = GGw[(gt0 + e) * D + gi];
-#pragma unroll
-            for (int e = 0; e < CH / 2; ++e) GGw[(gt0 + e) * D + gi] = gv[e] + g31;
-        }
-        // SiLU(conv(q)) -> q^ buffer, SiLU(conv(k)) -> k^ buffer (normalised below)
-        conv_silu_channel<Act>(qk ? rk : rq, cc, w_qk, cm.pos0, cm.len, tail ? tail + qk * p.H * D + cc : nullptr, p.n_ch,
-                               qk ? KHw : QHw);
-    }
     __syncthreads();
+    if (ok && qk >= 2 && gt0 > 0) {
+        const float g31 = GGw[(gt0 - 1) * D + gi];
+        float gv[CH / 2];
+#pragma unroll
+        for (int e = 0; e < CH / 2; ++e) gv[e] = GGw[(gt0 + e) * D + gi];
+#pragma unroll
+        for (int e = 0; e < CH / 2; ++e) GGw[(gt0 + e) * D + gi] = gv[e] + g31;
+    }
     // L2 norm of the 64 q rows and 64 k rows: a warp per row, 2 rows at a time
     if (ok) {
 #pragma unroll 1
@@ -523,11 +528,11 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
         ok = __syncthreads_and(ok && mbar_wait(bar_mma, mma_phase, p.err));
         mma_phase ^= 1;
         tc_fence_after();
-        const int m = (warp & 3) * 32 + lane;  // TMEM lane = row of X; warps w and w+4 split the columns
-        const int cbase = (warp >> 2) * 32;
+        const int m = (warp & 3) * 32 + lane;  // TMEM lane = row of X; the QW warps of a quarter split the columns
+        const int cbase = (warp >> 2) * (CH / is::QW);
         if (ok) {
 #pragma unroll 1
-            for (int c0 = cbase; c0 < cbase + 32; c0 += 16) {
+            for (int c0 = cbase; c0 < cbase + CH / is::QW; c0 += 16) {
                 float v[16];
                 tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + c0, v);
                 tmem_wait_ld();
@@ -647,11 +652,11 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     tc_fence_after();
     unsigned char *whi = sm + is::IN0, *wlo = sm + is::IN0 + 16384;
     const int i = (warp & 3) * 32 + lane;  // TMEM lane: key channel i (W^T row) / value channel j (Ut^T row)
-    const int cbase = (warp >> 2) * 32;
+    const int cbase = (warp >> 2) * (CH / is::QW);
     if (ok) {
         float *UT = at<float>(rec, Rec::UT) + i;  // column j = i of Ut [r][j]
 #pragma unroll 1
-        for (int c0 = cbase; c0 < cbase + 32; c0 += 16) {
+        for (int c0 = cbase; c0 < cbase + CH / is::QW; c0 += 16) {
             float v[16], u[16];
             tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + 64 + c0, v);
             tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + 128 + c0, u);
