@@ -143,34 +143,35 @@ __device__ __forceinline__ float4 act4<__nv_bfloat16>(const __nv_bfloat16 *p) {
 
 // ======================================================= conv helper ====
 // Causal conv (width 4, last tap on the current token) + SiLU of one channel
-// c over the chunk's 64 tokens, from a raw tile whose row t + 3 is token t
-// (row stride D).  Tile rows before the segment start come from the slot's
-// conv tail (tail_c points at channel c's oldest tap; rows n_ch apart) when
-// the sequence resumes, else they are zero.  Tokens past the segment end
-// give 0.  out[t * D + c] receives token t.  Raw values are loaded 8 tokens
-// at a time so their latencies overlap.
+// c for tokens t0 .. t0 + n - 1 of the chunk (n a multiple of 8), from a raw
+// tile whose row t + 3 is token t (row stride D).  Tile rows before the
+// segment start come from the slot's conv tail (tail_c points at channel c's
+// oldest tap; rows n_ch apart) when the sequence resumes, else they are zero.
+// Tokens past the segment end give 0.  out[t * D + c] receives token t.  Raw
+// values are loaded 8 tokens at a time so their latencies overlap.
 template <typename Act>
-__device__ __forceinline__ void conv_silu_channel(const Act *__restrict__ tile, int c, float4 w, int pos0, int len,
-                                                  const Act *__restrict__ tail_c, int n_ch, float *__restrict__ out) {
+__device__ __forceinline__ void conv_silu_channel(const Act *__restrict__ tile, int c, float4 w, int t0, int n, int pos0,
+                                                  int len, const Act *__restrict__ tail_c, int n_ch,
+                                                  float *__restrict__ out) {
     float x[3];
 #pragma unroll
     for (int j = 0; j < HALO; ++j) {
-        const int pos = pos0 - HALO + j;
-        x[j] = pos >= 0 ? to_f32(tile[j * D + c]) : (tail_c ? to_f32(tail_c[size_t(HALO + pos) * n_ch]) : 0.f);
+        const int row = t0 + j, pos = pos0 - HALO + row;
+        x[j] = pos >= 0 ? to_f32(tile[row * D + c]) : (tail_c ? to_f32(tail_c[size_t(HALO + pos) * n_ch]) : 0.f);
     }
     float x0 = x[0], x1 = x[1], x2 = x[2];
 #pragma unroll 1
-    for (int t0 = 0; t0 < CH; t0 += 8) {
+    for (int tb = t0; tb < t0 + n; tb += 8) {
         float xs[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) xs[e] = to_f32(tile[(t0 + e + HALO) * D + c]);
+        for (int e = 0; e < 8; ++e) xs[e] = to_f32(tile[(tb + e + HALO) * D + c]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             float acc = w.x * x0;
             acc = fmaf(w.y, x1, acc);
             acc = fmaf(w.z, x2, acc);
             acc = fmaf(w.w, xs[e], acc);
-            out[(t0 + e) * D + c] = t0 + e < len ? acc * sigmoid_fast(acc) : 0.f;
+            out[(tb + e) * D + c] = tb + e < len ? acc * sigmoid_fast(acc) : 0.f;
             x0 = x1;
             x1 = x2;
             x2 = xs[e];
@@ -310,7 +311,7 @@ __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS,
 // straight to the record from registers; the W image is staged and
 // bulk-stored.
 template <typename Act>
-__global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillParams p,
+__global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillParams p,
                                                                const __grid_constant__ CUtensorMap tm_q,
                                                                const __grid_constant__ CUtensorMap tm_k,
                                                                const __grid_constant__ CUtensorMap tm_v,
@@ -360,12 +361,14 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     if (tid < CH)
         beta[tid] = tid < cm.len ? to_f32(static_cast<const Act *>(p.beta)[size_t(cm.row0 + tid) * p.H + h]) : 0.f;
     // conv tail of this head (resumed sequences), and the conv taps of the
-    // channel this thread convolves: q (threads 0..127) or k (128..255), and
-    // v (threads 64..191, while T is formed); threads 256..511 form G
+    // channel this thread convolves: q or k (stream qk, channel cc, tokens
+    // 32 qh .. 32 qh + 31), and v (threads 64..319, while T is formed)
     const Act *tail = sq.has_init ? static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch + h * D : nullptr;
-    const int qk = tid >> 7, cc = tid & (D - 1), vc = tid - 64;
-    const float4 w_qk = qk < 2 ? conv_taps<Act>(p, qk, h, cc) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 w_v = (vc >= 0 && vc < D) ? conv_taps<Act>(p, 2, h, vc) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int qk = (tid >> 7) & 1, cc = tid & (D - 1), qh = tid >> 8;
+    const int vt = tid - 64, vc = vt & (D - 1), vh = vt >> 7;
+    const bool v_thread = vt >= 0 && vt < 2 * D;
+    const float4 w_qk = conv_taps<Act>(p, qk, h, cc);
+    const float4 w_v = v_thread ? conv_taps<Act>(p, 2, h, vc) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == 0) tmem_alloc(tbase, 256);
     tc_fence_before();
     __syncthreads();
@@ -373,45 +376,39 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
     const uint32_t tm = *tbase;
     bool ok = __syncthreads_and(mbar_wait(bar_ld, 0, p.err));
     uint32_t mma_phase = 0;
-    // Threads 0..255: SiLU(conv(q)) -> q^ buffer, SiLU(conv(k)) -> k^ buffer
-    // (normalised below).  Threads 256..511 at the same time: G = cumulative
-    // log decay, thread = (channel, half of the chunk); the second half adds
-    // the first half's total below.
+    // SiLU(conv(q)) -> q^ buffer, SiLU(conv(k)) -> k^ buffer (normalised
+    // below): two threads per channel, 32 tokens each.
     float *GGw = reinterpret_cast<float *>(sm + is::GG);
     float *QHw = reinterpret_cast<float *>(sm + is::IN0), *KHw = reinterpret_cast<float *>(sm + is::KH);
-    const int gi = tid & (D - 1), gt0 = ((tid >> 7) & 1) * (CH / 2);
-    if (ok && qk < 2) {
-        conv_silu_channel<Act>(qk ? rk : rq, cc, w_qk, cm.pos0, cm.len, tail ? tail + qk * p.H * D + cc : nullptr, p.n_ch,
-                               qk ? KHw : QHw);
-    } else if (ok) {
+    if (ok)
+        conv_silu_channel<Act>(qk ? rk : rq, cc, w_qk, qh * (CH / 2), CH / 2, cm.pos0, cm.len,
+                               tail ? tail + qk * p.H * D + cc : nullptr, p.n_ch, qk ? KHw : QHw);
+    __syncthreads();
+    // Threads 0..255: G = cumulative log decay, thread = (channel gi, half gh
+    // of the chunk); the second half adds the first half's total below.  (A
+    // 4-byte alpha tile is the G buffer itself: element in, element out.)
+    // Threads 256..511 meanwhile: L2 norm of the 64 q rows and 64 k rows, a
+    // warp per row, 2 rows at a time.
+    const int gi = tid & (D - 1), gh = tid >> 7;
+    if (ok && tid < 2 * D) {
         float G = 0.f;
 #pragma unroll 1
-        for (int t0 = gt0; t0 < gt0 + CH / 2; t0 += 8) {  // 8 logarithms in flight, compact code
+        for (int t0 = gh * (CH / 2); t0 < (gh + 1) * (CH / 2); t0 += 8) {  // 8 logarithms in flight
             float lg[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) lg[e] = to_f32(ra[(t0 + e) * D + gi]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) lg[e] = fmaxf(logf(lg[e]), kLogAlphaMin);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {  // (a 4-byte alpha tile is the G buffer: element in, element out)
+            for (int e = 0; e < 8; ++e) {
                 if (t0 + e < cm.len) G += lg[e];
                 GGw[(t0 + e) * D + gi] = G;
             }
         }
-    }
-    __syncthreads();
-    if (ok && qk >= 2 && gt0 > 0) {
-        const float g31 = GGw[(gt0 - 1) * D + gi];
-        float gv[CH / 2];
-#pragma unroll
-        for (int e = 0; e < CH / 2; ++e) gv[e] = GGw[(gt0 + e) * D + gi];
-#pragma unroll
-        for (int e = 0; e < CH / 2; ++e) GGw[(gt0 + e) * D + gi] = gv[e] + g31;
-    }
-    // L2 norm of the 64 q rows and 64 k rows: a warp per row, 2 rows at a time
-    if (ok) {
+    } else if (ok) {
+        constexpr int LW = is::NT / 32 - 8;  // warps 8..15
 #pragma unroll 1
-        for (int r0 = warp * 2; r0 < 2 * CH; r0 += is::NT / 32 * 2) {
+        for (int r0 = (warp - 8) * 2; r0 < 2 * CH; r0 += LW * 2) {
             float4 v[2];
             float ss[2];
 #pragma unroll
@@ -432,6 +429,15 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
                     make_float4(v[i].x * n, v[i].y * n, v[i].z * n, v[i].w * n);
             }
         }
+    }
+    __syncthreads();
+    if (ok && tid >= D && tid < 2 * D) {
+        const float g31 = GGw[(CH / 2 - 1) * D + gi];
+        float gv[CH / 2];
+#pragma unroll
+        for (int e = 0; e < CH / 2; ++e) gv[e] = GGw[(CH / 2 + e) * D + gi];
+#pragma unroll
+        for (int e = 0; e < CH / 2; ++e) GGw[(CH / 2 + e) * D + gi] = gv[e] + g31;
     }
     __syncthreads();
     if (ok && tid < D) {
@@ -607,14 +613,15 @@ __global__ void __launch_bounds__(is::NT) prefill_intra_kernel(const PrefillPara
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[(b0 + r) * CH + b0 + c] = tc[r];
     }
-    // meanwhile threads 64..191 form v = SiLU(conv(v raw)) in the q^ buffer
+    // meanwhile threads 64..319 form v = SiLU(conv(v raw)) in the q^ buffer,
+    // two threads per channel
     bool vok = true;
-    if (vc >= 0 && vc < D) {
+    if (v_thread) {
         // a late tile is only requested while ok; an early one is always in flight
         vok = (is::v_early<Act>() || ok) ? mbar_wait(bar_v, 0, p.err) : false;
         if (ok && vok)
-            conv_silu_channel<Act>(rv, vc, w_v, cm.pos0, cm.len, tail ? tail + 2 * p.H * D + vc : nullptr, p.n_ch,
-                                   reinterpret_cast<float *>(sm + is::IN0));
+            conv_silu_channel<Act>(rv, vc, w_v, vh * (CH / 2), CH / 2, cm.pos0, cm.len,
+                                   tail ? tail + 2 * p.H * D + vc : nullptr, p.n_ch, reinterpret_cast<float *>(sm + is::IN0));
     }
     ok = __syncthreads_and(ok && vok);
     // Blocks below the diagonal, by distance d: T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
