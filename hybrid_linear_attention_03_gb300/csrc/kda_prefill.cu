@@ -106,9 +106,23 @@ struct PrefillParams {
 };
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
-// sigma(x) with the hardware exp2 / reciprocal approximations (relative error
-// a few 1e-7; 0 for x below about -88, where exp(-x) overflows to inf).
-__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+// PTX's approximate 2^x and 1/x (flush-to-zero; relative errors of a few
+// 1e-7 and about 1 ulp).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// sigma(x) = 1 / (1 + e^-x), with e^-x = 2^(-x log2 e): 0 for x below about
+// -88, where 2^(-x log2 e) is +inf.
+__device__ __forceinline__ float sigmoid_fast(float x) {
+    return rcp_approx(1.0f + ex2_approx(-x * 1.4426950408889634f));
+}
 
 __device__ __forceinline__ char *rec_ptr(const PrefillParams &p, int g, int h) {
     return p.rec + (size_t(g) * p.H + h) * Rec::BYTES;
@@ -490,7 +504,7 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
             ld8(KHs + r * D + k0, a);
             ld8(EE + r * D + k0, ee);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __fdividef(a[e], ee[e]);  // ee in [e^-80, e^80]
+            for (int e = 0; e < 8; ++e) x[e] = a[e] * rcp_approx(ee[e]);  // ee in [e^-80, e^80]
         });
         fence_proxy_async_smem();
         tc_fence_before();
@@ -520,7 +534,7 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const float gv = GGs[(r0 + e) * D + i];
-                            x[e] = KHs[(r0 + e) * D + i] * (exact ? expf(gl - gv) : __fdividef(l, gv));
+                            x[e] = KHs[(r0 + e) * D + i] * (exact ? expf(gl - gv) : l * rcp_approx(gv));
                         }
                     });
     }
