@@ -492,20 +492,41 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
 
     // ---- phase 1: X = [K exp(G - c); Q exp(G - c)], Kb = K exp(c - G) -> A, P
     if (ok && !exact) {
-        build_image(sm + is::X_HI, sm + is::X_LO, 128, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
-            float a[8], ee[8];
-            ld8(r < CH ? KHs + r * D + k0 : QHs + (r - CH) * D + k0, a);
-            ld8(EE + (r & (CH - 1)) * D + k0, ee);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = a[e] * ee[e];
-        });
-        build_image(sm + is::KB_HI, sm + is::KB_LO, CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
-            float a[8], ee[8];
-            ld8(KHs + r * D + k0, a);
+        // One pass over (row r, 8-channel chunk c) of k^, q^ and E, which are
+        // read once: X rows r and 64 + r = k^ E and q^ E, Kb row r = k^ / E, and
+        // the chain's exp(G) . q image row 64 + r = q^ (E e^c) in the record.
+        unsigned char *wq_hi = reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI);
+        unsigned char *wq_lo = reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO);
+#pragma unroll 1
+        for (int u = tid; u < CH * (D / 8); u += is::NT) {
+            const int r = u / (D / 8), c = u % (D / 8), k0 = 8 * c;
+            float kk[8], qq[8], ee[8], cc[8], x[8];
+            ld8(KHs + r * D + k0, kk);
+            ld8(QHs + r * D + k0, qq);
             ld8(EE + r * D + k0, ee);
+            ld8(ec + k0, cc);
+            uint4 vh, vl;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = a[e] * rcp_approx(ee[e]);  // ee in [e^-80, e^80]
-        });
+            for (int e = 0; e < 8; ++e) x[e] = kk[e] * ee[e];
+            split8(x, vh, vl);
+            *reinterpret_cast<uint4 *>(sm + is::X_HI + sw128_chunk(r, c, 2 * CH)) = vh;
+            *reinterpret_cast<uint4 *>(sm + is::X_LO + sw128_chunk(r, c, 2 * CH)) = vl;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = qq[e] * ee[e];
+            split8(x, vh, vl);
+            *reinterpret_cast<uint4 *>(sm + is::X_HI + sw128_chunk(CH + r, c, 2 * CH)) = vh;
+            *reinterpret_cast<uint4 *>(sm + is::X_LO + sw128_chunk(CH + r, c, 2 * CH)) = vl;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = kk[e] * rcp_approx(ee[e]);  // ee in [e^-80, e^80]
+            split8(x, vh, vl);
+            *reinterpret_cast<uint4 *>(sm + is::KB_HI + sw128_chunk(r, c, CH)) = vh;
+            *reinterpret_cast<uint4 *>(sm + is::KB_LO + sw128_chunk(r, c, CH)) = vl;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = qq[e] * (ee[e] * cc[e]);
+            split8(x, vh, vl);
+            *reinterpret_cast<uint4 *>(wq_hi + sw128_chunk(CH + r, c, 2 * CH)) = vh;
+            *reinterpret_cast<uint4 *>(wq_lo + sw128_chunk(CH + r, c, 2 * CH)) = vl;
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -516,17 +537,19 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
             mma_commit(bar_mma);
         }
     }
-    // chain images that need no MMA: exp(G) . q (rows r) and (exp(G_last - G) . k)^T (rows i)
-    if (ok) {
+    // chain images that need no MMA: exp(G) . q (rows r; above when !exact) and
+    // (exp(G_last - G) . k)^T (rows i)
+    if (ok && exact) {
         build_image(reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI), reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO),
                     CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
-                        float a[8], gg[8], cc[8];
+                        float a[8], gg[8];
                         ld8(QHs + r * D + k0, a);
-                        ld8(GGs + r * D + k0, gg);  // E when !exact, G when exact
-                        ld8(ec + k0, cc);
+                        ld8(GGs + r * D + k0, gg);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = a[e] * (exact ? expf(gg[e]) : gg[e] * cc[e]);
+                        for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(gg[e]);
                     }, CH, 2 * CH);
+    }
+    if (ok) {
         build_image<true>(reinterpret_cast<unsigned char *>(rec + Rec::KP_HI),
                     reinterpret_cast<unsigned char *>(rec + Rec::KP_LO), D, 8, tid, is::NT,
                     [&](int i, int r0, float(&x)[8]) {
