@@ -56,7 +56,7 @@ constexpr int CH = 64;   // chunk length
 constexpr int HALO = 3;  // previous raw inputs the width-4 conv needs
 constexpr float kLogAlphaMin = -100.0f;  // log(alpha) floor: alpha below e^-100 acts as e^-100
 constexpr float kSafeSpan = 160.0f;      // max per-channel log-decay span for the split exponent
-constexpr int kMaxWindows = 8;           // chunk windows overlapped across two streams
+constexpr int kMaxWindows = 8;           // chunk windows overlapped across the streams
 constexpr int kMinWindowChunks = 32;     // smallest window worth a separate chain launch
 
 struct SeqMeta {
@@ -100,7 +100,7 @@ struct PrefillParams {
     void *out;
     const void *conv_w, *norm_w;
     int32_t H, n_ch, n_seqs, n_chunks, n_ckpts;
-    int32_t chunk_base;      // intra: global index of blockIdx.x == 0
+    int32_t chunk_base;      // intra, out: global index of blockIdx.x == 0
     int32_t win_lo, win_hi;  // chain: global chunk range of this launch
     float eps_l2, eps_rms;
 };
@@ -143,6 +143,12 @@ __device__ __forceinline__ void ld8(const float *p, float (&x)[8]) {  // p 16-by
 
 template <typename Act>
 __device__ __forceinline__ float4 act4(const Act *p);
+// 4 values -> 4 consecutive activations (16-byte fp32 or 8-byte bf16 store, round to nearest even)
+__device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+}
 template <>
 __device__ __forceinline__ float4 act4<float>(const float *p) {
     return *reinterpret_cast<const float4 *>(p);
@@ -153,6 +159,34 @@ __device__ __forceinline__ float4 act4<__nv_bfloat16>(const __nv_bfloat16 *p) {
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
     return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// ln(alpha) of 8 values.  A positive normal bf16 value is 2^e (1 + m/128):
+// its log is e ln 2 + ln(1 + m/128), the second term from a 128-entry table
+// (lnm).  When any lane of the warp holds a zero, subnormal, negative or
+// non-finite value, the whole warp takes logf for these 8 (a warp-uniform
+// branch keeps logf out of the common path); fp32 values always use logf.
+__device__ __forceinline__ void log_alpha8(const float (&a)[8], const float *, float (&l)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) l[e] = logf(a[e]);
+}
+__device__ __forceinline__ void log_alpha8(const __nv_bfloat16 (&a)[8], const float *lnm, float (&l)[8]) {
+    bool normal = true;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t b = __bfloat16_as_ushort(a[e]), ex = (b >> 7) & 0xFFu;
+        normal = normal && (b >> 15) == 0 && ex != 0 && ex != 0xFFu;
+    }
+    if (__all_sync(0xffffffffu, normal)) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t b = __bfloat16_as_ushort(a[e]);
+            l[e] = fmaf(float(int((b >> 7) & 0xFFu) - 127), 0.6931471805599453f, lnm[b & 0x7Fu]);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) l[e] = logf(__bfloat162float(a[e]));
+    }
 }
 
 // ======================================================= conv helper ====
@@ -211,6 +245,7 @@ constexpr uint32_t GG = 163840;   // fp32 [64][128] G, then E = exp(G - c)
 constexpr uint32_t SMALL = 196608;
 constexpr uint32_t RV_LATE = 32768;         // raw v tile of a 4-byte activation (free while T is formed)
 constexpr uint32_t RV_EARLY = SMALL + 2560; // raw v tile of a 2-byte activation (loaded with the others)
+constexpr uint32_t TDIAG = RV_EARLY + (CH + HALO) * D * 2;  // [4][16 s][16 r] diagonal blocks of T, transposed
 constexpr int NT = 512;
 constexpr int QW = NT / 128;  // warps per TMEM lane quarter (a warp reaches lanes 32 (w % 4) .. + 31)
 template <typename Act>
@@ -228,12 +263,13 @@ __host__ __device__ constexpr uint32_t RV() { return v_early<Act>() ? RV_EARLY :
 template <typename Act>
 __host__ __device__ constexpr uint32_t RA() { return sizeof(Act) == 2 ? RK<Act>() + tile_bytes<Act>() : GG; }
 template <typename Act>
-__host__ __device__ constexpr uint32_t BYTES() { return v_early<Act>() ? RV_EARLY + tile_bytes<Act>() : SMALL + 2560; }
+__host__ __device__ constexpr uint32_t BYTES() { return TDIAG + 4 * 16 * 16 * 4; }
 template <typename Act>
 __host__ __device__ constexpr bool map_ok() {
     return RK<Act>() + tile_bytes<Act>() <= IN0 && (sizeof(Act) != 2 || RA<Act>() + CH * D * sizeof(Act) <= IN0) &&
            (v_early<Act>() || (RV_LATE >= XS_F32 + 16384 && RV_LATE + tile_bytes<Act>() <= T_F32)) &&
-           BYTES<Act>() + 1024 <= 232448 && tile_bytes<Act>() % 128 == 0;
+           (!v_early<Act>() || RV_EARLY + tile_bytes<Act>() <= TDIAG) && BYTES<Act>() + 1024 <= 232448 &&
+           tile_bytes<Act>() % 128 == 0;
 }
 }  // namespace is
 
@@ -280,10 +316,12 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
 }
 
 // One level of the blocked inverse of I + A (A stored transposed: A[s * CH +
-// r] = A_rs): the 4 - d blocks at distance d below the diagonal; a thread
-// owns 4 adjacent columns of one row, so each A value it loads feeds 4 FMAs
-// and the T / X values arrive as 16-byte vectors.
-__device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS, int tid, int d) {
+// r] = A_rs; TD holds T's diagonal blocks transposed): the 4 - d blocks at
+// distance d below the diagonal; a thread owns 4 adjacent columns of one row,
+// so each A value it loads feeds 4 FMAs and the T / X values arrive as
+// 16-byte vectors; the 8 rows a warp covers read A and TD without bank
+// conflicts.
+__device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS, const float *TD, int tid, int d) {
     const int nblk = 4 - d;
     for (int e = tid; e < nblk * 64; e += is::NT) {
         const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4, a = blk + d, b = blk;
@@ -305,7 +343,7 @@ __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS,
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int s = 0; s < 16; ++s) {
-            const float tv = -T[(a * 16 + r) * CH + a * 16 + s];
+            const float tv = -TD[(a * 16 + s) * 16 + r];  // T[a16 + r][a16 + s]
             const float4 xv = ld4(XS + (a * 16 + s) * CH + b * 16 + c4);
             acc.x = fmaf(tv, xv.x, acc.x);
             acc.y = fmaf(tv, xv.y, acc.y);
@@ -397,6 +435,8 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
     if (ok)
         conv_silu_channel<Act>(qk ? rk : rq, cc, w_qk, qh * (CH / 2), CH / 2, cm.pos0, cm.len,
                                tail ? tail + qk * p.H * D + cc : nullptr, p.n_ch, qk ? KHw : QHw);
+    // ln of the 128 bf16 mantissas 1 + m/128, in the c buffer (written only after G)
+    if (sizeof(Act) == 2 && tid < D) cref[tid] = logf(1.0f + float(tid) * (1.0f / 128.0f));
     __syncthreads();
     // Threads 0..255: G = cumulative log decay, thread = (channel gi, half gh
     // of the chunk); the second half adds the first half's total below.  (A
@@ -408,11 +448,13 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
         float G = 0.f;
 #pragma unroll 1
         for (int t0 = gh * (CH / 2); t0 < (gh + 1) * (CH / 2); t0 += 8) {  // 8 logarithms in flight
+            Act av[8];
             float lg[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) lg[e] = to_f32(ra[(t0 + e) * D + gi]);
+            for (int e = 0; e < 8; ++e) av[e] = ra[(t0 + e) * D + gi];
+            log_alpha8(av, cref, lg);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) lg[e] = fmaxf(logf(lg[e]), kLogAlphaMin);
+            for (int e = 0; e < 8; ++e) lg[e] = fmaxf(lg[e], kLogAlphaMin);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 if (t0 + e < cm.len) G += lg[e];
@@ -631,6 +673,7 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
     // ---- T = (I + A)^-1 (unit lower triangular), 16 x 16 blocks
     float *T = reinterpret_cast<float *>(sm + is::T_F32);
     float *XS = reinterpret_cast<float *>(sm + is::XS_F32);
+    float *TD = reinterpret_cast<float *>(sm + is::TDIAG);  // TD[(a16 + s) 16 + r] = T[a16 + r][a16 + s]
     for (int e = tid; e < CH * CH; e += is::NT) T[e] = 0.f;  // the blocks above the diagonal stay 0
     __syncthreads();
     // Diagonal 16 x 16 blocks by forward substitution, a lane per column with
@@ -649,6 +692,9 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[(b0 + r) * CH + b0 + c] = tc[r];
+#pragma unroll
+        for (int r4 = 0; r4 < 16; r4 += 4)
+            *reinterpret_cast<float4 *>(TD + (b0 + c) * 16 + r4) = make_float4(tc[r4], tc[r4 + 1], tc[r4 + 2], tc[r4 + 3]);
     }
     // meanwhile threads 64..319 form v = SiLU(conv(v raw)) in the q^ buffer,
     // two threads per channel
@@ -663,7 +709,7 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
     ok = __syncthreads_and(ok && vok);
     // Blocks below the diagonal, by distance d: T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
 #pragma unroll 1
-    for (int d = 1; d < 4; ++d) tri_offdiag(A, T, XS, tid, d);
+    for (int d = 1; d < 4; ++d) tri_offdiag(A, T, XS, TD, tid, d);
     // ---- phase 3: W^T = (beta exp(G) . K)^T T^T and Ut^T = (beta V)^T T^T
     if (ok) {
         build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, is::NT, [&](int r, int s0, float(&x)[8]) {
@@ -956,25 +1002,23 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
 // ================================================================ out ====
 template <typename Act>
 __global__ void __launch_bounds__(128) prefill_out_kernel(const PrefillParams p) {
-    const int g = blockIdx.x, h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const ChunkMeta cm = p.chunks[g];
     const float *O = reinterpret_cast<const float *>(rec_ptr(p, g, h) + Rec::OO);
     const Act *gate = static_cast<const Act *>(p.gate);
-    const Act *nw = static_cast<const Act *>(p.norm_w);
     Act *out = static_cast<Act *>(p.out);
     const size_t HD = size_t(p.H) * D;
+    const Act *nwp = static_cast<const Act *>(p.norm_w) + lane * 4;  // no alignment asked of norm_w
+    const float4 wn = make_float4(to_f32(nwp[0]), to_f32(nwp[1]), to_f32(nwp[2]), to_f32(nwp[3]));
     for (int t = warp; t < cm.len; t += 4) {
+        const size_t base = size_t(cm.row0 + t) * HD + size_t(h) * D + lane * 4;
         const float4 o4 = ld4(O + t * D + lane * 4);
-        const float o[4] = {o4.x, o4.y, o4.z, o4.w};
-        float ss = 0.f;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) ss = fmaf(o[m], o[m], ss);
+        const float4 g4 = act4(gate + base);
+        float ss = fmaf(o4.x, o4.x, fmaf(o4.y, o4.y, fmaf(o4.z, o4.z, o4.w * o4.w)));
         for (int s = 16; s; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
         const float r = rsqrtf(ss * (1.0f / D) + p.eps_rms);
-        const size_t base = size_t(cm.row0 + t) * HD + size_t(h) * D + lane * 4;
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-            out[base + m] = from_f32<Act>(to_f32(nw[lane * 4 + m]) * (o[m] * r) * sigmoid_f(to_f32(gate[base + m])));
+        store4(out + base, make_float4(wn.x * (o4.x * r) * sigmoid_f(g4.x), wn.y * (o4.y * r) * sigmoid_f(g4.y),
+                                       wn.z * (o4.z * r) * sigmoid_f(g4.z), wn.w * (o4.w * r) * sigmoid_f(g4.w)));
     }
 }
 
@@ -1080,12 +1124,15 @@ constexpr size_t intra_smem() {
 }
 constexpr size_t kChainSmem = 1024 + cs::BYTES;
 
-// Per-device side stream (highest priority) and events for the windowed
-// overlap of the chain with the per-chunk kernels.  Not memory: nothing here
-// allocates device memory.
+// Per-device side streams (the chain's at the highest priority) and events
+// for the windowed overlap of the chain and the gated norm with the per-chunk
+// kernels.  Not memory: nothing here allocates device memory.
 struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t ev[2 * kMaxWindows + 1] = {};
+    cudaStream_t s = nullptr;  // chain (highest priority)
+    cudaStream_t o = nullptr;  // gated norm of finished windows
+    // [0, W): window w's intra done; [W, 2W): window w's chain done;
+    // 2W: call start; 2W + 1, 2W + 2: chain / norm streams done
+    cudaEvent_t ev[2 * kMaxWindows + 3] = {};
     bool ok = false;
 };
 
@@ -1099,6 +1146,7 @@ SideStream *side_stream() {
         int lo = 0, hi = 0;
         if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return;
         if (cudaStreamCreateWithPriority(&x.s, cudaStreamNonBlocking, hi) != cudaSuccess) return;
+        if (cudaStreamCreateWithPriority(&x.o, cudaStreamNonBlocking, lo) != cudaSuccess) return;
         for (auto &e : x.ev)
             if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return;
         x.ok = true;
@@ -1121,9 +1169,10 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
             return KDA_ERR_CUDA;
     }
     // Windows of chunks: the chain of window w (one CTA per sequence and
-    // head, on the side stream) runs while intra of window w + 1
-    // fill the other SMs; events order each chain launch after its window's
-    // records and the final join returns everything to the caller's stream.
+    // head, on the side stream) and then the gated norm of its chunks run
+    // while intra of window w + 1 fills the other SMs; events order each
+    // chain launch after its window's records and the final join returns
+    // everything to the caller's stream.
     // The side stream's events are shared by every caller of this device:
     // one call's record / wait sequence is enqueued as a whole.
     static std::mutex enqueue_mu;
@@ -1135,10 +1184,11 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
         if (side) n_win = int(std::min<long long>(kMaxWindows, n_chunks / kMinWindowChunks));
     }
     const long long per = (n_chunks + n_win - 1) / n_win;
-    cudaStream_t cs = side ? side->s : stream;
-    if (side) {  // the side stream starts after everything already on the caller's stream
-        if (cudaEventRecord(side->ev[2 * kMaxWindows], stream) != cudaSuccess ||
-            cudaStreamWaitEvent(cs, side->ev[2 * kMaxWindows], 0) != cudaSuccess)
+    cudaStream_t cs = side ? side->s : stream, os = side ? side->o : stream;
+    constexpr int W = kMaxWindows;
+    if (side) {  // the chain stream starts after everything already on the caller's stream
+        if (cudaEventRecord(side->ev[2 * W], stream) != cudaSuccess ||
+            cudaStreamWaitEvent(cs, side->ev[2 * W], 0) != cudaSuccess)
             return KDA_ERR_CUDA;
     }
     for (int w = 0; w < n_win; ++w) {
@@ -1155,14 +1205,25 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
                 return KDA_ERR_CUDA;
         }
         prefill_chain_kernel<<<unsigned(N) * p.H, 256, kChainSmem, cs>>>(p);
+        if (hi > lo) {  // gated norm of the window's chunks once their chain is done, off the chain's stream
+            if (side) {
+                if (cudaEventRecord(side->ev[W + w], cs) != cudaSuccess ||
+                    cudaStreamWaitEvent(os, side->ev[W + w], 0) != cudaSuccess)
+                    return KDA_ERR_CUDA;
+            }
+            PrefillParams po = p;
+            po.chunk_base = int(lo);
+            prefill_out_kernel<Act><<<dim3(unsigned(hi - lo), unsigned(p.H)), 128, 0, os>>>(po);
+        }
     }
     if (side) {
-        if (cudaEventRecord(side->ev[kMaxWindows], cs) != cudaSuccess ||
-            cudaStreamWaitEvent(stream, side->ev[kMaxWindows], 0) != cudaSuccess)
+        if (cudaEventRecord(side->ev[2 * W + 1], cs) != cudaSuccess ||
+            cudaEventRecord(side->ev[2 * W + 2], os) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, side->ev[2 * W + 1], 0) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, side->ev[2 * W + 2], 0) != cudaSuccess)
             return KDA_ERR_CUDA;
     }
     p.chunk_base = 0;
-    if (n_chunks > 0) prefill_out_kernel<Act><<<dim3(unsigned(n_chunks), unsigned(p.H)), 128, 0, stream>>>(p);
     if (n_reqs > 0) prefill_tails_kernel<Act><<<n_reqs, 256, 0, stream>>>(p, 1);
     prefill_tails_kernel<Act><<<N, 256, 0, stream>>>(p, 0);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
