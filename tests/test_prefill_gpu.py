@@ -100,6 +100,26 @@ def test_prefill_strong_decay_takes_exact_path():
     _check(m, out, ref, [0])
 
 
+def test_prefill_alpha_edge_values():
+    """bf16 alpha with exact zeros, subnormals, exact ones and 1 - 2^-8 mixed
+    in: both ways the kernel takes log(alpha) (per-exponent table, and logf
+    for zero / subnormal lanes) match the oracle, and alpha = 0 erases."""
+    H, act, L = 2, torch.bfloat16, 150
+    m = Mirror(4, H, D, act, I.layer_weights(59, H, D, D, 4, act))
+    inp = I.token_inputs(59, 0, L, H, D, D, 2.0, act)
+    a = inp["alpha"].float()
+    idx = torch.arange(a.numel()).view_as(a)
+    a = torch.where(idx % 7 == 0, torch.zeros_like(a), a)
+    a = torch.where(idx % 11 == 0, torch.full_like(a, 5e-39), a)  # below the smallest normal, 1.18e-38
+    a = torch.where(idx % 13 == 0, torch.ones_like(a), a)
+    a = torch.where(idx % 17 == 0, torch.full_like(a, 1.0 - 2.0 ** -8), a)
+    inp["alpha"] = a.to(act)
+    assert (inp["alpha"].float() == 0).any() and ((inp["alpha"].float() > 0) & (inp["alpha"].float() < 1.18e-38)).any()
+    out = prefill_gpu(m, hp.to_device(inp), [L], [0], [0])
+    ref = prefill_oracle(m, inp, [L], [0], [0])
+    _check(m, out, ref, [0])
+
+
 def test_decode_after_prefill_equals_one_long_run():
     H, act = 4, torch.bfloat16
     m = Mirror(4, H, D, act, I.layer_weights(53, H, D, D, 4, act))
