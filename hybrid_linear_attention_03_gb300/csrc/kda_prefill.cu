@@ -355,7 +355,7 @@ __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS,
     __syncthreads();
 }
 
-// One CTA (8 warps) per (chunk, head).  TMA brings the raw q, k, v tiles of
+// One CTA (16 warps) per (chunk, head).  TMA brings the raw q, k, v tiles of
 // the chunk's 64 tokens plus the 3 before them (the conv halo) and the alpha
 // tile; the kernel forms G, q^, k^ (conv + SiLU + L2) and v (conv + SiLU) in
 // shared memory, so every operand build reads shared memory.  Images the
@@ -414,11 +414,12 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
         beta[tid] = tid < cm.len ? to_f32(static_cast<const Act *>(p.beta)[size_t(cm.row0 + tid) * p.H + h]) : 0.f;
     // conv tail of this head (resumed sequences), and the conv taps of the
     // channel this thread convolves: q or k (stream qk, channel cc, tokens
-    // 32 qh .. 32 qh + 31), and v (threads 64..319, while T is formed)
+    // 32 qh .. 32 qh + 31), and v (threads 64..447, three per channel, while
+    // T is formed)
     const Act *tail = sq.has_init ? static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch + h * D : nullptr;
     const int qk = (tid >> 7) & 1, cc = tid & (D - 1), qh = tid >> 8;
     const int vt = tid - 64, vc = vt & (D - 1), vh = vt >> 7;
-    const bool v_thread = vt >= 0 && vt < 2 * D;
+    const bool v_thread = vt >= 0 && vt < 3 * D;
     const float4 w_qk = conv_taps<Act>(p, qk, h, cc);
     const float4 w_v = v_thread ? conv_taps<Act>(p, 2, h, vc) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp == 0) tmem_alloc(tbase, 256);
@@ -696,14 +697,14 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
         for (int r4 = 0; r4 < 16; r4 += 4)
             *reinterpret_cast<float4 *>(TD + (b0 + c) * 16 + r4) = make_float4(tc[r4], tc[r4 + 1], tc[r4 + 2], tc[r4 + 3]);
     }
-    // meanwhile threads 64..319 form v = SiLU(conv(v raw)) in the q^ buffer,
-    // two threads per channel
+    // meanwhile threads 64..447 form v = SiLU(conv(v raw)) in the q^ buffer,
+    // three threads per channel (tokens 0..23, 24..47, 48..63)
     bool vok = true;
     if (v_thread) {
         // a late tile is only requested while ok; an early one is always in flight
         vok = (is::v_early<Act>() || ok) ? mbar_wait(bar_v, 0, p.err) : false;
         if (ok && vok)
-            conv_silu_channel<Act>(rv, vc, w_v, vh * (CH / 2), CH / 2, cm.pos0, cm.len,
+            conv_silu_channel<Act>(rv, vc, w_v, vh * 24, vh < 2 ? 24 : CH - 48, cm.pos0, cm.len,
                                    tail ? tail + 2 * p.H * D + vc : nullptr, p.n_ch, reinterpret_cast<float *>(sm + is::IN0));
     }
     ok = __syncthreads_and(ok && vok);
