@@ -278,9 +278,9 @@ __host__ __device__ constexpr bool map_ok() {
 // Row-major unit order (consecutive threads walk one row's chunks) suits f
 // reading rows of a [row][K] array; chunk-major order (consecutive threads
 // take consecutive rows of one chunk) suits f reading columns of a [K][row]
-// array without shared-memory bank conflicts.  A thread gathers the inputs of
-// 4 units before it stores any, so their load latencies overlap (the stores
-// could alias the inputs as far as the compiler knows).
+// array without shared-memory bank conflicts.  The loop is kept rolled: this
+// kernel runs each phase once per CTA, so compact code (fewer instruction
+// cache misses) measured faster than unrolled, batched loads.
 template <bool kChunkMajor = false, typename F>
 __device__ __forceinline__ void build_image(unsigned char *hi, unsigned char *lo, int rows, int chunks_per_row,
                                             int tid, int nthreads, F f, int row0 = 0, int total_rows = 0) {
