@@ -42,7 +42,15 @@
 namespace kda {
 namespace {
 
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+// sigma(x) = 1 / (1 + e^-x) with e^-x = 2^(-x log2 e), from PTX's approximate
+// 2^x and 1/x (flush-to-zero; relative errors of a few 1e-7 and about 1 ulp).
+// 0 for x below about -88, where 2^(-x log2 e) is +inf.
+__device__ __forceinline__ float sigmoid_f(float x) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-x * 1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return r;
+}
 
 __device__ __forceinline__ float dot4(const float4 a, const float4 b) {
     return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, a.x * b.x)));
@@ -107,14 +115,14 @@ __host__ __device__ constexpr size_t pad4(size_t n) { return (n + 3) / 4 * 4; }
 // Dynamic shared memory, in order (every part starts on a 16-byte boundary):
 // staging, conv outputs [T][3][D], u rows [WPC][16], o [T][D], per-warp sums
 // of squares [T][WPC], beta [T], snapshot slots [T], then in the activation
-// type the raw conv window [T+3][3][D] (old tail + tokens), alpha [T][D] and
-// the gate logits [T][D].
+// type the raw conv window [T+3][3][D] (old tail + tokens), alpha [T][D],
+// the gate logits [T][D] and the head's conv taps [3][D][4].
 template <int D, typename Act>
 __host__ __device__ constexpr size_t step_smem_bytes(int T) {
     constexpr int WPC = D / 16;
     return sizeof(float) * (stage_floats<D>(T) + size_t(T) * 3 * D + WPC * 16 + size_t(T) * D +
                             pad4(size_t(T) * WPC) + 2 * pad4(size_t(T))) +
-           sizeof(Act) * (size_t(T + 3) * 3 * D + 2 * size_t(T) * D);
+           sizeof(Act) * (size_t(T + 3) * 3 * D + 2 * size_t(T) * D + 3 * D * 4);
 }
 
 template <int D, typename Act>
@@ -133,6 +141,7 @@ kda_step_kernel(const StepParams p) {
     Act *raw = reinterpret_cast<Act *>(snap_sm + pad4(T));   // [T+3][3][D]
     Act *araw = raw + size_t(T + 3) * 3 * D;                 // [T][D] alpha
     Act *graw = araw + size_t(T) * D;                        // [T][D] gate logits
+    Act *wtap = graw + size_t(T) * D;                        // [3][D][4] conv taps
 
     const int b = blockIdx.x / p.H, h = blockIdx.x - b * p.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -154,6 +163,12 @@ kda_step_kernel(const StepParams p) {
         const Act *src = static_cast<const Act *>(r == 0 ? p.q : r == 1 ? p.k : r == 2 ? p.v : r == 3 ? p.alpha : p.gate);
         Act *dst = r < 3 ? raw + size_t((t + 3) * 3 + r) * D : (r == 3 ? araw : graw) + size_t(t) * D;
         sm100::cp_async16(dst + cc * EPC, src + src_off);
+    }
+    // the head's conv taps: per stream, D channels x 4 taps contiguous
+    for (int i = threadIdx.x; i < 3 * 4 * CPR; i += C::NT) {
+        const int st = i / (4 * CPR), cc = i - st * 4 * CPR;
+        sm100::cp_async16(wtap + size_t(st) * D * 4 + cc * EPC,
+                          static_cast<const Act *>(p.conv_w) + (size_t(st) * p.H + h) * D * 4 + cc * EPC);
     }
     sm100::cp_async_commit();
     if (threadIdx.x < T) bsm[threadIdx.x] = to_f32(beta[(size_t(b) * T + threadIdx.x) * p.H + h]);
@@ -177,18 +192,6 @@ kda_step_kernel(const StepParams p) {
     const int own_row = n_own * C::RPL + sub;  // 0..15 within the warp
     const int own_j = warp * 16 + own_row;     // value channel this lane reports
 
-    // conv taps of this thread's channels
-    const Act *cw = static_cast<const Act *>(p.conv_w);
-    constexpr int PER = (3 * D + C::NT - 1) / C::NT;
-    float4 wv[PER];
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int idx = threadIdx.x + u * C::NT;
-        if (idx < 3 * D) {
-            const int s = idx / D, c = idx - s * D;
-            wv[u] = load4(cw + size_t(s * p.H * D + h * D + c) * 4);
-        }
-    }
     // The pool's state and tail may have been written by the preceding step
     // launch: wait for it to complete before reading them.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -211,37 +214,36 @@ kda_step_kernel(const StepParams p) {
     sm100::cp_async_wait_all();
     __syncthreads();
 
-    // ---- conv + SiLU for the head's 3*D channels over the T tokens --------
+    // ---- conv + SiLU (+ L2 for q and k): a warp per (token, stream) row --------
+    for (int row = warp; row < 3 * T; row += C::WPC) {
+        const int t = row / 3, s = row - t * 3;
+        float y[(D + 31) / 32];
+        float ss = 0.f;
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int idx = threadIdx.x + u * C::NT;
-        if (idx < 3 * D) {
-            const int s = idx / D, c = idx - s * D;
-            float x0 = to_f32(raw[(0 * 3 + s) * D + c]), x1 = to_f32(raw[(1 * 3 + s) * D + c]);
-            float x2 = to_f32(raw[(2 * 3 + s) * D + c]);
-            for (int t = 0; t < T; ++t) {
-                const float xt = to_f32(raw[((t + 3) * 3 + s) * D + c]);
-                float acc = wv[u].x * x0;
-                acc = fmaf(wv[u].y, x1, acc);
-                acc = fmaf(wv[u].z, x2, acc);
-                acc = fmaf(wv[u].w, xt, acc);
-                conv[(t * 3 + s) * D + c] = acc * sigmoid_f(acc);
-                x0 = x1;
-                x1 = x2;
-                x2 = xt;
+        for (int m = 0; m < (D + 31) / 32; ++m) {
+            const int c = lane + 32 * m;
+            y[m] = 0.f;
+            if (c < D) {
+                const float4 w = load4(wtap + (size_t(s) * D + c) * 4);
+                float acc = w.x * to_f32(raw[((t + 0) * 3 + s) * D + c]);
+                acc = fmaf(w.y, to_f32(raw[((t + 1) * 3 + s) * D + c]), acc);
+                acc = fmaf(w.z, to_f32(raw[((t + 2) * 3 + s) * D + c]), acc);
+                acc = fmaf(w.w, to_f32(raw[((t + 3) * 3 + s) * D + c]), acc);
+                y[m] = acc * sigmoid_f(acc);
+                ss = fmaf(y[m], y[m], ss);
             }
         }
-    }
-    __syncthreads();
-    // ---- L2 norm of q and k per token ---------------------------------------
-    for (int pr = warp; pr < 2 * T; pr += C::WPC) {
-        float *x = conv + ((pr >> 1) * 3 + (pr & 1)) * D;
-        float ss = 0.f;
-        for (int c = lane; c < D; c += 32) ss = fmaf(x[c], x[c], ss);
+        float r = 1.f;
+        if (s < 2) {  // q and k: L2 norm over the head's D channels
 #pragma unroll
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float r = rsqrtf(ss + p.eps_l2);
-        for (int c = lane; c < D; c += 32) x[c] *= r;
+            for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            r = rsqrtf(ss + p.eps_l2);
+        }
+#pragma unroll
+        for (int m = 0; m < (D + 31) / 32; ++m) {
+            const int c = lane + 32 * m;
+            if (c < D) conv[(t * 3 + s) * D + c] = y[m] * r;
+        }
     }
     // The old tail is fully read (raw) before any snapshot tail is written.
     __syncthreads();
