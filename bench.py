@@ -86,8 +86,9 @@ def args_():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
-    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "prefill", "mixed"], default=None,
-                    help="run one secondary case alone (for profiling) and print its numbers")
+    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "prefill", "mixed", "mma_rates"], default=None,
+                    help="run one secondary case alone (for profiling) and print its numbers; mma_rates times "
+                         "the prefill's tensor-core MMA groups in a separately built timing library")
     ap.add_argument("--prefill-tokens", type=int, default=None,
                     help="with --only prefill: a shorter sequence of the same workload (small profiling case)")
     return ap.parse_args()
@@ -177,7 +178,9 @@ def run_ours(a, rank, world, local):
     hbm_peak, tf_peak, _, peak_kind = load_peaks()
     if a.only:
         kbuild.build()
-        if a.only == "prefill":
+        if a.only == "mma_rates":
+            res = mma_rates(kbuild, kda, dev, tf_peak, peak_kind, L=a.prefill_tokens or 8192)
+        elif a.only == "prefill":
             res = prefill_case(kda, dev, iters=a.steps, warmup=a.warmup, L=a.prefill_tokens)
         elif a.only == "mixed":
             res = mixed_case(kda, dev, iters=a.steps, warmup=a.warmup)
@@ -475,6 +478,65 @@ def mixed_case(kda, dev, iters=3, warmup=1):
 
 
 # ----------------------------------------------------------------------- oracle
+
+def mma_rates(kbuild, kda, dev, tf_peak, peak_kind, L=8192):
+    """Tensor-core rate of each prefill MMA group while it runs.  A timing build
+    of the library (-DKDA_MMA_TIMING) has thread 0 wait for each group right
+    after issuing it and accumulate clock64 cycles from the first issue to the
+    completion.  FLOP are the issued bf16 products (three per split product:
+    hi.hi + hi.lo + lo.hi); the rate is per SM at the SM clock sampled during
+    the run, compared with the measured dense bf16 peak per SM."""
+    import ctypes
+    from pathlib import Path
+
+    lib_path = kbuild.build_mma_timing()
+    kda._LIB_PATH = Path(lib_path)
+    kda._LIB = None
+    L_ = kda.lib()
+    L_.kda_mma_timing_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    wl = I.PREFILL_32K
+    H, D, act = wl.H, wl.dk, wl.act
+    w_dev = {k: v.to(dev) for k, v in wl.weights().items()}
+    w = kda.make_weights(w_dev["conv_w"], w_dev["norm_w"], wl.eps_l2, wl.eps_rms)
+    pool = kda.StatePool(4, H, D, D, act)
+    toks = {k: v.to(dev) for k, v in wl.tokens(300, L).items()}
+    out = torch.empty(L, H, D, dtype=act, device=dev)
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(pool, [0, L]), dtype=torch.uint8, device=dev)
+    io = kda.make_io(toks, out)
+    kda.kda_prefill_chunked(pool, w, io, [0, L], [0], [0], 64, (), ws)
+    torch.cuda.synchronize()
+    buf = (ctypes.c_ulonglong * 8)()
+    assert L_.kda_mma_timing_read(buf, 1) == 0
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.25)
+    for _ in range(5):
+        kda.kda_prefill_chunked(pool, w, io, [0, L], [0], [0], 64, (), ws)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert L_.kda_mma_timing_read(buf, 1) == 0
+    mhz = float(clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0)
+    max_mhz = float(clk.get("sm_max_mhz") or mhz)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak_fpc = tf_peak * 1e12 / sms / (mhz * 1e6)  # measured peak, FLOP per cycle per SM at this clock
+    nominal_fpc = 2.25e15 / sms / (max_mhz * 1e6)  # nominal dense bf16 (2.25 PFLOP/s) at the maximum clock
+    groups = [("intra [A; P] = [K~; Q~] Kb^T", 0, 4, 3 * 128 * 64 * 128),
+              ("intra W^T and Ut^T", 1, 4, 2 * 3 * 128 * 64 * 64),
+              ("chain (W S | Q S)^T", 2, 5, 3 * 128 * 128 * 128),
+              ("chain (K^T U | P U)^T", 3, 5, 3 * 128 * 192 * 64)]
+    res = {"workload": f"prefill_l{L}_h{H}_d{D}_c64 (timing build)", "sm_mhz": mhz, "peak_tflops": tf_peak,
+           "peak_kind": peak_kind, "groups": {}}
+    for name, slot, cnt_slot, mac in groups:
+        n = max(int(buf[cnt_slot]), 1)
+        cyc = buf[slot] / n
+        fpc = 2 * mac / cyc
+        res["groups"][name] = {"count": int(buf[cnt_slot]), "cycles_issue_to_done": round(cyc, 1),
+                               "issued_flop": 2 * mac, "flop_per_cycle_per_sm": round(fpc, 1),
+                               "frac_of_peak": round(fpc / peak_fpc, 4),
+                               "frac_of_nominal": round(fpc / nominal_fpc, 4)}
+    res["clocks"] = clk
+    return res
+
 
 def oracle_decode_run(o, wl, w, tok, n):
     """The CPU oracle over n chained decode tokens of the batch-1 sequence."""

@@ -124,6 +124,31 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
     return rcp_approx(1.0f + ex2_approx(-x * 1.4426950408889634f));
 }
 
+// Timing build only (compiled with -DKDA_MMA_TIMING into a separate library):
+// per MMA group, the cycles from its first issue to its commit's completion,
+// thread 0 waiting right after the commit.  [0] intra A,P  [1] intra W,Ut
+// [2] chain stage 1  [3] chain stage 2  [4] intra CTAs  [5] chain steps.
+#ifdef KDA_MMA_TIMING
+__device__ unsigned long long g_mma_timing[8];
+#endif
+__device__ __forceinline__ unsigned long long mma_timer_start() {
+#ifdef KDA_MMA_TIMING
+    return clock64();
+#else
+    return 0;
+#endif
+}
+__device__ __forceinline__ void mma_timer_stop(unsigned long long t0, uint64_t *bar, uint32_t parity, uint32_t *err,
+                                               int slot, int count_slot) {
+#ifdef KDA_MMA_TIMING
+    mbar_wait(bar, parity, err);
+    atomicAdd(&g_mma_timing[slot], clock64() - t0);
+    if (count_slot >= 0) atomicAdd(&g_mma_timing[count_slot], 1ull);
+#else
+    (void)t0; (void)bar; (void)parity; (void)err; (void)slot; (void)count_slot;
+#endif
+}
+
 __device__ __forceinline__ char *rec_ptr(const PrefillParams &p, int g, int h) {
     return p.rec + (size_t(g) * p.H + h) * Rec::BYTES;
 }
@@ -575,9 +600,11 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
+            const unsigned long long t0 = mma_timer_start();
             mma3(tm, sbase + is::X_HI, sbase + is::X_LO, sbase + is::KB_HI, sbase + is::KB_LO, 128, CH, D,
                  idesc_bf16_f32(128, CH), false);
             mma_commit(bar_mma);
+            mma_timer_stop(t0, bar_mma, mma_phase, p.err, 0, 4);
         }
     }
     // chain images that need no MMA: exp(G) . q (rows r; above when !exact) and
@@ -735,9 +762,11 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
     tc_fence_after();
     if (tid == 0 && ok) {
         const uint32_t id = idesc_bf16_f32(128, CH);
+        const unsigned long long t0 = mma_timer_start();
         mma3(tm + 64, sbase + is::AK_HI, sbase + is::AK_LO, sbase + is::T_HI, sbase + is::T_LO, D, CH, CH, id, false);
         mma3(tm + 128, sbase + is::AV_HI, sbase + is::AV_LO, sbase + is::T_HI, sbase + is::T_LO, D, CH, CH, id, false);
         mma_commit(bar_mma);
+        mma_timer_stop(t0, bar_mma, mma_phase, p.err, 1, -1);
     }
     ok = __syncthreads_and(ok && mbar_wait(bar_mma, mma_phase, p.err));
     tc_fence_after();
@@ -874,9 +903,11 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         if (!ok) break;
         if (tid == 0) {
             tc_fence_after();
+            const unsigned long long t0 = mma_timer_start();
             mma3(tm + 0, sbase + cs::A1_HI, sbase + cs::A1_LO, sbase + cs::WQ_HI, sbase + cs::WQ_LO, D, 2 * CH, D,
                  id128, false);
             mma_commit(bar_m1);
+            mma_timer_stop(t0, bar_m1, par, p.err, 2, 5);
         }
         // Ut row entries (r = uc0 .. uc0 + 31, column j) while the MMAs run
         float ut[32];
@@ -916,9 +947,11 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
+            const unsigned long long t0 = mma_timer_start();
             mma3(tm + 128, sbase + cs::A2_HI, sbase + cs::A2_LO, sbase + cs::KP_HI, sbase + cs::KP_LO, D, D + CH, CH,
                  id192, false);
             mma_commit(bar_m2);
+            mma_timer_stop(t0, bar_m2, par, p.err, 3, -1);
         }
         ok = __syncthreads_and(mbar_wait(bar_m2, par, p.err));
         if (!ok) break;
@@ -1359,3 +1392,15 @@ kda_status launch_prefill_noalloc(const kda_pool *pool, const kda_weights *w, co
 }
 
 }  // namespace kda
+
+#ifdef KDA_MMA_TIMING
+// Timing build only: copies (and optionally clears) the MMA group counters.
+extern "C" KDA_API int kda_mma_timing_read(unsigned long long *host, int reset) {
+    if (cudaMemcpyFromSymbol(host, kda::g_mma_timing, sizeof(unsigned long long) * 8) != cudaSuccess) return 1;
+    if (reset) {
+        const unsigned long long z[8] = {};
+        if (cudaMemcpyToSymbol(kda::g_mma_timing, z, sizeof(z)) != cudaSuccess) return 1;
+    }
+    return 0;
+}
+#endif
