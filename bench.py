@@ -419,8 +419,19 @@ def prefill_case(kda, dev, iters=3, warmup=1, L=None):
     ms = float(np.mean(times))
     st, flags = kda.kda_poll_device_error(pool)
     assert st == 0, f"device error word {flags:#x}"
+    # tensor-core work issued per (chunk, head): intra [A; P] 128x64x128 and W^T, Ut^T 2 x 128x64x64;
+    # chain 128x128x128 and 128x192x64; each a split product of three bf16 MMAs
+    chunk_heads = ((L + 63) // 64) * H
+    flop = chunk_heads * 2 * 3 * (128 * 64 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 128 + 128 * 192 * 64)
+    _, tf_peak, _, peak_kind = load_peaks()
+    tflops = flop / (ms * 1e-3) / 1e12
     return {"workload": wl.name if L == wl.extra["L"] else f"{wl.name} (first {L} tokens)", "tok_per_s": round(L / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
             "workspace_bytes": ws.numel(),
+            "tensor": {"issued_bf16_tflop_per_call": round(flop / 1e12, 4), "tflops": round(tflops, 1),
+                       "peak": tf_peak, "frac": round(tflops / tf_peak, 4), "peak_kind": peak_kind,
+                       "note": "issued bf16 MMA FLOP of the intra and chain kernels (three per split product) "
+                               "over the whole call; bench.py --only mma_rates gives each MMA group's rate "
+                               "while it runs"},
             "l2": "inputs (3.2 GB) and workspace exceed L2; not flushed between calls"}
 
 
