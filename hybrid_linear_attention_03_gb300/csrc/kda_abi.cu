@@ -212,6 +212,24 @@ static kda_status check_prefill_args(kda_pool *pool, const kda_weights *w, const
     return KDA_OK;
 }
 
+size_t kda_prefill_workspace_bytes_bound(const kda_pool *pool, int32_t N, int32_t max_tokens, int32_t n_reqs,
+                                         int32_t chunk) {
+    if (!pool) return 0;
+    return kda::prefill_workspace_bytes_bound(pool, N, max_tokens, n_reqs, chunk);
+}
+
+kda_status kda_prefill_chunked_dev(kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *cu_seqlens,
+                                   const int32_t *slots, const uint8_t *has_initial_state, int32_t N,
+                                   int32_t max_tokens, int32_t chunk, const kda_ckpt_req *reqs, int32_t n_reqs,
+                                   void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    if (!pool || !valid_weights(w) || !valid_io(io) || N < 0 || n_reqs < 0 || max_tokens < 0 ||
+        (n_reqs > 0 && !reqs) || (N > 0 && (!cu_seqlens || !slots || !has_initial_state)))
+        return KDA_ERR_INVALID_ARG;
+    if (N == 0) return n_reqs == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    return kda::launch_prefill_dev(pool, w, io, cu_seqlens, slots, has_initial_state, N, max_tokens, chunk, reqs,
+                                   n_reqs, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
 kda_status kda_prefill_chunked_noalloc(kda_pool *pool, const kda_weights *w, const kda_io *io,
                                        const int32_t *cu_seqlens, const int32_t *slots,
                                        const uint8_t *has_initial_state, int32_t N, int32_t chunk,
@@ -270,6 +288,36 @@ kda_status kda_state_checkpoint(kda_pool *pool, const int32_t *src_slots, const 
         is_dst[dst_slots[i]] = 1;
     }
     return kda::launch_slot_copy(pool, src_slots, dst_slots, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t kda_state_slot_bytes(const kda_pool *pool) {
+    if (!pool) return 0;
+    return pool->slot_state_elems * sizeof(float) + pool->slot_tail_elems * size_t(pool->act_bytes);
+}
+
+static kda_status slot_transfer(kda_pool *pool, int32_t slot, void *host, size_t bytes, bool to_host,
+                                kda_stream_t stream) {
+    if (!pool || !host || bytes < kda_state_slot_bytes(pool)) return KDA_ERR_INVALID_ARG;
+    if (slot < 0 || slot >= pool->desc.num_slots) return KDA_ERR_SLOT_RANGE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t sb = pool->slot_state_elems * sizeof(float), tb = pool->slot_tail_elems * size_t(pool->act_bytes);
+    char *dst_state = reinterpret_cast<char *>(pool->states) + size_t(slot) * sb;
+    char *dst_tail = static_cast<char *>(pool->tails) + size_t(slot) * tb;
+    char *h = static_cast<char *>(host);
+    const cudaError_t e1 = to_host ? cudaMemcpyAsync(h, dst_state, sb, cudaMemcpyDeviceToHost, s)
+                                   : cudaMemcpyAsync(dst_state, h, sb, cudaMemcpyHostToDevice, s);
+    if (e1 != cudaSuccess) return KDA_ERR_CUDA;
+    const cudaError_t e2 = to_host ? cudaMemcpyAsync(h + sb, dst_tail, tb, cudaMemcpyDeviceToHost, s)
+                                   : cudaMemcpyAsync(dst_tail, h + sb, tb, cudaMemcpyHostToDevice, s);
+    return e2 == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_state_export(kda_pool *pool, int32_t slot, void *host, size_t bytes, kda_stream_t stream) {
+    return slot_transfer(pool, slot, host, bytes, true, stream);
+}
+
+kda_status kda_state_import(kda_pool *pool, int32_t slot, const void *host, size_t bytes, kda_stream_t stream) {
+    return slot_transfer(pool, slot, const_cast<void *>(host), bytes, false, stream);
 }
 
 kda_status kda_poll_device_error(kda_pool *pool, kda_stream_t stream, uint32_t *flags) {

@@ -69,5 +69,10 @@ kda_status launch_prefill_noalloc(const kda_pool *pool, const kda_weights *w, co
                                   const int32_t *cu_seqlens, const int32_t *slots,
                                   const uint8_t *has_initial_state, int N, int chunk, const kda_ckpt_req *reqs,
                                   int n_reqs, cudaStream_t stream);
+size_t prefill_workspace_bytes_bound(const kda_pool *pool, int N, int max_tokens, int n_reqs, int chunk);
+kda_status launch_prefill_dev(const kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *cu_seqlens,
+                              const int32_t *slots, const uint8_t *has_initial_state, int N, int max_tokens,
+                              int chunk, const kda_ckpt_req *reqs, int n_reqs, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 }  // namespace kda

@@ -417,6 +417,7 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
     const float *GGs = reinterpret_cast<const float *>(sm + is::GG);
     const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const ChunkMeta cm = p.chunks[g];
+    if (cm.len <= 0) return;  // a padding entry of a device-built table: no chunk here
     const SeqMeta sq = p.seqs[cm.seq];
     char *rec = rec_ptr(p, g, h);
     const uint32_t sbase = smem_u32(sm);
@@ -838,6 +839,7 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
     const int j = (warp & 3) * 32 + lane, half = warp >> 2;
     const int h = blockIdx.x % p.H, n = blockIdx.x / p.H;
     const SeqMeta sq = p.seqs[n];
+    if (sq.slot < 0) return;  // disabled by the device metadata check: leave every slot alone
     // The chunks of this sequence inside the launch's window [win_lo, win_hi).
     // A sequence with no chunks is settled by the window that starts at 0.
     const int c_lo = max(sq.chunk0, p.win_lo) - sq.chunk0;
@@ -1075,6 +1077,7 @@ __global__ void __launch_bounds__(256) prefill_tails_kernel(const PrefillParams 
         pos = p.seqs[item].len;
         dst = p.seqs[item].slot;
     }
+    if (seq < 0 || dst < 0 || p.seqs[seq].slot < 0) return;  // disabled by the device metadata check
     const SeqMeta sq = p.seqs[seq];
     const Act *old = static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch;
     Act *nt = static_cast<Act *>(p.tails) + size_t(dst) * 3 * p.n_ch;
@@ -1092,12 +1095,161 @@ __global__ void __launch_bounds__(256) prefill_tails_kernel(const PrefillParams 
     }
 }
 
+// ============================================================ metadata ===
+// Builds the sequence, chunk and checkpoint tables on the device from device
+// arrays (one CTA), with the host builder's rules: cu_seqlens from 0 and
+// non-decreasing within max_tokens; sequence slots and request slots in range
+// and all distinct; a request's position in (0, len] and a multiple of the
+// chunk or the sequence end.  Chunks beyond the real count (the grid is sized
+// from bounds) get len 0.  On any violation the error word gets
+// KDA_DEVERR_SLOT_RANGE / KDA_DEVERR_META and every table entry disables its
+// item (slot -1, no chunks, no requests), so the call changes nothing.
+struct MetaArgs {
+    const int32_t *cu;
+    const int32_t *slots;
+    const uint8_t *has_init;
+    const kda_ckpt_req *reqs;
+    int32_t N, n_reqs, max_tokens, max_chunks, num_slots;
+    SeqMeta *seqs;
+    ChunkMeta *chunks;
+    CkptMeta *ckpts;
+    uint32_t *used;  // ceil(num_slots / 32) words of scratch
+    uint32_t *err;
+};
+constexpr int kMetaThreads = 1024;
+
+__device__ __forceinline__ bool mark_slot(uint32_t *used, int slot) {  // true if already marked
+    const uint32_t bit = 1u << (slot & 31);
+    return (atomicOr(used + (slot >> 5), bit) & bit) != 0;
+}
+
+// (seq, pos) of sorted request r is after (s, t)
+__device__ __forceinline__ bool req_after(const CkptMeta &c, int s, int t) {
+    return c.seq > s || (c.seq == s && c.token_pos > t);
+}
+
+__global__ void __launch_bounds__(kMetaThreads) prefill_meta_kernel(const MetaArgs a) {
+    __shared__ int bad_meta, bad_slot, carry;
+    __shared__ int scan[kMetaThreads];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        bad_meta = 0;
+        bad_slot = 0;
+        carry = 0;
+    }
+    for (int i = tid; i < (a.num_slots + 31) / 32; i += kMetaThreads) a.used[i] = 0u;
+    __syncthreads();
+    for (int s = tid; s < a.N; s += kMetaThreads) {
+        const int lo = a.cu[s], hi = a.cu[s + 1], sl = a.slots[s];
+        if ((s == 0 && lo != 0) || hi < lo || hi > a.max_tokens) bad_meta = 1;
+        if (sl < 0 || sl >= a.num_slots) bad_slot = 1;
+        else if (mark_slot(a.used, sl)) bad_meta = 1;
+    }
+    __syncthreads();  // sequence slots are marked before request slots are checked against them
+    for (int r = tid; r < a.n_reqs; r += kMetaThreads) {
+        const kda_ckpt_req q = a.reqs[r];
+        if (q.seq < 0 || q.seq >= a.N) {
+            bad_meta = 1;
+            continue;
+        }
+        const int len = a.cu[q.seq + 1] - a.cu[q.seq];
+        if (q.token_pos <= 0 || q.token_pos > len || (q.token_pos != len && q.token_pos % CH != 0)) bad_meta = 1;
+        if (q.dst_slot < 0 || q.dst_slot >= a.num_slots) bad_slot = 1;
+        else if (mark_slot(a.used, q.dst_slot)) bad_meta = 1;
+    }
+    __syncthreads();
+    const bool ok = !bad_meta && !bad_slot;
+    if (tid == 0 && !ok) atomicOr(a.err, (bad_slot ? KDA_DEVERR_SLOT_RANGE : 0u) | (bad_meta ? KDA_DEVERR_META : 0u));
+    // sequences: chunk counts, exclusive prefix -> first chunk
+    for (int base = 0; base < a.N; base += kMetaThreads) {
+        const int s = base + tid;
+        const int len = (ok && s < a.N) ? a.cu[s + 1] - a.cu[s] : 0;
+        const int nch = (len + CH - 1) / CH;
+        scan[tid] = nch;
+        __syncthreads();
+        for (int off = 1; off < kMetaThreads; off <<= 1) {
+            const int v = tid >= off ? scan[tid - off] : 0;
+            __syncthreads();
+            scan[tid] += v;
+            __syncthreads();
+        }
+        if (s < a.N) {
+            SeqMeta m = {0, 0, -1, 0, 0, 0};
+            if (ok) m = {a.cu[s], len, a.slots[s], a.has_init[s] ? 1 : 0, carry + scan[tid] - nch, nch};
+            a.seqs[s] = m;
+        }
+        __syncthreads();
+        if (tid == kMetaThreads - 1) carry += scan[tid];
+        __syncthreads();
+    }
+    const int total_chunks = carry;
+    // requests sorted by (sequence, position): rank of each among all
+    for (int r = tid; r < a.n_reqs; r += kMetaThreads) {
+        const kda_ckpt_req q = a.reqs[r];
+        int rank = 0;
+        for (int k = 0; k < a.n_reqs; ++k) {
+            const kda_ckpt_req o = a.reqs[k];
+            rank += (o.seq < q.seq || (o.seq == q.seq && (o.token_pos < q.token_pos || (o.token_pos == q.token_pos && k < r))))
+                        ? 1 : 0;
+        }
+        CkptMeta c = {-1, 0, -1, 0};
+        if (ok) c = {q.seq, q.token_pos, q.dst_slot, 0};
+        a.ckpts[rank] = c;
+    }
+    __syncthreads();  // the tables above are read back below
+    // chunks: owning sequence (the last one starting at or before g), rows, and its requests
+    for (int g = tid; g < a.max_chunks; g += kMetaThreads) {
+        ChunkMeta cm = {-1, 0, 0, 0, 0, 0};
+        if (ok && g < total_chunks) {
+            int lo = 0, hi = a.N - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (a.seqs[mid].chunk0 <= g) lo = mid;
+                else hi = mid - 1;
+            }
+            const SeqMeta sq = a.seqs[lo];
+            const int pos0 = (g - sq.chunk0) * CH, clen = min(CH, sq.len - pos0);
+            // requests of this sequence at positions (pos0, pos0 + clen]: all at pos0 + clen
+            int b = 0, e = a.n_reqs;
+            while (b < e) {
+                const int mid = (b + e) >> 1;
+                if (req_after(a.ckpts[mid], lo, pos0)) e = mid;
+                else b = mid + 1;
+            }
+            int f = b, e2 = a.n_reqs;
+            while (f < e2) {
+                const int mid = (f + e2) >> 1;
+                if (req_after(a.ckpts[mid], lo, pos0 + clen)) e2 = mid;
+                else f = mid + 1;
+            }
+            cm = {lo, sq.row0 + pos0, clen, pos0, b, f - b};
+        }
+        a.chunks[g] = cm;
+    }
+}
+
 // ================================================================ host ===
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
     size_t seqs, chunks, ckpts, rec, total;
 };
+
+WsLayout ws_layout(int N, long long n_chunks, long long n_reqs, int H);
+
+// The device-built tables' workspace: ws_layout plus the slot bitmap the
+// builder uses to find repeated slots (at the end).
+struct WsLayoutDev {
+    WsLayout L;
+    size_t used, total;
+};
+WsLayoutDev ws_layout_dev(int N, long long max_chunks, long long n_reqs, int H, int num_slots) {
+    WsLayoutDev d;
+    d.L = ws_layout(N, max_chunks, n_reqs, H);
+    d.used = align256(d.L.total);
+    d.total = d.used + sizeof(uint32_t) * size_t((num_slots + 31) / 32);
+    return d;
+}
 
 WsLayout ws_layout(int N, long long n_chunks, long long n_reqs, int H) {
     WsLayout L;
@@ -1275,6 +1427,42 @@ size_t prefill_workspace_bytes(const kda_pool *pool, const int32_t *cu_seqlens, 
     return ws_layout(N, nc, 2 * (nc + N), pool->desc.num_heads).total;
 }
 
+// Launch parameters over the workspace's tables (written, or enqueued to be
+// written, on the stream) and the kernels.  n_chunks sizes the grids; n_tok
+// is the token extent of the activation arrays the tensor maps describe.
+kda_status launch_tables(const kda_pool *pool, const kda_weights *w, const kda_io *io, char *ws, const WsLayout &L,
+                         int N, int n_reqs, long long n_chunks, int n_tok, cudaStream_t stream) {
+    PrefillParams p{};
+    p.chunk_base = 0;
+    p.win_lo = 0;
+    p.win_hi = int(n_chunks);
+    p.seqs = reinterpret_cast<const SeqMeta *>(ws + L.seqs);
+    p.chunks = reinterpret_cast<const ChunkMeta *>(ws + L.chunks);
+    p.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.ckpts);
+    p.rec = ws + L.rec;
+    p.states = pool->states;
+    p.tails = pool->tails;
+    p.err = pool->err;
+    p.q = io->q;
+    p.k = io->k;
+    p.v = io->v;
+    p.alpha = io->alpha;
+    p.beta = io->beta;
+    p.gate = io->gate;
+    p.out = io->out;
+    p.conv_w = w->conv_w;
+    p.norm_w = w->norm_w;
+    p.H = pool->desc.num_heads;
+    p.n_ch = pool->n_ch;
+    p.n_seqs = N;
+    p.n_chunks = int(n_chunks);
+    p.n_ckpts = n_reqs;
+    p.eps_l2 = w->eps_l2;
+    p.eps_rms = w->eps_rms;
+    if (pool->desc.act == KDA_BF16) return launch_act<__nv_bfloat16>(p, io, n_tok, N, n_chunks, n_reqs, stream);
+    return launch_act<float>(p, io, n_tok, N, n_chunks, n_reqs, stream);
+}
+
 kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *cu_seqlens,
                           const int32_t *slots, const uint8_t *has_initial_state, int N, int chunk,
                           const kda_ckpt_req *reqs, int n_reqs, void *workspace, size_t workspace_bytes,
@@ -1322,36 +1510,45 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
     if (!cks.empty() && cudaMemcpyAsync(ws + L.ckpts, cks.data(), sizeof(CkptMeta) * cks.size(),
                                         cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
-    PrefillParams p;
-    p.chunk_base = 0;
-    p.win_lo = 0;
-    p.win_hi = int(n_chunks);
-    p.seqs = reinterpret_cast<const SeqMeta *>(ws + L.seqs);
-    p.chunks = reinterpret_cast<const ChunkMeta *>(ws + L.chunks);
-    p.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.ckpts);
-    p.rec = ws + L.rec;
-    p.states = pool->states;
-    p.tails = pool->tails;
-    p.err = pool->err;
-    p.q = io->q;
-    p.k = io->k;
-    p.v = io->v;
-    p.alpha = io->alpha;
-    p.beta = io->beta;
-    p.gate = io->gate;
-    p.out = io->out;
-    p.conv_w = w->conv_w;
-    p.norm_w = w->norm_w;
-    p.H = H;
-    p.n_ch = pool->n_ch;
-    p.n_seqs = N;
-    p.n_chunks = int(n_chunks);
-    p.n_ckpts = n_reqs;
-    p.eps_l2 = w->eps_l2;
-    p.eps_rms = w->eps_rms;
-    const int n_tok = cu_seqlens[N];
-    if (pool->desc.act == KDA_BF16) return launch_act<__nv_bfloat16>(p, io, n_tok, N, n_chunks, n_reqs, stream);
-    return launch_act<float>(p, io, n_tok, N, n_chunks, n_reqs, stream);
+    return launch_tables(pool, w, io, ws, L, N, n_reqs, n_chunks, cu_seqlens[N], stream);
+}
+
+size_t prefill_workspace_bytes_bound(const kda_pool *pool, int N, int max_tokens, int n_reqs, int chunk) {
+    if (chunk != CH || pool->desc.d_k != D || pool->desc.d_v != D || N < 0 || max_tokens < 0 || n_reqs < 0) return 0;
+    const long long mc = max_tokens / CH + N;
+    return ws_layout_dev(N, mc, n_reqs, pool->desc.num_heads, pool->desc.num_slots).total;
+}
+
+kda_status launch_prefill_dev(const kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *cu_seqlens,
+                              const int32_t *slots, const uint8_t *has_initial_state, int N, int max_tokens,
+                              int chunk, const kda_ckpt_req *reqs, int n_reqs, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+    if (pool->desc.d_k != D || pool->desc.d_v != D || chunk != CH) return KDA_ERR_UNSUPPORTED;
+    const int H = pool->desc.num_heads;
+    // every sequence adds at most one partial chunk to max_tokens / CH whole ones
+    const long long max_chunks = max_tokens / CH + N;
+    if (max_chunks > (1LL << 31) / std::max(H, 1)) return KDA_ERR_INVALID_ARG;
+    const WsLayoutDev LD = ws_layout_dev(N, max_chunks, n_reqs, H, pool->desc.num_slots);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 256) != 0 || workspace_bytes < LD.total)
+        return KDA_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    MetaArgs a;
+    a.cu = cu_seqlens;
+    a.slots = slots;
+    a.has_init = has_initial_state;
+    a.reqs = reqs;
+    a.N = N;
+    a.n_reqs = n_reqs;
+    a.max_tokens = max_tokens;
+    a.max_chunks = int(max_chunks);
+    a.num_slots = pool->desc.num_slots;
+    a.seqs = reinterpret_cast<SeqMeta *>(ws + LD.L.seqs);
+    a.chunks = reinterpret_cast<ChunkMeta *>(ws + LD.L.chunks);
+    a.ckpts = reinterpret_cast<CkptMeta *>(ws + LD.L.ckpts);
+    a.used = reinterpret_cast<uint32_t *>(ws + LD.used);
+    a.err = pool->err;
+    prefill_meta_kernel<<<1, kMetaThreads, 0, stream>>>(a);
+    return launch_tables(pool, w, io, ws, LD.L, N, n_reqs, max_chunks, max_tokens, stream);
 }
 
 // ------------------------------------------------------ no-allocation entry --

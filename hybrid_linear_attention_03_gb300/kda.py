@@ -34,7 +34,9 @@ KDA_DEVERR_TIMEOUT = 0x4
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_state_pool_bytes", "kda_state_pool_create", "kda_state_pool_destroy", "kda_state_pool_layout",
            "kda_check_slots", "kda_decode", "kda_verify", "kda_prefill_workspace_bytes", "kda_prefill_chunked",
-           "kda_state_checkpoint", "kda_poll_device_error", "kda_status_string", "kda_prefill_chunked_noalloc")
+           "kda_state_checkpoint", "kda_poll_device_error", "kda_status_string", "kda_prefill_chunked_noalloc",
+           "kda_state_slot_bytes", "kda_state_export", "kda_state_import", "kda_prefill_workspace_bytes_bound",
+           "kda_prefill_chunked_dev")
 
 KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -107,6 +109,17 @@ def lib() -> ctypes.CDLL:
         L.kda_prefill_chunked_noalloc.restype = i32
         L.kda_state_checkpoint.argtypes = [vp, vp, vp, i32, vp]
         L.kda_state_checkpoint.restype = i32
+        L.kda_prefill_workspace_bytes_bound.argtypes = [vp, i32, i32, i32, i32]
+        L.kda_prefill_workspace_bytes_bound.restype = sz
+        L.kda_prefill_chunked_dev.argtypes = [vp, P(kda_weights), P(kda_io), vp, vp, vp, i32, i32, i32, vp, i32,
+                                              vp, sz, vp]
+        L.kda_prefill_chunked_dev.restype = i32
+        L.kda_state_slot_bytes.argtypes = [vp]
+        L.kda_state_slot_bytes.restype = sz
+        L.kda_state_export.argtypes = [vp, i32, vp, sz, vp]
+        L.kda_state_export.restype = i32
+        L.kda_state_import.argtypes = [vp, i32, vp, sz, vp]
+        L.kda_state_import.restype = i32
         L.kda_poll_device_error.argtypes = [vp, vp, P(ctypes.c_uint32)]
         L.kda_poll_device_error.restype = i32
         L.kda_status_string.argtypes = [i32]
@@ -177,12 +190,20 @@ def kda_state_pool_layout(handle) -> kda_pool_layout:
 
 
 def make_weights(conv_w: torch.Tensor, norm_w: torch.Tensor, eps_l2=1e-6, eps_rms=1e-5) -> kda_weights:
-    return kda_weights(conv_w.data_ptr(), norm_w.data_ptr(), float(eps_l2), float(eps_rms))
+    """The struct holds raw device pointers; it also keeps the two tensors
+    alive, so their memory cannot be handed to another tensor while the
+    struct is in use."""
+    w = kda_weights(conv_w.data_ptr(), norm_w.data_ptr(), float(eps_l2), float(eps_rms))
+    w._tensors = (conv_w, norm_w)
+    return w
 
 
 def make_io(inp: dict, out: torch.Tensor) -> kda_io:
-    return kda_io(inp["q"].data_ptr(), inp["k"].data_ptr(), inp["v"].data_ptr(), inp["alpha"].data_ptr(),
-                  inp["beta"].data_ptr(), inp["gate"].data_ptr(), out.data_ptr())
+    """Raw pointers to the step's arrays; the struct keeps the tensors alive."""
+    io = kda_io(inp["q"].data_ptr(), inp["k"].data_ptr(), inp["v"].data_ptr(), inp["alpha"].data_ptr(),
+                inp["beta"].data_ptr(), inp["gate"].data_ptr(), out.data_ptr())
+    io._tensors = (inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"], inp["gate"], out)
+    return io
 
 
 class StatePool:
@@ -268,6 +289,34 @@ def kda_prefill_chunked(pool: StatePool, weights: kda_weights, io: kda_io, cu_se
            "kda_prefill_chunked")
 
 
+def kda_prefill_workspace_bytes_bound(pool: StatePool, n_seqs: int, max_tokens: int, n_reqs: int,
+                                      chunk: int = 64) -> int:
+    return int(lib().kda_prefill_workspace_bytes_bound(pool.handle, int(n_seqs), int(max_tokens), int(n_reqs),
+                                                       int(chunk)))
+
+
+def kda_prefill_chunked_dev(pool: StatePool, weights: kda_weights, io: kda_io, cu_seqlens: torch.Tensor,
+                            slots: torch.Tensor, has_initial_state: torch.Tensor, max_tokens: int,
+                            reqs: torch.Tensor | None, workspace: torch.Tensor, chunk: int = 64, stream=None) -> None:
+    """kda_prefill_chunked with the metadata in device memory: cu_seqlens and
+    slots int32, has_initial_state uint8, reqs int32 [n, 3] (seq, token_pos,
+    dst_slot) or None, all CUDA tensors; the tables are built on the GPU."""
+    for name, t, dt in (("cu_seqlens", cu_seqlens, torch.int32), ("slots", slots, torch.int32),
+                        ("has_initial_state", has_initial_state, torch.uint8)):
+        if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    n_req = 0 if reqs is None else int(reqs.shape[0])
+    if reqs is not None and (not reqs.is_cuda or reqs.dtype != torch.int32 or tuple(reqs.shape[1:]) != (3,)
+                             or not reqs.is_contiguous()):
+        raise ValueError("reqs must be a contiguous CUDA int32 tensor of shape [n, 3]")
+    _check(lib().kda_prefill_chunked_dev(pool.handle, ctypes.byref(weights), ctypes.byref(io), cu_seqlens.data_ptr(),
+                                         slots.data_ptr(), has_initial_state.data_ptr(), int(cu_seqlens.numel() - 1),
+                                         int(max_tokens), int(chunk), None if n_req == 0 else reqs.data_ptr(),
+                                         n_req, _dptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)),
+           "kda_prefill_chunked_dev")
+
+
 def kda_prefill_chunked_noalloc(pool: StatePool, weights: kda_weights, io: kda_io, cu_seqlens, slots,
                                 has_initial_state, chunk: int = 64, reqs=(), stream=None) -> None:
     """kda_prefill_chunked for callers that cannot allocate device memory: the
@@ -290,6 +339,27 @@ def kda_state_checkpoint(pool: StatePool, src_slots, dst_slots, stream=None) -> 
         raise ValueError("src and dst slot lists differ in length")
     _check(lib().kda_state_checkpoint(pool.handle, ps, pd, int(ts.numel()), _stream(stream)),
            "kda_state_checkpoint")
+
+
+def kda_state_slot_bytes(pool: StatePool) -> int:
+    return int(lib().kda_state_slot_bytes(pool.handle))
+
+
+def kda_state_export(pool: StatePool, slot: int, host: torch.Tensor, stream=None) -> None:
+    """Copies slot `slot` (state, then conv tail) into the CPU uint8 tensor
+    `host` (pin it for an asynchronous copy); bit-exact."""
+    if host.device.type != "cpu" or not host.is_contiguous():
+        raise ValueError("host must be a contiguous CPU tensor")
+    _check(lib().kda_state_export(pool.handle, int(slot), host.data_ptr(), host.numel() * host.element_size(),
+                                  _stream(stream)), "kda_state_export")
+
+
+def kda_state_import(pool: StatePool, slot: int, host: torch.Tensor, stream=None) -> None:
+    """Copies a buffer written by kda_state_export into slot `slot`; bit-exact."""
+    if host.device.type != "cpu" or not host.is_contiguous():
+        raise ValueError("host must be a contiguous CPU tensor")
+    _check(lib().kda_state_import(pool.handle, int(slot), host.data_ptr(), host.numel() * host.element_size(),
+                                  _stream(stream)), "kda_state_import")
 
 
 def kda_poll_device_error(pool: StatePool, stream=None) -> tuple[int, int]:

@@ -241,12 +241,60 @@ KDA_API kda_status kda_prefill_chunked_noalloc(kda_pool *pool, const kda_weights
                                                const uint8_t *has_initial_state, int32_t N, int32_t chunk,
                                                const kda_ckpt_req *reqs, int32_t n_reqs, kda_stream_t stream);
 
+/* kda_prefill_chunked with its metadata in DEVICE memory, for callers whose
+ * sequence tables live on the GPU and for CUDA graph capture: the call
+ * enqueues no host-to-device copy.  The sequence, chunk and checkpoint tables
+ * are built on the stream by one kernel, with the rules kda_prefill_chunked
+ * checks on the host.  Source: "vLLM Kimi K3 지원", section "Fused Kernels 및
+ * 메타데이터 최적화", Metadata Builder bullet (the KDA metadata prepared by
+ * one fused GPU kernel).
+ * cu_seqlens: device int32 [N + 1]; slots: device int32 [N];
+ * has_initial_state: device uint8 [N]; reqs: device kda_ckpt_req [n_reqs].
+ * N, n_reqs: host counts.  max_tokens: host bound on cu_seqlens[N]; q, k, v,
+ *   alpha, beta, gate and out must have max_tokens rows (rows past
+ *   cu_seqlens[N] may be read, are never written and never affect results).
+ * workspace: device, 256-aligned, >= kda_prefill_workspace_bytes_bound(pool,
+ *   N, max_tokens, n_reqs, chunk) bytes (sized from the bounds, so the host
+ *   needs no sequence lengths).
+ * Host errors: those of kda_prefill_chunked that need no device data
+ *   (KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE).
+ * Device errors: cu_seqlens not starting at 0, decreasing or past max_tokens,
+ *   a request at a bad sequence or position, or a repeated slot set
+ *   KDA_DEVERR_META; a slot out of range sets KDA_DEVERR_SLOT_RANGE.  Either
+ *   way the call then changes no slot and writes no output (read the error
+ *   word with kda_poll_device_error). */
+KDA_API size_t kda_prefill_workspace_bytes_bound(const kda_pool *pool, int32_t N, int32_t max_tokens, int32_t n_reqs,
+                                                 int32_t chunk);
+KDA_API kda_status kda_prefill_chunked_dev(kda_pool *pool, const kda_weights *w, const kda_io *io,
+                                           const int32_t *cu_seqlens, const int32_t *slots,
+                                           const uint8_t *has_initial_state, int32_t N, int32_t max_tokens,
+                                           int32_t chunk, const kda_ckpt_req *reqs, int32_t n_reqs, void *workspace,
+                                           size_t workspace_bytes, kda_stream_t stream);
+
 /* Copies state and conv tail of src_slots[i] into dst_slots[i], bit-exact,
  * for i < n (HOST arrays).  Restoring a checkpoint is the same call with the
  * roles swapped.  dst slots must be distinct and must not appear among the
  * sources.  Source: "vLLM Kimi K3 지원", section "에이전틱 캐시 유지 정책". */
 KDA_API kda_status kda_state_checkpoint(kda_pool *pool, const int32_t *src_slots,
                                 const int32_t *dst_slots, int32_t n, kda_stream_t stream);
+
+/* Request-level state transfer between a slot and host memory: the state
+ * (fp32 [H][d_v][d_k], S^T per head) followed by the conv tail (act
+ * [3][n_ch]), kda_state_slot_bytes() bytes in all, copied bit-exactly.  It is
+ * the single-GPU side of moving a request's KDA state between prefill and
+ * decode replicas.  Source: "vLLM Kimi K3 지원", section "Prefill/Decode 분리
+ * (Disaggregation)" (request-level KDA state transfer).
+ * host: HOST buffer of at least kda_state_slot_bytes(pool) bytes, owned by
+ *       the caller; page-locked memory makes the copies asynchronous, other
+ *       host memory makes them return once the data is staged.  The buffer
+ *       must stay valid (and, for import, unchanged) until the stream has
+ *       executed the copies.
+ * Errors: KDA_ERR_INVALID_ARG (null pool / host, bytes too small),
+ *         KDA_ERR_SLOT_RANGE (slot outside the pool), KDA_ERR_CUDA. */
+KDA_API size_t kda_state_slot_bytes(const kda_pool *pool);
+KDA_API kda_status kda_state_export(kda_pool *pool, int32_t slot, void *host, size_t bytes, kda_stream_t stream);
+KDA_API kda_status kda_state_import(kda_pool *pool, int32_t slot, const void *host, size_t bytes,
+                                    kda_stream_t stream);
 
 /* Waits for `stream`, reads the device error word into *flags (may be NULL)
  * and clears it.  Returns KDA_ERR_DEVICE if any bit was set, else KDA_OK. */

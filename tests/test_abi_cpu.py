@@ -64,3 +64,12 @@ def test_create_rejects_null_buffer(lib):
     h = ctypes.c_void_p()
     st = lib.kda_state_pool_create(ctypes.byref(desc), None, 1 << 20, ctypes.byref(h))
     assert st == kda.KDA_ERR_INVALID_ARG and not h.value
+
+
+def test_state_transfer_rejects_null_arguments(lib):
+    """Host checks of the state export / import entry points (no device call)."""
+    import ctypes
+    buf = (ctypes.c_uint8 * 16)()
+    assert lib.kda_state_slot_bytes(None) == 0
+    assert lib.kda_state_export(None, 0, ctypes.addressof(buf), 16, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_state_import(None, 0, ctypes.addressof(buf), 16, None) == kda.KDA_ERR_INVALID_ARG

@@ -171,6 +171,43 @@ def test_checkpoint_copy_is_bitexact():
         assert torch.equal(pool.states()[s], before[0][s])
 
 
+def test_state_export_import_round_trip_continues_the_request():
+    """A warmed slot exported to host memory and imported into another slot
+    (the request moving between replicas) is bit-exact, and decoding from
+    the imported copy gives the same outputs as decoding from the original."""
+    H, D, act = 2, 32, torch.bfloat16
+    m = Mirror(8, H, D, act, _weights(11, H, D, act))
+    warm = hp.to_device(_tokens(11, 0, 6, H, D, act))
+    out = torch.empty(1, H, D, dtype=act, device="cuda")
+    for t in range(6):
+        kda.kda_decode(m.gpu, m.w, kda.make_io({k: v[t:t + 1] for k, v in warm.items()}, out),
+                       torch.tensor([2], dtype=torch.int32, device="cuda"), 1)
+    nb = kda.kda_state_slot_bytes(m.gpu)
+    assert nb == H * D * D * 4 + 3 * m.gpu.n_ch * 2
+    host = torch.empty(nb, dtype=torch.uint8).pin_memory()
+    kda.kda_state_export(m.gpu, 2, host)
+    torch.cuda.synchronize()
+    kda.kda_state_import(m.gpu, 5, host)
+    torch.cuda.synchronize()
+    assert torch.equal(m.gpu.states()[5], m.gpu.states()[2]) and torch.equal(m.gpu.tails()[5], m.gpu.tails()[2])
+    nxt = hp.to_device(_tokens(11, 1, 3, H, D, act))
+    for t in range(3):
+        tok = {k: v[t:t + 1] for k, v in nxt.items()}
+        oa = torch.empty(1, H, D, dtype=act, device="cuda")
+        ob = torch.empty(1, H, D, dtype=act, device="cuda")
+        kda.kda_decode(m.gpu, m.w, kda.make_io(tok, oa), torch.tensor([2], dtype=torch.int32, device="cuda"), 1)
+        kda.kda_decode(m.gpu, m.w, kda.make_io(tok, ob), torch.tensor([5], dtype=torch.int32, device="cuda"), 1)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+    assert torch.equal(m.gpu.states()[5], m.gpu.states()[2])
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_state_export(m.gpu, 8, host)
+    assert e.value.status == kda.KDA_ERR_SLOT_RANGE
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_state_import(m.gpu, 1, host[: nb - 1])
+    assert e.value.status == kda.KDA_ERR_INVALID_ARG
+
+
 def test_out_of_range_device_slot_sets_error_and_skips():
     H, D, act = 2, 16, torch.float32
     m = Mirror(4, H, D, act, _weights(2, H, D, act))
