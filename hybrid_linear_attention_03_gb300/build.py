@@ -1,4 +1,4 @@
-"""Builds libkda.so (all CUDA sources under csrc/) for sm_103a with nvcc.
+"""Builds libkda.so (all CUDA and host C++ sources under csrc/) for sm_103a with nvcc.
 
 Each translation unit compiles in parallel with
 ``-gencode arch=compute_103a,code=sm_103a``; the objects link into
@@ -35,7 +35,8 @@ def nvcc() -> str:
 
 
 def sources() -> list[Path]:
-    return sorted(CSRC.glob("*.cu"))
+    """CUDA translation units and host-only C++ ones (compiled by nvcc too)."""
+    return sorted([*CSRC.glob("*.cu"), *CSRC.glob("*.cpp")])
 
 
 def _stale(obj: Path, src: Path) -> bool:

@@ -341,6 +341,7 @@ const char *kda_status_string(kda_status s) {
         case KDA_ERR_CUDA: return "CUDA runtime error";
         case KDA_ERR_DEVICE: return "device error word set";
         case KDA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case KDA_ERR_HOST_MEMORY: return "host allocation failed";
     }
     return "unknown status";
 }

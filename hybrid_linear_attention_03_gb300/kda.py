@@ -25,6 +25,7 @@ KDA_ERR_UNSUPPORTED = 4
 KDA_ERR_CUDA = 5
 KDA_ERR_DEVICE = 6
 KDA_ERR_WORKSPACE = 7
+KDA_ERR_HOST_MEMORY = 8
 KDA_F32 = 0
 KDA_BF16 = 1
 KDA_DEVERR_SLOT_RANGE = 0x1
@@ -36,7 +37,8 @@ EXPORTS = ("kda_state_pool_bytes", "kda_state_pool_create", "kda_state_pool_dest
            "kda_check_slots", "kda_decode", "kda_verify", "kda_prefill_workspace_bytes", "kda_prefill_chunked",
            "kda_state_checkpoint", "kda_poll_device_error", "kda_status_string", "kda_prefill_chunked_noalloc",
            "kda_state_slot_bytes", "kda_state_export", "kda_state_import", "kda_prefill_workspace_bytes_bound",
-           "kda_prefill_chunked_dev")
+           "kda_prefill_chunked_dev", "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_plan",
+           "kda_prefix_cache_forget", "kda_prefix_cache_get_stats", "kda_prefix_cache_saved")
 
 KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -64,6 +66,16 @@ class kda_io(ctypes.Structure):
 
 class kda_ckpt_req(ctypes.Structure):
     _fields_ = [("seq", ctypes.c_int32), ("token_pos", ctypes.c_int32), ("dst_slot", ctypes.c_int32)]
+
+
+class kda_prefix_plan(ctypes.Structure):
+    _fields_ = [("hit_len", ctypes.c_int32), ("hit_slot", ctypes.c_int32), ("admit_pos", ctypes.c_int32),
+                ("admit_slot", ctypes.c_int32)]
+
+
+class kda_prefix_cache_stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("plans", "hits", "admissions", "evictions", "n_saved", "n_unsaved",
+                                               "n_free")]
 
 
 class KdaError(RuntimeError):
@@ -122,6 +134,18 @@ def lib() -> ctypes.CDLL:
         L.kda_state_import.restype = i32
         L.kda_poll_device_error.argtypes = [vp, vp, P(ctypes.c_uint32)]
         L.kda_poll_device_error.restype = i32
+        L.kda_prefix_cache_create.argtypes = [i32, vp, i32, i32, P(vp)]
+        L.kda_prefix_cache_create.restype = i32
+        L.kda_prefix_cache_destroy.argtypes = [vp]
+        L.kda_prefix_cache_destroy.restype = None
+        L.kda_prefix_cache_plan.argtypes = [vp, vp, i32, P(kda_prefix_plan)]
+        L.kda_prefix_cache_plan.restype = i32
+        L.kda_prefix_cache_forget.argtypes = [vp, i32]
+        L.kda_prefix_cache_forget.restype = i32
+        L.kda_prefix_cache_get_stats.argtypes = [vp, P(kda_prefix_cache_stats)]
+        L.kda_prefix_cache_get_stats.restype = i32
+        L.kda_prefix_cache_saved.argtypes = [vp, vp, vp, i32]
+        L.kda_prefix_cache_saved.restype = i32
         L.kda_status_string.argtypes = [i32]
         L.kda_status_string.restype = ctypes.c_char_p
         _LIB = L
@@ -314,7 +338,8 @@ def kda_prefill_chunked_dev(pool: StatePool, weights: kda_weights, io: kda_io, c
                                          int(max_tokens), int(chunk), None if n_req == 0 else reqs.data_ptr(),
                                          n_req, _dptr(workspace), workspace.numel() * workspace.element_size(),
                                          _stream(stream)),
-           "kda_prefill_chunked_dev")
+           "kda_prefill_chunked_dev", "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_plan",
+           "kda_prefix_cache_forget", "kda_prefix_cache_get_stats", "kda_prefix_cache_saved")
 
 
 def kda_prefill_chunked_noalloc(pool: StatePool, weights: kda_weights, io: kda_io, cu_seqlens, slots,
@@ -367,3 +392,45 @@ def kda_poll_device_error(pool: StatePool, stream=None) -> tuple[int, int]:
     flags = ctypes.c_uint32(0)
     st = int(lib().kda_poll_device_error(pool.handle, _stream(stream), ctypes.byref(flags)))
     return st, int(flags.value)
+
+
+class PrefixCache:
+    """Prefix-state cache with second-hit admission (host only): see
+    kda_prefix_cache_plan in include/kda.h."""
+
+    def __init__(self, block: int, slots, max_tracked: int):
+        ts, ps = _host_i32(slots)
+        h = ctypes.c_void_p()
+        _check(lib().kda_prefix_cache_create(int(block), ps, int(ts.numel()), int(max_tracked), ctypes.byref(h)),
+               "kda_prefix_cache_create")
+        self.handle = h
+        self.block = int(block)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value and _LIB is not None:
+            _LIB.kda_prefix_cache_destroy(h)
+            self.handle = None
+
+    def plan(self, tokens) -> tuple[int, int, int, int]:
+        """(hit_len, hit_slot, admit_pos, admit_slot) for a prompt of token ids."""
+        t, pt = _host_i32(tokens)
+        out = kda_prefix_plan()
+        _check(lib().kda_prefix_cache_plan(self.handle, pt, int(t.numel()), ctypes.byref(out)), "kda_prefix_cache_plan")
+        return out.hit_len, out.hit_slot, out.admit_pos, out.admit_slot
+
+    def forget(self, slot: int) -> None:
+        _check(lib().kda_prefix_cache_forget(self.handle, int(slot)), "kda_prefix_cache_forget")
+
+    def stats(self) -> dict:
+        st = kda_prefix_cache_stats()
+        _check(lib().kda_prefix_cache_get_stats(self.handle, ctypes.byref(st)), "kda_prefix_cache_get_stats")
+        return {n: getattr(st, n) for n, _ in kda_prefix_cache_stats._fields_}
+
+    def saved(self) -> dict:
+        """{slot: prefix length} of the saved prefixes."""
+        n = lib().kda_prefix_cache_saved(self.handle, None, None, 0)
+        lens = (ctypes.c_int32 * max(n, 1))()
+        slots = (ctypes.c_int32 * max(n, 1))()
+        m = lib().kda_prefix_cache_saved(self.handle, lens, slots, n)
+        return {int(slots[i]): int(lens[i]) for i in range(m)}

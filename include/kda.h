@@ -69,7 +69,8 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 4, /* a legal shape this build has no kernel for */
     KDA_ERR_CUDA = 5,        /* a CUDA runtime call failed */
     KDA_ERR_DEVICE = 6,      /* the device error word was set (kda_poll_device_error) */
-    KDA_ERR_WORKSPACE = 7    /* workspace missing, misaligned or too small */
+    KDA_ERR_WORKSPACE = 7,   /* workspace missing, misaligned or too small */
+    KDA_ERR_HOST_MEMORY = 8  /* a host allocation failed */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -295,6 +296,61 @@ KDA_API size_t kda_state_slot_bytes(const kda_pool *pool);
 KDA_API kda_status kda_state_export(kda_pool *pool, int32_t slot, void *host, size_t bytes, kda_stream_t stream);
 KDA_API kda_status kda_state_import(kda_pool *pool, int32_t slot, const void *host, size_t bytes,
                                     kda_stream_t stream);
+
+/* ---- Prefix-state cache with second-hit admission (host only) ----------
+ * Decides, per prompt, which saved KDA state to resume from and where to
+ * save a new one.  Source: "vLLM Kimi K3 지원", section "하이브리드 KV-Cache
+ * 관리" (KDA state blocks kept apart from prefix matching, so a shared
+ * prompt reuses the saved state) and section "에이전틱 캐시 유지 정책"
+ * (Marconi-style selective retention: a prefix's state is saved only on the
+ * prefix's second hit).
+ *
+ * A prefix is the first i * block tokens of a prompt (block: a positive
+ * multiple of the chunk length 64), so every saved state is a checkpoint at
+ * a chunk end.  kda_prefix_cache_plan, for a prompt of n token ids:
+ *   - counts one hit on each of its n / block prefixes;
+ *   - hit_len / hit_slot: the longest saved prefix of at most n - 1 tokens
+ *     (0 / -1 if none).  The caller copies hit_slot into the request's slot
+ *     (kda_state_checkpoint) and prefills tokens [hit_len, n) with
+ *     has_initial_state = 1;
+ *   - admit_pos / admit_slot: at most one longer prefix with two or more hits
+ *     and no saved state (-1 / -1 if none).  The caller adds the checkpoint
+ *     request {seq, admit_pos - hit_len, admit_slot} to that prefill, which
+ *     writes the state there.
+ * Admission slots come from the cache's list, lowest free first; with none
+ * free, the least recently counted saved prefix other than the reused one
+ * gives its slot up (it stays tracked, unsaved, with its hits); with no such
+ * prefix nothing is admitted.  Unsaved prefixes beyond max_tracked are
+ * dropped, least recently counted first, at the end of each plan.  A saved
+ * prefix keeps its tokens, so only an exact match resumes from it.
+ * The slots are pool slots the caller sets aside for the cache; the device
+ * copies and prefills that use a plan go on one stream (or are ordered by
+ * the caller), which keeps a slot from being overwritten before an earlier
+ * copy from it has run.  Not thread-safe.
+ * Errors: KDA_ERR_INVALID_ARG (null pointer, negative count, block not a
+ * positive multiple of 64; forget of a slot holding no saved prefix),
+ * KDA_ERR_SLOT_RANGE (a negative slot), KDA_ERR_ALIAS (a slot listed twice),
+ * KDA_ERR_HOST_MEMORY. */
+typedef struct kda_prefix_cache kda_prefix_cache;
+typedef struct {
+    int32_t hit_len, hit_slot, admit_pos, admit_slot;
+} kda_prefix_plan;
+typedef struct {
+    int64_t plans, hits, admissions, evictions; /* hits: plans that reused a state */
+    int64_t n_saved, n_unsaved, n_free;
+} kda_prefix_cache_stats;
+KDA_API kda_status kda_prefix_cache_create(int32_t block, const int32_t *slots, int32_t n_slots, int32_t max_tracked,
+                                           kda_prefix_cache **out);
+KDA_API void kda_prefix_cache_destroy(kda_prefix_cache *cache);
+KDA_API kda_status kda_prefix_cache_plan(kda_prefix_cache *cache, const int32_t *tokens, int32_t n,
+                                         kda_prefix_plan *out);
+/* Gives up the state saved in `slot` (e.g. its prefill was abandoned): the
+ * slot returns to the free list and the prefix stays tracked, unsaved. */
+KDA_API kda_status kda_prefix_cache_forget(kda_prefix_cache *cache, int32_t slot);
+KDA_API kda_status kda_prefix_cache_get_stats(const kda_prefix_cache *cache, kda_prefix_cache_stats *out);
+/* Writes up to cap (prefix length, slot) pairs of the saved prefixes, least
+ * recently counted first; returns how many there are (-1 on a bad argument). */
+KDA_API int32_t kda_prefix_cache_saved(const kda_prefix_cache *cache, int32_t *lens, int32_t *slots, int32_t cap);
 
 /* Waits for `stream`, reads the device error word into *flags (may be NULL)
  * and clears it.  Returns KDA_ERR_DEVICE if any bit was set, else KDA_OK. */

@@ -101,8 +101,8 @@ class PrefixPolicy:
         return False
 
     def saved(self):
-        """{prefix length: slot} of the saved prefixes (for checks)."""
-        return {len(p): e[1] for p, e in self.entries.items() if e[1] >= 0}
+        """{slot: prefix length} of the saved prefixes (for checks)."""
+        return {e[1]: len(p) for p, e in self.entries.items() if e[1] >= 0}
 
     def n_unsaved(self) -> int:
         return sum(1 for e in self.entries.values() if e[1] < 0)

@@ -53,7 +53,7 @@ def test_pool_bytes_rejects_bad_descriptions(lib, bad):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         s = kda.kda_status_string(code)
         assert s and s != "unknown status"
     assert kda.kda_status_string(99) == "unknown status"
