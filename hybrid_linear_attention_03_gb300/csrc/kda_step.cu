@@ -149,6 +149,24 @@ kda_step_kernel(const StepParams p) {
     const size_t slot_elems = size_t(p.H) * head_elems;
     const Act *beta = static_cast<const Act *>(p.beta);
 
+    // The slot indices and beta go into registers first; nothing reads them
+    // before the grid-dependency wait, so their latency overlaps the copies
+    // below and the wait (consuming them here cost two dependent memory
+    // round trips ahead of the wait: 2.4K of 8.7K cycles per batch-1 step).
+    const int sub = lane / C::LPR, c4 = lane % C::LPR;
+    const int n_own = c4 / C::OWN;
+    const bool owner = (c4 % C::OWN) == 0;
+    const int own_row = n_own * C::RPL + sub;  // 0..15 within the warp
+    const int own_j = warp * 16 + own_row;     // value channel this lane reports
+    const int in_slot = p.in_slots[b];
+    int snap_r = 0;
+    const Act wn_r = static_cast<const Act *>(p.norm_w)[own_j];  // a weight: safe before the wait
+    Act beta_r = from_f32<Act>(0.f);
+    if (threadIdx.x < T) {
+        snap_r = p.snap_slots[b * T + threadIdx.x];
+        beta_r = beta[(size_t(b) * T + threadIdx.x) * p.H + h];
+    }
+
     // Per-token inputs of all T tokens (never written by the preceding step
     // launch): 16-byte asynchronous copies into shared memory, issued first
     // so the whole prologue costs one memory latency.  Every (token, head)
@@ -171,30 +189,22 @@ kda_step_kernel(const StepParams p) {
                           static_cast<const Act *>(p.conv_w) + (size_t(st) * p.H + h) * D * 4 + cc * EPC);
     }
     sm100::cp_async_commit();
-    if (threadIdx.x < T) bsm[threadIdx.x] = to_f32(beta[(size_t(b) * T + threadIdx.x) * p.H + h]);
 
-    const int in_slot = p.in_slots[b];
-    bool bad = in_slot < 0 || in_slot >= p.num_slots;
-    for (int t = 0; t < T; ++t) {
-        const int s = p.snap_slots[b * T + t];
-        bad |= (s < 0 || s >= p.num_slots);
-        if (threadIdx.x == t) snap_sm[t] = s;
-    }
-    if (bad) {
-        if (threadIdx.x == 0) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
-        sm100::cp_async_wait_all();  // no copy may land after the CTA is gone
-        return;
-    }
-
-    const int sub = lane / C::LPR, c4 = lane % C::LPR;
-    const int n_own = c4 / C::OWN;
-    const bool owner = (c4 % C::OWN) == 0;
-    const int own_row = n_own * C::RPL + sub;  // 0..15 within the warp
-    const int own_j = warp * 16 + own_row;     // value channel this lane reports
 
     // The pool's state and tail may have been written by the preceding step
     // launch: wait for it to complete before reading them.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x < T) {
+        bsm[threadIdx.x] = to_f32(beta_r);
+        snap_sm[threadIdx.x] = snap_r;
+    }
+    // A bad input slot (uniform over the CTA) stops before any state access;
+    // bad snapshot slots are found at the barrier below, before any write.
+    if (in_slot < 0 || in_slot >= p.num_slots) {
+        if (threadIdx.x == 0) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
+        sm100::cp_async_wait_all();  // no copy may land after the CTA is gone
+        return;
+    }
     const float *Sin = p.states + size_t(in_slot) * slot_elems + size_t(h) * head_elems;
     float4 S[C::NV];
 #pragma unroll
@@ -212,7 +222,10 @@ kda_step_kernel(const StepParams p) {
     }
     sm100::cp_async_commit();
     sm100::cp_async_wait_all();
-    __syncthreads();
+    if (__syncthreads_or(threadIdx.x < T && (snap_r < 0 || snap_r >= p.num_slots))) {
+        if (threadIdx.x == 0) atomicOr(p.err, KDA_DEVERR_SLOT_RANGE);
+        return;
+    }
 
     // ---- conv + SiLU (+ L2 for q and k): a warp per (token, stream) row --------
     for (int row = warp; row < 3 * T; row += C::WPC) {
@@ -245,11 +258,34 @@ kda_step_kernel(const StepParams p) {
             if (c < D) conv[(t * 3 + s) * D + c] = y[m] * r;
         }
     }
-    // The old tail is fully read (raw) before any snapshot tail is written.
+    // New conv tails: the raw rows t+1 .. t+3 of the window, already in
+    // shared memory (the old tail was read into it above, so the global
+    // tail may be overwritten).  When the conv leaves warps idle (3T < warps)
+    // they store every token's tail now, off the critical path; otherwise
+    // each warp stores its channels' tails in the token loop.
+    const bool early_tails = 3 * T < C::WPC;
+    Act *tails = static_cast<Act *>(p.tails);
+    if (early_tails && warp >= 3 * T) {
+        for (int i = threadIdx.x - 3 * T * 32; i < T * 9 * CPR; i += (C::WPC - 3 * T) * 32) {
+            const int row = i / CPR, cc = i - row * CPR;  // row = t * 9 + tap * 3 + stream
+            const int t = row / 9, js = row - t * 9, j = js / 3, st = js - j * 3;
+            Act *dst = tails + size_t(snap_sm[t]) * 3 * p.n_ch + size_t(j) * p.n_ch + size_t(st) * p.H * D +
+                       size_t(h) * D + cc * EPC;
+            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(raw + size_t((t + 1 + j) * 3 + st) * D + cc * EPC);
+        }
+    }
     __syncthreads();
 
+    // Programmatic dependent launch: the next step-kernel launch on this
+    // stream may start now and run its own prologue up to its
+    // griddepcontrol.wait, which waits for this whole grid to complete (so
+    // the trigger's position only moves the overlap).  Measured at batch 1
+    // (graph of 1000 steps, same GPU): 3.86 us per step with the trigger
+    // here, 4.09 us after the token loop, 3.88 us right after the wait;
+    // batch 64: 87.8, 88.0 and 88.1 us.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     Act *out = static_cast<Act *>(p.out);
-    Act *tails = static_cast<Act *>(p.tails);
 
     for (int t = 0; t < T; ++t) {
         const float4 qv = load4(conv + (t * 3 + 0) * D + 4 * c4);
@@ -259,6 +295,11 @@ kda_step_kernel(const StepParams p) {
         const float4 ka = make_float4(kv.x * av.x, kv.y * av.y, kv.z * av.z, kv.w * av.w);
         const float4 bk = make_float4(bt * kv.x, bt * kv.y, bt * kv.z, bt * kv.w);
 
+        const float *vrow = conv + (t * 3 + 2) * D + warp * 16;
+        float vv[C::NV];
+#pragma unroll
+        for (int n = 0; n < C::NV; ++n) vv[n] = vrow[n * C::RPL + sub];
+
         // u_j = sum_i k_i alpha_i S_ij  (prediction of v_j by the decayed state)
         float red[C::NV];
 #pragma unroll
@@ -267,30 +308,17 @@ kda_step_kernel(const StepParams p) {
         if (owner) ubuf[warp * 16 + own_row] = red[0];
         __syncwarp();
         // S'_ij = alpha_i S_ij + beta k_i (v_j - u_j)
-        const float *vrow = conv + (t * 3 + 2) * D + warp * 16;
 #pragma unroll
         for (int n = 0; n < C::NV; ++n) {
-            const int r = n * C::RPL + sub;
-            const float d = vrow[r] - ubuf[warp * 16 + r];
+            const float d = vv[n] - ubuf[warp * 16 + n * C::RPL + sub];
             S[n].x = fmaf(av.x, S[n].x, bk.x * d);
             S[n].y = fmaf(av.y, S[n].y, bk.y * d);
             S[n].z = fmaf(av.z, S[n].z, bk.z * d);
             S[n].w = fmaf(av.w, S[n].w, bk.w * d);
         }
-        // o_j = sum_i q_i S'_ij
-#pragma unroll
-        for (int n = 0; n < C::NV; ++n) red[n] = dot4(qv, S[n]);
-        RowReduce<C::NV, C::LPR / 2>::run(red, lane);
-        if (owner) obuf[t * D + own_j] = red[0];
-        __syncwarp();
-        if (lane == 0) {
-            float a = 0.f;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) a = fmaf(obuf[t * D + warp * 16 + r], obuf[t * D + warp * 16 + r], a);
-            sq[t * C::WPC + warp] = a;
-        }
 
-        // Snapshot.  A single-token launch stores its rows directly (in
+        // Snapshot, issued before the readout so the stores drain while it
+        // runs.  A single-token launch stores its rows directly (in
         // place).  With several drafts the snapshot stream dominates: this
         // warp's 16 state rows are one contiguous 16*D*4-byte block in HBM,
         // staged in shared memory and handed to the TMA engine as one bulk
@@ -320,11 +348,24 @@ kda_step_kernel(const StepParams p) {
                 sm100::bulk_commit();
             }
         }
-        Act *tail_out = tails + size_t(snap) * 3 * p.n_ch;
-        for (int idx = lane; idx < 9 * 16; idx += 32) {  // 3 taps x 3 streams x this warp's 16 channels
-            const int j = idx / 48, rem = idx - j * 48;
-            const int s = rem >> 4, c = warp * 16 + (rem & 15);
-            tail_out[j * p.n_ch + s * p.H * D + h * D + c] = raw[((t + 1 + j) * 3 + s) * D + c];
+
+        // o_j = sum_i q_i S'_ij; this warp's sum of o_j^2 for the norm
+#pragma unroll
+        for (int n = 0; n < C::NV; ++n) red[n] = dot4(qv, S[n]);
+        RowReduce<C::NV, C::LPR / 2>::run(red, lane);
+        if (owner) obuf[t * D + own_j] = red[0];
+        float o2 = owner ? red[0] * red[0] : 0.f;  // each of the warp's 16 rows has exactly one owner lane
+#pragma unroll
+        for (int o = 16; o; o >>= 1) o2 += __shfl_xor_sync(0xffffffffu, o2, o);
+        if (lane == 0) sq[t * C::WPC + warp] = o2;
+
+        if (!early_tails) {
+            Act *tail_out = tails + size_t(snap) * 3 * p.n_ch;
+            for (int idx = lane; idx < 9 * 16; idx += 32) {  // 3 taps x 3 streams x this warp's 16 channels
+                const int j = idx / 48, rem = idx - j * 48;
+                const int s = rem >> 4, c = warp * 16 + (rem & 15);
+                tail_out[j * p.n_ch + s * p.H * D + h * D + c] = raw[((t + 1 + j) * 3 + s) * D + c];
+            }
         }
         __syncwarp();  // ubuf is rewritten by the next token
     }
@@ -334,13 +375,7 @@ kda_step_kernel(const StepParams p) {
     if (T > 1 && lane == 0) sm100::bulk_wait_read();
     // Gated RMSNorm of every token over the head's D value channels.
     __syncthreads();
-    // Programmatic dependent launch: the next step-kernel launch on this
-    // stream may start now and run its own prologue up to its
-    // griddepcontrol.wait, which waits for this grid to complete.  Measured
-    // at batch 1 (graph of 1000 steps, same GPU): 5.3 us per step with the
-    // trigger here, 6.2 us with it at kernel start, 6.0 us without it.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const float wn = to_f32(static_cast<const Act *>(p.norm_w)[own_j]);
+    const float wn = to_f32(wn_r);
     for (int t = 0; t < T; ++t) {
         float tot = 0.f;
 #pragma unroll
