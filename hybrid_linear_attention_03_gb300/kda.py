@@ -338,8 +338,7 @@ def kda_prefill_chunked_dev(pool: StatePool, weights: kda_weights, io: kda_io, c
                                          int(max_tokens), int(chunk), None if n_req == 0 else reqs.data_ptr(),
                                          n_req, _dptr(workspace), workspace.numel() * workspace.element_size(),
                                          _stream(stream)),
-           "kda_prefill_chunked_dev", "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_plan",
-           "kda_prefix_cache_forget", "kda_prefix_cache_get_stats", "kda_prefix_cache_saved")
+           "kda_prefill_chunked_dev")
 
 
 def kda_prefill_chunked_noalloc(pool: StatePool, weights: kda_weights, io: kda_io, cu_seqlens, slots,

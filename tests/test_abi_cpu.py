@@ -73,3 +73,14 @@ def test_state_transfer_rejects_null_arguments(lib):
     assert lib.kda_state_slot_bytes(None) == 0
     assert lib.kda_state_export(None, 0, ctypes.addressof(buf), 16, None) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_state_import(None, 0, ctypes.addressof(buf), 16, None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_binding_status_checks_name_their_entry_point():
+    """Every _check(status, where) call in the binding passes exactly two
+    arguments (a wrapper whose call is malformed only fails on a GPU)."""
+    import ast
+    tree = ast.parse(Path(kda.__file__).read_text())
+    calls = [n for n in ast.walk(tree) if isinstance(n, ast.Call) and getattr(n.func, "id", None) == "_check"]
+    assert calls
+    for c in calls:
+        assert len(c.args) == 2 and isinstance(c.args[1], ast.Constant), f"line {c.lineno}"
