@@ -261,7 +261,7 @@ __device__ __forceinline__ float4 conv_taps(const PrefillParams &p, int s, int h
 // ============================================================== intra ====
 namespace is {  // intra shared-memory map (bytes from a 1 KiB-aligned base)
 constexpr uint32_t X_HI = 0, X_LO = 32768, KB_HI = 65536, KB_LO = 81920;           // phase 1 images
-constexpr uint32_t A_F32 = 0, XS_F32 = 16384, T_F32 = 81920;                        // inverse (fp32)
+constexpr uint32_t A_F32 = 0, T_F32 = 81920;                                        // inverse (fp32)
 constexpr uint32_t T_HI = 0, T_LO = 8192, AK_HI = 16384, AK_LO = 32768, AV_HI = 49152, AV_LO = 65536;  // phase 3
 constexpr uint32_t RQ = 0;        // raw q, k (67 rows each) and, 2-byte, alpha tiles; then the phase-1 images
 constexpr uint32_t IN0 = 98304;   // q^, then v, then the W image staging (32 KiB)
@@ -271,6 +271,8 @@ constexpr uint32_t SMALL = 196608;
 constexpr uint32_t RV_LATE = 32768;         // raw v tile of a 4-byte activation (free while T is formed)
 constexpr uint32_t RV_EARLY = SMALL + 2560; // raw v tile of a 2-byte activation (loaded with the others)
 constexpr uint32_t TDIAG = RV_EARLY + (CH + HALO) * D * 2;  // [4][16 s][16 r] diagonal blocks of T, transposed
+constexpr uint32_t XS_C = RV_EARLY;  // [3][16][16] fp32 scratch of the off-diagonal blocks (the raw v tile is consumed)
+constexpr int OFFDIAG_THREADS = 192;  // warps 0..5 form T's off-diagonal blocks, the rest the T-free phase-3 images
 constexpr int NT = 512;
 constexpr int QW = NT / 128;  // warps per TMEM lane quarter (a warp reaches lanes 32 (w % 4) .. + 31)
 template <typename Act>
@@ -292,7 +294,8 @@ __host__ __device__ constexpr uint32_t BYTES() { return TDIAG + 4 * 16 * 16 * 4;
 template <typename Act>
 __host__ __device__ constexpr bool map_ok() {
     return RK<Act>() + tile_bytes<Act>() <= IN0 && (sizeof(Act) != 2 || RA<Act>() + CH * D * sizeof(Act) <= IN0) &&
-           (v_early<Act>() || (RV_LATE >= XS_F32 + 16384 && RV_LATE + tile_bytes<Act>() <= T_F32)) &&
+           (v_early<Act>() || (RV_LATE >= A_F32 + 16384 && RV_LATE + tile_bytes<Act>() <= T_F32)) &&
+           XS_C + 3 * 16 * 16 * 4 <= TDIAG &&
            (!v_early<Act>() || RV_EARLY + tile_bytes<Act>() <= TDIAG) && BYTES<Act>() + 1024 <= 232448 &&
            tile_bytes<Act>() % 128 == 0;
 }
@@ -342,13 +345,18 @@ __device__ __forceinline__ void mma3(uint32_t d, uint32_t a_hi, uint32_t a_lo, u
 
 // One level of the blocked inverse of I + A (A stored transposed: A[s * CH +
 // r] = A_rs; TD holds T's diagonal blocks transposed): the 4 - d blocks at
-// distance d below the diagonal; a thread owns 4 adjacent columns of one row,
-// so each A value it loads feeds 4 FMAs and the T / X values arrive as
-// 16-byte vectors; the 8 rows a warp covers read A and TD without bank
-// conflicts.
+// distance d below the diagonal, T_ab = -T_aa sum_{b <= c < a} A_ac T_cb,
+// by the first OFFDIAG_THREADS threads (named barrier 1; a level has at most
+// 3 x 64 work items).  A thread owns 4 adjacent columns of one row, so each A
+// value it loads feeds 4 FMAs and the T / X values arrive as 16-byte vectors;
+// the 8 rows a warp covers read A and TD without bank conflicts.  XS holds the
+// level's sums, block blk = b at [blk][16][16].
+__device__ __forceinline__ void offdiag_sync() {
+    asm volatile("bar.sync 1, %0;" :: "n"(is::OFFDIAG_THREADS) : "memory");
+}
 __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS, const float *TD, int tid, int d) {
     const int nblk = 4 - d;
-    for (int e = tid; e < nblk * 64; e += is::NT) {
+    for (int e = tid; e < nblk * 64; e += is::OFFDIAG_THREADS) {
         const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4, a = blk + d, b = blk;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
@@ -360,16 +368,16 @@ __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS,
             acc.z = fmaf(av, tv.z, acc.z);
             acc.w = fmaf(av, tv.w, acc.w);
         }
-        *reinterpret_cast<float4 *>(XS + (a * 16 + r) * CH + b * 16 + c4) = acc;
+        *reinterpret_cast<float4 *>(XS + (blk * 16 + r) * 16 + c4) = acc;
     }
-    __syncthreads();
-    for (int e = tid; e < nblk * 64; e += is::NT) {
+    offdiag_sync();
+    for (int e = tid; e < nblk * 64; e += is::OFFDIAG_THREADS) {
         const int blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4, a = blk + d, b = blk;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
         for (int s = 0; s < 16; ++s) {
             const float tv = -TD[(a * 16 + s) * 16 + r];  // T[a16 + r][a16 + s]
-            const float4 xv = ld4(XS + (a * 16 + s) * CH + b * 16 + c4);
+            const float4 xv = ld4(XS + (blk * 16 + s) * 16 + c4);
             acc.x = fmaf(tv, xv.x, acc.x);
             acc.y = fmaf(tv, xv.y, acc.y);
             acc.z = fmaf(tv, xv.z, acc.z);
@@ -377,7 +385,7 @@ __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS,
         }
         *reinterpret_cast<float4 *>(T + (a * 16 + r) * CH + b * 16 + c4) = acc;
     }
-    __syncthreads();
+    offdiag_sync();
 }
 
 // One CTA (16 warps) per (chunk, head).  TMA brings the raw q, k, v tiles of
@@ -701,7 +709,7 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
     }
     // ---- T = (I + A)^-1 (unit lower triangular), 16 x 16 blocks
     float *T = reinterpret_cast<float *>(sm + is::T_F32);
-    float *XS = reinterpret_cast<float *>(sm + is::XS_F32);
+    float *XS = reinterpret_cast<float *>(sm + is::XS_C);
     float *TD = reinterpret_cast<float *>(sm + is::TDIAG);  // TD[(a16 + s) 16 + r] = T[a16 + r][a16 + s]
     for (int e = tid; e < CH * CH; e += is::NT) T[e] = 0.f;  // the blocks above the diagonal stay 0
     __syncthreads();
@@ -736,15 +744,16 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
                                    tail ? tail + 2 * p.H * D + vc : nullptr, p.n_ch, reinterpret_cast<float *>(sm + is::IN0));
     }
     ok = __syncthreads_and(ok && vok);
-    // Blocks below the diagonal, by distance d: T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
+    // ---- phase 3: W^T = (beta exp(G) . K)^T T^T and Ut^T = (beta V)^T T^T.
+    // Warps 0..5 form T's blocks below the diagonal, by distance d, while the
+    // other warps build the two operand images that do not involve T (the
+    // off-diagonal levels have at most 192 work items).
+    if (tid < is::OFFDIAG_THREADS) {
 #pragma unroll 1
-    for (int d = 1; d < 4; ++d) tri_offdiag(A, T, XS, TD, tid, d);
-    // ---- phase 3: W^T = (beta exp(G) . K)^T T^T and Ut^T = (beta V)^T T^T
-    if (ok) {
-        build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, is::NT, [&](int r, int s0, float(&x)[8]) {
-            ld8(T + r * CH + s0, x);
-        });
-        build_image<true>(sm + is::AK_HI, sm + is::AK_LO, D, 8, tid, is::NT, [&](int i, int s0, float(&x)[8]) {
+        for (int d = 1; d < 4; ++d) tri_offdiag(A, T, XS, TD, tid, d);
+    } else if (ok) {
+        const int t2 = tid - is::OFFDIAG_THREADS, n2 = is::NT - is::OFFDIAG_THREADS;
+        build_image<true>(sm + is::AK_HI, sm + is::AK_LO, D, 8, t2, n2, [&](int i, int s0, float(&x)[8]) {
             const float cc = ec[i];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -752,9 +761,15 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
                 x[e] = beta[s0 + e] * (exact ? expf(gv) : gv * cc) * KHs[(s0 + e) * D + i];
             }
         });
-        build_image<true>(sm + is::AV_HI, sm + is::AV_LO, D, 8, tid, is::NT, [&](int j, int s0, float(&x)[8]) {
+        build_image<true>(sm + is::AV_HI, sm + is::AV_LO, D, 8, t2, n2, [&](int j, int s0, float(&x)[8]) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = beta[s0 + e] * VVs[(s0 + e) * D + j];
+        });
+    }
+    __syncthreads();
+    if (ok) {
+        build_image(sm + is::T_HI, sm + is::T_LO, CH, 8, tid, is::NT, [&](int r, int s0, float(&x)[8]) {
+            ld8(T + r * CH + s0, x);
         });
     }
     fence_proxy_async_smem();
