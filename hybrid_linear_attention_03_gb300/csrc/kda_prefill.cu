@@ -252,6 +252,56 @@ __device__ __forceinline__ void conv_silu_channel(const Act *__restrict__ tile, 
     }
 }
 
+// The same for exactly 32 tokens t0 .. t0 + 31, into registers (fully
+// unrolled so y stays in registers): y[e] is token t0 + e.
+template <typename Act>
+__device__ __forceinline__ void conv_silu_regs32(const Act *__restrict__ tile, int c, float4 w, int t0, int pos0, int len,
+                                                 const Act *__restrict__ tail_c, int n_ch, float (&y)[32]) {
+    float x[3];
+#pragma unroll
+    for (int j = 0; j < HALO; ++j) {
+        const int row = t0 + j, pos = pos0 - HALO + row;
+        x[j] = pos >= 0 ? to_f32(tile[row * D + c]) : (tail_c ? to_f32(tail_c[size_t(HALO + pos) * n_ch]) : 0.f);
+    }
+    float x0 = x[0], x1 = x[1], x2 = x[2];
+#pragma unroll
+    for (int b = 0; b < 32; b += 8) {
+        float xs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xs[e] = to_f32(tile[(t0 + b + e + HALO) * D + c]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float acc = w.x * x0;
+            acc = fmaf(w.y, x1, acc);
+            acc = fmaf(w.z, x2, acc);
+            acc = fmaf(w.w, xs[e], acc);
+            y[b + e] = t0 + b + e < len ? acc * sigmoid_fast(acc) : 0.f;
+            x0 = x1;
+            x1 = x2;
+            x2 = xs[e];
+        }
+    }
+}
+
+// Transpose-reduce of 32 values per lane across the warp: afterwards v[0] of
+// lane l is the sum over all 32 lanes of their value l.  At the stage with
+// xor-offset O the upper lane of each pair keeps the upper half of its
+// values, so the live values halve every stage (31 shuffles in all).
+template <int CNT, int O>
+__device__ __forceinline__ void lane_transpose_sum(float *v, int lane) {
+    if constexpr (O > 0) {
+        constexpr int HALF = CNT / 2;
+        const bool upper = (lane & O) != 0;
+#pragma unroll
+        for (int m = 0; m < HALF; ++m) {
+            const float send = upper ? v[m] : v[m + HALF];
+            const float keep = upper ? v[m + HALF] : v[m];
+            v[m] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+        }
+        lane_transpose_sum<HALF, O / 2>(v, lane);
+    }
+}
+
 // Conv taps of channel c of stream s (0 q, 1 k, 2 v) of head h.
 template <typename Act>
 __device__ __forceinline__ float4 conv_taps(const PrefillParams &p, int s, int h, int c) {
@@ -265,6 +315,7 @@ constexpr uint32_t A_F32 = 0, T_F32 = 81920;                                    
 constexpr uint32_t T_HI = 0, T_LO = 8192, AK_HI = 16384, AK_LO = 32768, AV_HI = 49152, AV_LO = 65536;  // phase 3
 constexpr uint32_t RQ = 0;        // raw q, k (67 rows each) and, 2-byte, alpha tiles; then the phase-1 images
 constexpr uint32_t IN0 = 98304;   // q^, then v, then the W image staging (32 KiB)
+constexpr uint32_t SSQ = IN0 - 4096;  // [2 qk][2 halves][4 warps][32] sums of squares, then [16 warps][32] norms (conv phase)
 constexpr uint32_t KH = 131072;   // fp32 [64][128] k^
 constexpr uint32_t GG = 163840;   // fp32 [64][128] G, then E = exp(G - c)
 constexpr uint32_t SMALL = 196608;
@@ -296,6 +347,7 @@ __host__ __device__ constexpr bool map_ok() {
     return RK<Act>() + tile_bytes<Act>() <= IN0 && (sizeof(Act) != 2 || RA<Act>() + CH * D * sizeof(Act) <= IN0) &&
            (v_early<Act>() || (RV_LATE >= A_F32 + 16384 && RV_LATE + tile_bytes<Act>() <= T_F32)) &&
            XS_C + 3 * 16 * 16 * 4 <= TDIAG &&
+           SSQ >= RK<Act>() + tile_bytes<Act>() && (sizeof(Act) != 2 || SSQ >= RA<Act>() + CH * D * sizeof(Act)) &&
            (!v_early<Act>() || RV_EARLY + tile_bytes<Act>() <= TDIAG) && BYTES<Act>() + 1024 <= 232448 &&
            tile_bytes<Act>() % 128 == 0;
 }
@@ -463,62 +515,64 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
     const uint32_t tm = *tbase;
     bool ok = __syncthreads_and(mbar_wait(bar_ld, 0, p.err));
     uint32_t mma_phase = 0;
-    // SiLU(conv(q)) -> q^ buffer, SiLU(conv(k)) -> k^ buffer (normalised
-    // below): two threads per channel, 32 tokens each.
+    // q^ = L2(SiLU(conv(q))), k^ likewise: two threads per channel, 32 tokens
+    // each, the values kept in registers.  The warp's 32 lanes are 32
+    // channels of one (stream, half): a transpose-reduce gives each lane the
+    // warp's sum of squares of one token, the 4 warps of the (stream, half)
+    // add theirs through shared memory, and the scaled values are stored once.
     float *GGw = reinterpret_cast<float *>(sm + is::GG);
     float *QHw = reinterpret_cast<float *>(sm + is::IN0), *KHw = reinterpret_cast<float *>(sm + is::KH);
-    if (ok)
-        conv_silu_channel<Act>(qk ? rk : rq, cc, w_qk, qh * (CH / 2), CH / 2, cm.pos0, cm.len,
-                               tail ? tail + qk * p.H * D + cc : nullptr, p.n_ch, qk ? KHw : QHw);
-    // ln of the 128 bf16 mantissas 1 + m/128, in the c buffer (written only after G)
-    if (sizeof(Act) == 2 && tid < D) cref[tid] = logf(1.0f + float(tid) * (1.0f / 128.0f));
-    __syncthreads();
-    // Threads 0..255: G = cumulative log decay, thread = (channel gi, half gh
-    // of the chunk); the second half adds the first half's total below.  (A
-    // 4-byte alpha tile is the G buffer itself: element in, element out.)
-    // Threads 256..511 meanwhile: L2 norm of the 64 q rows and 64 k rows, a
-    // warp per row, 2 rows at a time.
-    const int gi = tid & (D - 1), gh = tid >> 7;
-    if (ok && tid < 2 * D) {
-        float G = 0.f;
-#pragma unroll 1
-        for (int t0 = gh * (CH / 2); t0 < (gh + 1) * (CH / 2); t0 += 8) {  // 8 logarithms in flight
-            Act av[8];
-            float lg[8];
+    float *ssq = reinterpret_cast<float *>(sm + is::SSQ);
+    {
+        float y[32];
+        if (ok) {
+            conv_silu_regs32<Act>(qk ? rk : rq, cc, w_qk, qh * (CH / 2), cm.pos0, cm.len,
+                                  tail ? tail + qk * p.H * D + cc : nullptr, p.n_ch, y);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) av[e] = ra[(t0 + e) * D + gi];
-            log_alpha8(av, cref, lg);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) lg[e] = fmaxf(lg[e], kLogAlphaMin);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (t0 + e < cm.len) G += lg[e];
-                GGw[(t0 + e) * D + gi] = G;
-            }
+            for (int e = 0; e < 32; ++e) y[e] = 0.f;
         }
-    } else if (ok) {
-        constexpr int LW = is::NT / 32 - 8;  // warps 8..15
-#pragma unroll 1
-        for (int r0 = (warp - 8) * 2; r0 < 2 * CH; r0 += LW * 2) {
-            float4 v[2];
-            float ss[2];
+        float s2[32];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int row = r0 + i;
-                v[i] = ld4((row < CH ? QHw + row * D : KHw + (row - CH) * D) + 4 * lane);
-                ss[i] = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, v[i].w * v[i].w)));
-            }
+        for (int e = 0; e < 32; ++e) s2[e] = y[e] * y[e];
+        lane_transpose_sum<32, 16>(s2, lane);
+        const int grp = (qk * 2 + qh) * 4;  // the 4 warps of this (stream, half): warp & 3 = channel quarter
+        ssq[(grp + (warp & 3)) * 32 + lane] = s2[0];
+        // ln of the 128 bf16 mantissas 1 + m/128, in the c buffer (written only after G)
+        if (sizeof(Act) == 2 && tid < D) cref[tid] = logf(1.0f + float(tid) * (1.0f / 128.0f));
+        __syncthreads();
+        float *rn = ssq + 512 + warp * 32;  // this warp's 32 token norms
+        rn[lane] = rsqrtf(ssq[grp * 32 + lane] + ssq[(grp + 1) * 32 + lane] + ssq[(grp + 2) * 32 + lane] +
+                          ssq[(grp + 3) * 32 + lane] + p.eps_l2);
+        __syncwarp();
+        float *outp = (qk ? KHw : QHw) + qh * (CH / 2) * D + cc;
 #pragma unroll
-            for (int o = 16; o; o >>= 1)
+        for (int e = 0; e < 32; e += 4) {
+            const float4 r4 = ld4(rn + e);
+            outp[(e + 0) * D] = y[e + 0] * r4.x;
+            outp[(e + 1) * D] = y[e + 1] * r4.y;
+            outp[(e + 2) * D] = y[e + 2] * r4.z;
+            outp[(e + 3) * D] = y[e + 3] * r4.w;
+        }
+    }
+    // G = cumulative log decay, thread = (channel gi, half gh of the chunk);
+    // the second half adds the first half's total below.  (A 4-byte alpha
+    // tile is the G buffer itself: element in, element out.)
+    const int gi = tid & (D - 1), gh = tid >> 7;
+    if (ok && tid < 2 * D) {  // all 32 loads, then all 32 logarithms, then the scan: one latency each
+        const int t0 = gh * (CH / 2);
+        Act av[CH / 2];
+        float lg[CH / 2];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], o);
+        for (int e = 0; e < CH / 2; ++e) av[e] = ra[(t0 + e) * D + gi];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int row = r0 + i;
-                const float n = rsqrtf(ss[i] + p.eps_l2);
-                *reinterpret_cast<float4 *>((row < CH ? QHw + row * D : KHw + (row - CH) * D) + 4 * lane) =
-                    make_float4(v[i].x * n, v[i].y * n, v[i].z * n, v[i].w * n);
-            }
+        for (int b = 0; b < CH / 2; b += 8)
+            log_alpha8(*reinterpret_cast<const Act(*)[8]>(av + b), cref, *reinterpret_cast<float(*)[8]>(lg + b));
+        float G = 0.f;
+#pragma unroll
+        for (int e = 0; e < CH / 2; ++e) {
+            if (t0 + e < cm.len) G += fmaxf(lg[e], kLogAlphaMin);
+            GGw[(t0 + e) * D + gi] = G;
         }
     }
     __syncthreads();
