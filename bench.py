@@ -99,6 +99,26 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+# The layer has no exchange step: under torchrun every rank runs its own
+# replica of the workload, and the ranks meet only around the timed region.
+def rank_barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(ms, world, device):
+    """The slowest rank's timed milliseconds (every rank holds the result)."""
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms):
+    """Units all ranks processed per second over the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -248,19 +268,13 @@ def run_ours(a, rank, world, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.25)
-    if world > 1:
-        torch.distributed.barrier()
+    rank_barrier(world)
     torch.cuda.synchronize()
     evs = [one_step() for _ in range(a.steps)]
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = sum(s.elapsed_time(e) for s, e in evs)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(ms_t.item())
-    value = a.steps * n_steps * world / (ms / 1e3)
+    rank_barrier(world)
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs), world, dev)
+    value = job_throughput(a.steps * n_steps, world, ms)
     bytes_b1 = step_bytes(H, D, 1, 1)
     launch_us = ms * 1e3 / (a.steps * n_steps)
     achieved = bytes_b1 / (launch_us * 1e-6) / 1e9
@@ -288,10 +302,12 @@ def run_ours(a, rank, world, local):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
+    rank_barrier(world)
     evs2 = [e2e_step() for _ in range(a.steps)]
     torch.cuda.synchronize()
-    ms2 = sum(s.elapsed_time(e) for s, e in evs2)
-    e2e_value = a.steps * n_steps * world / (ms2 / 1e3)
+    rank_barrier(world)
+    ms2 = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs2), world, dev)
+    e2e_value = job_throughput(a.steps * n_steps, world, ms2)
     clk = clocks.stop()
 
     line = {
