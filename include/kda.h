@@ -263,7 +263,10 @@ KDA_API kda_status kda_prefill_chunked_noalloc(kda_pool *pool, const kda_weights
  *   a request at a bad sequence or position, or a repeated slot set
  *   KDA_DEVERR_META; a slot out of range sets KDA_DEVERR_SLOT_RANGE.  Either
  *   way the call then changes no slot and writes no output (read the error
- *   word with kda_poll_device_error). */
+ *   word with kda_poll_device_error).
+ * Cost: the builder is one 1024-thread CTA; it ranks the requests by
+ *   comparing every pair, so its time grows with n_reqs^2 / 1024 (a few
+ *   microseconds for hundreds of requests). */
 KDA_API size_t kda_prefill_workspace_bytes_bound(const kda_pool *pool, int32_t N, int32_t max_tokens, int32_t n_reqs,
                                                  int32_t chunk);
 KDA_API kda_status kda_prefill_chunked_dev(kda_pool *pool, const kda_weights *w, const kda_io *io,
@@ -330,7 +333,8 @@ KDA_API kda_status kda_state_import(kda_pool *pool, int32_t slot, const void *ho
  * Errors: KDA_ERR_INVALID_ARG (null pointer, negative count, block not a
  * positive multiple of 64; forget of a slot holding no saved prefix),
  * KDA_ERR_SLOT_RANGE (a negative slot), KDA_ERR_ALIAS (a slot listed twice),
- * KDA_ERR_HOST_MEMORY. */
+ * KDA_ERR_HOST_MEMORY (a plan or forget that fails this way may leave the
+ * cache partly updated: destroy it and start a new one). */
 typedef struct kda_prefix_cache kda_prefix_cache;
 typedef struct {
     int32_t hit_len, hit_slot, admit_pos, admit_slot;
