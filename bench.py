@@ -86,7 +86,8 @@ def args_():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
-    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "prefill", "mixed", "mma_rates"], default=None,
+    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "decode_b1_l2_flushed", "prefill", "mixed",
+                                       "mma_rates"], default=None,
                     help="run one secondary case alone (for profiling) and print its numbers; mma_rates times "
                          "the prefill's tensor-core MMA groups in a separately built timing library")
     ap.add_argument("--prefill-tokens", type=int, default=None,
@@ -350,7 +351,9 @@ def run_ours(a, rank, world, local):
 
 
 def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
-    """Batch-64 rooflines of the step kernel: decode (T = 1) and verify (T = 8)."""
+    """HBM rooflines of the step kernel with L2 flushed before every launch:
+    batch-64 decode (T = 1) and verify (T = 8), and a single batch-1 decode
+    (its state then comes from HBM, unlike the chained headline steps)."""
     res = {}
     wl = I.VERIFY_B64
     H, D, act, B = wl.H, wl.dk, wl.act, wl.extra["B"]
@@ -361,8 +364,9 @@ def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
     perm = torch.from_numpy(I.permutation(wl.seed, 0, wl.num_slots)).to(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    for name, T, profile in (("decode_b64", 1, "kda_step_decode_b64_full.md"),
-                             ("verify_b64_t8", 8, "kda_step_verify_b64_t8_dram.md")):
+    for name, B, T, profile in (("decode_b64", wl.extra["B"], 1, "kda_step_decode_b64_full.md"),
+                                ("verify_b64_t8", wl.extra["B"], 8, "kda_step_verify_b64_t8_dram.md"),
+                                ("decode_b1_l2_flushed", 1, 1, "kda_step_decode_b1_cold_dram.md")):
         if only is not None and name != only:
             continue
         toks = {k: v.to(dev) for k, v in wl.tokens(200, B * T).items()}
