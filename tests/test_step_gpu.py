@@ -85,6 +85,28 @@ def test_verify_matches_oracle(B):
         assert m.tail_equal(int(s))
 
 
+@pytest.mark.parametrize("T", [1, 3, 16])
+def test_verify_draft_counts_match_oracle(T):
+    """The draft-count edges: one draft, an odd count and the maximum (16),
+    3 sequences (H = 4, d = 128, bf16), each continuing from a warmed slot
+    with its snapshots in a shuffled table."""
+    H, D, B, act = 4, 128, 3, torch.bfloat16
+    ns = 2 * B * T + B
+    m = Mirror(ns, H, D, act, _weights(13, H, D, act))
+    perm = [int(x) for x in I.permutation(13, T, ns)]
+    warm_in, warm_snap = perm[:B], np.array(perm[B:B + B * T], dtype=np.int32).reshape(B, T)
+    m.verify(warm_in, warm_snap, T, _tokens(13, 1, B * T, H, D, act))
+    starts = warm_snap[:, T - 1].copy()
+    rest = [x for x in perm if x not in set(int(v) for v in starts)][:B * T]
+    table = np.array(rest, dtype=np.int32).reshape(B, T)
+    assert kda.kda_check_slots(m.gpu, starts, table.reshape(-1)) == kda.KDA_OK
+    out, ref = m.verify(starts, table, T, _tokens(13, 2, B * T, H, D, act))
+    assert hp.block_rel_err(hp.f64(out), ref, 1) <= hp.OUT_TOL_BF16
+    for s in table.reshape(-1):
+        assert m.state_err(int(s)) <= hp.STATE_TOL
+        assert m.tail_equal(int(s))
+
+
 def test_verify_snapshots_equal_decode_steps_bitexact():
     """Snapshot t of one verify launch equals t + 1 decode launches, bit for
     bit (state, tail and outputs)."""
