@@ -21,7 +21,9 @@
  * Conventions shared by every entry point
  *   - Device memory is owned by the caller: the pool buffer, inputs, outputs
  *     and workspaces are plain device pointers.  The library allocates no
- *     device memory.  A pool handle owns host metadata only.
+ *     device memory at run time (the no-allocation prefill's fixed scratch is
+ *     a static array of the module image).  A pool handle owns host metadata
+ *     only; a prefix cache handle owns host memory only.
  *   - Calls that take a stream are asynchronous on that stream.  A host-side
  *     argument error returns a status synchronously and enqueues nothing.
  *   - A fault found on the device (a slot index out of range) sets a bit of
