@@ -87,7 +87,7 @@ def args_():
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
     ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "decode_b1_l2_flushed", "prefill", "mixed",
-                                       "mma_rates"], default=None,
+                                       "next_rows", "mma_rates"], default=None,
                     help="run one secondary case alone (for profiling) and print its numbers; mma_rates times "
                          "the prefill's tensor-core MMA groups in a separately built timing library")
     ap.add_argument("--prefill-tokens", type=int, default=None,
@@ -203,6 +203,8 @@ def run_ours(a, rank, world, local):
             res = mma_rates(kbuild, kda, dev, tf_peak, peak_kind, L=a.prefill_tokens or 8192)
         elif a.only == "prefill":
             res = prefill_case(kda, dev, iters=a.steps, warmup=a.warmup, L=a.prefill_tokens)
+        elif a.only == "next_rows":
+            res = next_rows_case(kda, dev, iters=a.steps)
         elif a.only == "mixed":
             res = mixed_case(kda, dev, iters=a.steps, warmup=a.warmup)
         else:
@@ -335,7 +337,8 @@ def run_ours(a, rank, world, local):
     if not a.no_secondary:
         sec = secondary(kda, dev, hbm_peak, peak_kind)
         for name, fn in (("prefill", lambda: prefill_case(kda, dev, iters=3, warmup=1)),
-                         ("mixed", lambda: mixed_case(kda, dev, iters=3, warmup=1))):
+                         ("mixed", lambda: mixed_case(kda, dev, iters=3, warmup=1)),
+                         ("next_rows", lambda: next_rows_case(kda, dev))):
             try:
                 sec[name] = fn()
             except Exception as e:  # reported, not hidden: the line says why the entry is absent
@@ -453,6 +456,117 @@ def prefill_case(kda, dev, iters=3, warmup=1, L=None):
                                "over the whole call; bench.py --only mma_rates gives each MMA group's rate "
                                "while it runs"},
             "l2": "inputs (3.2 GB) and workspace exceed L2; not flushed between calls"}
+
+
+def _event_us(stream, fn, iters):
+    """Mean device time of fn() over iters calls, CUDA events on `stream`."""
+    ts = []
+    for _ in range(iters):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        ts.append(s.elapsed_time(e) * 1e3)
+    return float(np.mean(ts))
+
+
+def next_rows_case(kda, dev, iters=20):
+    """The widened rows, each measured: (1) prefill with device-built
+    metadata in a CUDA graph against the host-built tables, for 1 and 64
+    short sequences; (2) the prefix cache: host planning time for a 32K-token
+    prompt, and the GPU time of resuming from a saved prefix (slot copy plus
+    the 64-token tail) against prefilling the whole prompt; (3) one slot's
+    state export / import through pinned host memory."""
+    wl = I.PREFILL_32K
+    H, D, act = wl.H, wl.dk, wl.act
+    w_dev = {k: v.to(dev) for k, v in wl.weights().items()}
+    w = kda.make_weights(w_dev["conv_w"], w_dev["norm_w"], wl.eps_l2, wl.eps_rms)
+    pool = kda.StatePool(160, H, D, D, act)
+    stream = torch.cuda.Stream(device=dev)
+    res = {}
+    # (1) metadata: N sequences of 64 tokens each
+    meta = {}
+    for N in (1, 64):
+        L = 64 * N
+        toks = {k: v.to(dev) for k, v in wl.tokens(400, L).items()}
+        out = torch.empty(L, H, D, dtype=act, device=dev)
+        io = kda.make_io(toks, out)
+        cu = np.arange(N + 1, dtype=np.int32) * 64
+        slots, has = list(range(N)), [1] * N
+        ws_h = torch.empty(kda.kda_prefill_workspace_bytes(pool, cu), dtype=torch.uint8, device=dev)
+        cu_d = torch.tensor(cu, device=dev)
+        sl_d = torch.tensor(slots, dtype=torch.int32, device=dev)
+        hi_d = torch.tensor(has, dtype=torch.uint8, device=dev)
+        ws_d = torch.empty(kda.kda_prefill_workspace_bytes_bound(pool, N, L, 0), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                kda.kda_prefill_chunked(pool, w, io, cu, slots, has, 64, (), ws_h, stream)
+                kda.kda_prefill_chunked_dev(pool, w, io, cu_d, sl_d, hi_d, L, None, ws_d, stream=stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            kda.kda_prefill_chunked_dev(pool, w, io, cu_d, sl_d, hi_d, L, None, ws_d, stream=stream)
+        host_us = _event_us(stream, lambda: kda.kda_prefill_chunked(pool, w, io, cu, slots, has, 64, (), ws_h, stream),
+                            iters)
+        def replay():
+            with torch.cuda.stream(stream):  # replay() launches on the current stream
+                graph.replay()
+
+        dev_us = _event_us(stream, replay, iters)
+        meta[f"n{N}_x64_tokens"] = {"host_tables_us": round(host_us, 2), "device_tables_graph_us": round(dev_us, 2)}
+        del graph
+    res["device_metadata"] = meta
+    # (2) prefix cache: a 32768-token prompt whose first 32704 tokens are saved
+    L = wl.extra["L"]
+    ids = [int(x) for x in I.integers(wl.seed, 7, 0, 1 << 30, L)]
+    cache = kda.PrefixCache(64, [100], 1000)
+    toks = {k: v.to(dev) for k, v in wl.tokens(300, L).items()}
+    out = torch.empty(L, H, D, dtype=act, device=dev)
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(pool, [0, L]), dtype=torch.uint8, device=dev)
+
+    def full(reqs=()):
+        kda.kda_prefill_chunked(pool, w, kda.make_io(toks, out), [0, L], [101], [0], 64, list(reqs), ws, stream)
+
+    # a prompt of a whole number of blocks: its second plan admits the whole
+    # prompt, which leaves no token to compute; the third admits one block
+    # less, saved by that plan's prefill, and later plans reuse it
+    plans = [cache.plan(ids) for _ in range(3)]
+    _, _, admit_pos, admit_slot = plans[-1]
+    with torch.cuda.stream(stream):
+        full([(0, admit_pos, admit_slot)])
+    ids_t = torch.tensor(ids, dtype=torch.int32)  # the token ids as one int32 array, as a server holds them
+    t0 = time.perf_counter()
+    n_plan = 20
+    for _ in range(n_plan):
+        hit, hit_slot, _, _ = cache.plan(ids_t)
+    plan_us = (time.perf_counter() - t0) / n_plan * 1e6
+    assert hit == admit_pos and hit_slot == admit_slot
+    tail = {k: v[hit:].contiguous() for k, v in toks.items()}
+    out_t = out[hit:]
+
+    def resumed():
+        kda.kda_state_checkpoint(pool, [hit_slot], [102], stream)
+        kda.kda_prefill_chunked(pool, w, kda.make_io(tail, out_t), [0, L - hit], [102], [1], 64, (), ws, stream)
+
+    with torch.cuda.stream(stream):
+        full()
+        resumed()
+    stream.synchronize()
+    res["prefix_cache"] = {"prompt_tokens": L, "reused_prefix_tokens": hit, "host_plan_us": round(plan_us, 1),
+                           "full_prefill_us": round(_event_us(stream, full, 3), 1),
+                           "copy_and_tail_prefill_us": round(_event_us(stream, resumed, iters), 1)}
+    # (3) state export / import of one slot (state + conv tail) through pinned memory
+    nb = kda.kda_state_slot_bytes(pool)
+    host = torch.empty(nb, dtype=torch.uint8).pin_memory()
+    ex_us = _event_us(stream, lambda: kda.kda_state_export(pool, 3, host, stream), iters)
+    im_us = _event_us(stream, lambda: kda.kda_state_import(pool, 4, host, stream), iters)
+    res["state_transfer"] = {"slot_bytes": nb, "export_us": round(ex_us, 1), "import_us": round(im_us, 1),
+                             "export_gbs": round(nb / (ex_us * 1e-6) / 1e9, 1),
+                             "import_gbs": round(nb / (im_us * 1e-6) / 1e9, 1)}
+    st, flags = kda.kda_poll_device_error(pool, stream)
+    assert st == 0, f"device error word {flags:#x}"
+    return res
 
 
 def mixed_case(kda, dev, iters=3, warmup=1):

@@ -20,10 +20,11 @@
 
 #include <cstdint>
 #include <cstring>
+#include <iterator>
+#include <list>
 #include <new>
 #include <set>
 #include <unordered_map>
-#include <utility>
 #include <vector>
 
 #include "kda.h"
@@ -33,8 +34,9 @@ namespace {
 struct Entry {
     int32_t hits = 0;
     int32_t slot = -1;  // -1: tracked, not saved
-    uint64_t stamp = 0;
-    std::vector<int32_t> tokens;  // the prefix, while saved
+    uint64_t stamp = 0;  // the count clock at its last count
+    std::list<uint64_t>::iterator pos;  // its node in the saved or the unsaved recency list
+    std::vector<int32_t> tokens;        // the prefix, while saved
 };
 
 // splitmix64's output function (Steele, Lea, Flood: "Fast splittable
@@ -47,25 +49,51 @@ inline uint64_t mix64(uint64_t z) {
 
 }  // namespace
 
+// Recency: each prefix key sits in one of two lists (saved, unsaved), least
+// recently counted first; counting a prefix splices its node to the back, so
+// the order is the order of the last counts and no touch allocates.
 struct kda_prefix_cache {
     int32_t block = 0, max_tracked = 0;
     std::set<int32_t> free_slots;
     std::unordered_map<uint64_t, Entry> map;
-    std::set<std::pair<uint64_t, uint64_t>> unsaved, saved;  // (stamp, key), oldest first
+    std::list<uint64_t> unsaved, saved;
     uint64_t clock = 0;
     kda_prefix_cache_stats stats{};
 
-    // keys[i] = hash of the first i blocks, i = 1 .. n / block
+    // Moves entry e (key k) from one list to the other, at its place by last
+    // count (a scan from the back; admissions, evictions and forgets only).
+    void move_entry(Entry &e, std::list<uint64_t> &from, std::list<uint64_t> &to) {
+        auto at = to.end();
+        while (at != to.begin()) {
+            auto prev = std::prev(at);
+            if (map.at(*prev).stamp < e.stamp) break;
+            at = prev;
+        }
+        to.splice(at, from, e.pos);
+    }
+
+    // keys[i] = hash of the first i blocks, i = 1 .. n / block.  A block's
+    // tokens go through four independent mixing chains (token t into chain
+    // t % 4; block is a multiple of 64), folded into the running hash at the
+    // block's end: four times the instruction-level parallelism of one chain.
     void keys_of(const int32_t *tok, int32_t n, std::vector<uint64_t> &keys) const {
         const int32_t nb = n / block;
         keys.assign(size_t(nb) + 1, 0);
         uint64_t h = 0x6a09e667f3bcc909ull;
         for (int32_t i = 1; i <= nb; ++i) {
-            for (int32_t t = (i - 1) * block; t < i * block; ++t) h = mix64(h ^ uint64_t(uint32_t(tok[t])));
+            uint64_t a0 = h, a1 = h ^ 0xbb67ae8584caa73bull, a2 = h ^ 0x3c6ef372fe94f82bull, a3 = h ^ 0xa54ff53a5f1d36f1ull;
+            const int32_t *b = tok + size_t(i - 1) * size_t(block);
+            for (int32_t t = 0; t < block; t += 4) {
+                a0 = mix64(a0 ^ uint64_t(uint32_t(b[t])));
+                a1 = mix64(a1 ^ uint64_t(uint32_t(b[t + 1])));
+                a2 = mix64(a2 ^ uint64_t(uint32_t(b[t + 2])));
+                a3 = mix64(a3 ^ uint64_t(uint32_t(b[t + 3])));
+            }
+            h = mix64(a0 ^ ((a1 << 16) | (a1 >> 48)) ^ ((a2 << 32) | (a2 >> 32)) ^ ((a3 << 48) | (a3 >> 16)));
             keys[size_t(i)] = mix64(h + uint64_t(i));
         }
     }
-    std::set<std::pair<uint64_t, uint64_t>> &set_of(const Entry &e) { return e.slot >= 0 ? saved : unsaved; }
+    std::list<uint64_t> &list_of(const Entry &e) { return e.slot >= 0 ? saved : unsaved; }
 
     void plan(const int32_t *tok, int32_t n, kda_prefix_plan *out) {
         const int32_t B = block, nb = n / B, cap = n > 0 ? (n - 1) / B : 0;
@@ -84,10 +112,14 @@ struct kda_prefix_cache {
             const uint64_t k = keys[size_t(i)];
             auto ins = map.try_emplace(k);
             Entry &e = ins.first->second;
-            if (!ins.second) set_of(e).erase({e.stamp, k});
+            std::list<uint64_t> &l = list_of(e);
+            if (ins.second) {
+                e.pos = l.insert(l.end(), k);
+            } else {
+                l.splice(l.end(), l, e.pos);
+            }
             e.hits += 1;
             e.stamp = ++clock;
-            set_of(e).insert({e.stamp, k});
         }
         int32_t admit = 0, slot = -1;
         for (int32_t i = nb; i > hit; --i) {
@@ -104,33 +136,29 @@ struct kda_prefix_cache {
             } else {
                 const uint64_t keep = hit ? keys[size_t(hit)] : 0;
                 for (auto it = saved.begin(); it != saved.end(); ++it) {
-                    if (hit && it->second == keep) continue;
-                    Entry &v = map.at(it->second);
+                    if (hit && *it == keep) continue;
+                    Entry &v = map.at(*it);
                     slot = v.slot;
-                    const std::pair<uint64_t, uint64_t> sk = *it;
-                    saved.erase(it);
                     v.slot = -1;
                     std::vector<int32_t>().swap(v.tokens);
-                    unsaved.insert(sk);
+                    move_entry(v, saved, unsaved);
                     stats.evictions += 1;
                     break;
                 }
             }
             if (slot >= 0) {
-                const uint64_t k = keys[size_t(admit)];
-                Entry &e = map.at(k);
-                unsaved.erase({e.stamp, k});
-                e.slot = slot;
+                Entry &e = map.at(keys[size_t(admit)]);
                 e.tokens.assign(tok, tok + size_t(admit) * size_t(B));
-                saved.insert({e.stamp, k});
+                e.slot = slot;
+                move_entry(e, unsaved, saved);
                 stats.admissions += 1;
             } else {
                 admit = 0;
             }
         }
         while (unsaved.size() > size_t(max_tracked)) {
-            map.erase(unsaved.begin()->second);
-            unsaved.erase(unsaved.begin());
+            map.erase(unsaved.front());
+            unsaved.pop_front();
         }
         stats.plans += 1;
         if (hit) stats.hits += 1;
@@ -182,17 +210,16 @@ kda_status kda_prefix_cache_plan(kda_prefix_cache *cache, const int32_t *tokens,
 kda_status kda_prefix_cache_forget(kda_prefix_cache *cache, int32_t slot) {
     if (!cache) return KDA_ERR_INVALID_ARG;
     for (auto it = cache->saved.begin(); it != cache->saved.end(); ++it) {
-        Entry &e = cache->map.at(it->second);
+        Entry &e = cache->map.at(*it);
         if (e.slot != slot) continue;
         try {
-            cache->unsaved.insert(*it);
             cache->free_slots.insert(slot);
         } catch (const std::bad_alloc &) {
             return KDA_ERR_HOST_MEMORY;
         }
-        cache->saved.erase(it);
         e.slot = -1;
         std::vector<int32_t>().swap(e.tokens);
+        cache->move_entry(e, cache->saved, cache->unsaved);
         return KDA_OK;  // the tracked bound applies again at the next plan
     }
     return KDA_ERR_INVALID_ARG;
@@ -210,8 +237,8 @@ kda_status kda_prefix_cache_get_stats(const kda_prefix_cache *cache, kda_prefix_
 int32_t kda_prefix_cache_saved(const kda_prefix_cache *cache, int32_t *lens, int32_t *slots, int32_t cap) {
     if (!cache || cap < 0 || (cap > 0 && (!lens || !slots))) return -1;
     int32_t n = 0;
-    for (const auto &sk : cache->saved) {
-        const Entry &e = cache->map.at(sk.second);
+    for (const uint64_t k : cache->saved) {
+        const Entry &e = cache->map.at(k);
         if (n < cap) {
             lens[n] = int32_t(e.tokens.size());
             slots[n] = e.slot;
