@@ -107,6 +107,29 @@ def test_verify_draft_counts_match_oracle(T):
         assert m.tail_equal(int(s))
 
 
+@pytest.mark.parametrize("D", [32, 64])
+@pytest.mark.parametrize("act", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_verify_other_head_sizes_match_oracle(D, act):
+    """Verify (T = 5 drafts, 4 sequences, H = 3) at the smaller head sizes the
+    step kernel is built for, in both activation dtypes."""
+    H, B, T = 3, 4, 5
+    ns = B * T + B
+    m = Mirror(ns, H, D, act, _weights(17, H, D, act))
+    perm = [int(x) for x in I.permutation(17, D, ns)]
+    ins, table = perm[:B], np.array(perm[B:B + B * T], dtype=np.int32).reshape(B, T)
+    m.verify(ins, table, T, _tokens(17, 1, B * T, H, D, act))  # from zero slots
+    starts = table[:, T - 1].copy()  # each sequence continues from its last snapshot, which is also its snapshot 0
+    rest = [x for x in perm if x not in set(int(v) for v in starts)]
+    table2 = np.array([[int(starts[b])] + rest[b * (T - 1):(b + 1) * (T - 1)] for b in range(B)], dtype=np.int32)
+    assert kda.kda_check_slots(m.gpu, starts, table2.reshape(-1)) == kda.KDA_OK
+    out, ref = m.verify(starts, table2, T, _tokens(17, 2, B * T, H, D, act))
+    tol = hp.out_tol(act)
+    assert hp.block_rel_err(hp.f64(out), ref, 1) <= tol
+    for s in table2.reshape(-1):
+        assert m.state_err(int(s)) <= hp.STATE_TOL
+        assert m.tail_equal(int(s))
+
+
 def test_verify_snapshots_equal_decode_steps_bitexact():
     """Snapshot t of one verify launch equals t + 1 decode launches, bit for
     bit (state, tail and outputs)."""
