@@ -189,18 +189,20 @@ __device__ __forceinline__ float4 act4<__nv_bfloat16>(const __nv_bfloat16 *p) {
 // ln(alpha) of 8 values.  A positive normal bf16 value is 2^e (1 + m/128):
 // its log is e ln 2 + ln(1 + m/128), the second term from a 128-entry table
 // (lnm).  When any lane of the warp holds a zero, subnormal, negative or
-// non-finite value, the whole warp takes logf for these 8 (a warp-uniform
+// non-finite value among its n_valid leading ones (the tokens before the
+// segment end, so that nothing past it can change a token's bits), the
+// whole warp takes logf for these 8 (a warp-uniform
 // branch keeps logf out of the common path); fp32 values always use logf.
-__device__ __forceinline__ void log_alpha8(const float (&a)[8], const float *, float (&l)[8]) {
+__device__ __forceinline__ void log_alpha8(const float (&a)[8], const float *, int, float (&l)[8]) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) l[e] = logf(a[e]);
 }
-__device__ __forceinline__ void log_alpha8(const __nv_bfloat16 (&a)[8], const float *lnm, float (&l)[8]) {
-    bool normal = true;
+__device__ __forceinline__ void log_alpha8(const __nv_bfloat16 (&a)[8], const float *lnm, int n_valid, float (&l)[8]) {
+    bool normal = true;  // only the n_valid leading values (tokens before the segment end) decide the path
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const uint32_t b = __bfloat16_as_ushort(a[e]), ex = (b >> 7) & 0xFFu;
-        normal = normal && (b >> 15) == 0 && ex != 0 && ex != 0xFFu;
+        normal = normal && (e >= n_valid || ((b >> 15) == 0 && ex != 0 && ex != 0xFFu));
     }
     if (__all_sync(0xffffffffu, normal)) {
 #pragma unroll
@@ -567,7 +569,8 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
         for (int e = 0; e < CH / 2; ++e) av[e] = ra[(t0 + e) * D + gi];
 #pragma unroll
         for (int b = 0; b < CH / 2; b += 8)
-            log_alpha8(*reinterpret_cast<const Act(*)[8]>(av + b), cref, *reinterpret_cast<float(*)[8]>(lg + b));
+            log_alpha8(*reinterpret_cast<const Act(*)[8]>(av + b), cref, cm.len - (t0 + b),
+                       *reinterpret_cast<float(*)[8]>(lg + b));
         float G = 0.f;
 #pragma unroll
         for (int e = 0; e < CH / 2; ++e) {

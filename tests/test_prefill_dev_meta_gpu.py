@@ -155,3 +155,37 @@ def test_device_metadata_host_errors():
         kda.kda_prefill_chunked_dev(pa, wk, kda.make_io(inp, out), cu, sl, hi, -1, None, small)
     assert e.value.status == kda.KDA_ERR_INVALID_ARG
     assert kda.kda_poll_device_error(pa) == (kda.KDA_OK, 0)
+
+
+@pytest.mark.parametrize("seed", [101, 202, 303])
+def test_random_metadata_device_equals_host_bitexact(seed):
+    """Seeded random batches: 1..9 sequences of 0..300 tokens, shuffled slots,
+    random resume flags and checkpoint requests at random chunk ends and
+    sequence ends.  Device-built tables must give the host-built tables'
+    outputs, states and tails bit for bit."""
+    rng = np.random.default_rng(seed)
+    N = int(rng.integers(1, 10))
+    lens = [int(x) for x in rng.integers(0, 301, N)]
+    order = rng.permutation(32)
+    slots = [int(x) for x in order[:N]]
+    has_init = [int(x) for x in rng.integers(0, 2, N)]
+    free = [int(x) for x in order[N:]]
+    reqs = []
+    for n, L in enumerate(lens):
+        ends = sorted({p for p in range(64, L, 64)} | ({L} if L else set()))
+        for pos in ends:
+            if free and rng.random() < 0.4:
+                reqs.append((n, pos, free.pop()))
+    H, wk, (pa, pb), inp, n_tok, max_tokens = _setup(torch.bfloat16, seed, lens)
+    real = {k: v[:n_tok].contiguous() for k, v in inp.items()}
+    out_a = torch.full((max(n_tok, 1), H, D), 7.0, dtype=torch.bfloat16, device="cuda")[:n_tok]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ws = torch.empty(max(kda.kda_prefill_workspace_bytes(pa, cu), 256), dtype=torch.uint8, device="cuda")
+    kda.kda_prefill_chunked(pa, wk, kda.make_io(real, out_a), cu, slots, has_init, 64, reqs, ws)
+    out_b = torch.full((max_tokens, H, D), 7.0, dtype=torch.bfloat16, device="cuda")
+    _run_dev(pb, wk, inp, lens, slots, has_init, reqs, max_tokens, out_b)
+    torch.cuda.synchronize()
+    assert kda.kda_poll_device_error(pb) == (kda.KDA_OK, 0)
+    assert torch.equal(out_b[:n_tok], out_a)
+    assert torch.all(out_b[n_tok:] == 7.0)
+    assert torch.equal(pb.states(), pa.states()) and torch.equal(pb.tails(), pa.tails())

@@ -172,3 +172,23 @@ def test_prefill_across_chunk_windows_matches_oracle():
     out = prefill_gpu(m, hp.to_device(inp), lens, [0, 1, 2], [0, 0, 0], reqs)
     ref = prefill_oracle(m, inp, lens, [0, 1, 2], [0, 0, 0], reqs)
     _check(m, out, ref, [0, 1, 2], reqs)
+
+
+def test_prefill_results_do_not_depend_on_batch_composition():
+    """A sequence prefilled alone and inside a batch (between sequences whose
+    lengths put its chunk ends mid-group) gives the same outputs, state and
+    tail bit for bit: nothing past a segment's end reaches its tokens."""
+    H, act = 2, torch.bfloat16
+    m = Mirror(8, H, D, act, I.layer_weights(53, H, D, D, 4, act))
+    X = I.token_inputs(53, 0, 100, H, D, D, 2.0, act)
+    Y = I.token_inputs(53, 1, 37, H, D, D, 2.0, act)
+    Z = I.token_inputs(53, 2, 50, H, D, D, 2.0, act)
+    Z["alpha"][:5].zero_()  # zero and tiny alphas right after X's end
+    Z["alpha"][5:9] = 1e-40
+    alone = prefill_gpu(m, hp.to_device(X), [100], [0], [0])
+    batch = {k: torch.cat([Y[k], X[k], Z[k]]) for k in X}
+    out = prefill_gpu(m, hp.to_device(batch), [37, 100, 50], [1, 2, 3], [0, 0, 0])
+    torch.cuda.synchronize()
+    assert torch.equal(out[37:137], alone)
+    assert torch.equal(m.gpu.states()[2], m.gpu.states()[0])
+    assert torch.equal(m.gpu.tails()[2], m.gpu.tails()[0])
