@@ -393,16 +393,51 @@ def kda_poll_device_error(pool: StatePool, stream=None) -> tuple[int, int]:
     return st, int(flags.value)
 
 
+def kda_prefix_cache_create(block: int, slots, max_tracked: int) -> ctypes.c_void_p:
+    ts, ps = _host_i32(slots)
+    h = ctypes.c_void_p()
+    _check(lib().kda_prefix_cache_create(int(block), ps, int(ts.numel()), int(max_tracked), ctypes.byref(h)),
+           "kda_prefix_cache_create")
+    return h
+
+
+def kda_prefix_cache_destroy(handle: ctypes.c_void_p) -> None:
+    lib().kda_prefix_cache_destroy(handle)
+
+
+def kda_prefix_cache_plan(handle: ctypes.c_void_p, tokens) -> tuple[int, int, int, int]:
+    """(hit_len, hit_slot, admit_pos, admit_slot) for a prompt of token ids."""
+    t, pt = _host_i32(tokens)
+    out = kda_prefix_plan()
+    _check(lib().kda_prefix_cache_plan(handle, pt, int(t.numel()), ctypes.byref(out)), "kda_prefix_cache_plan")
+    return out.hit_len, out.hit_slot, out.admit_pos, out.admit_slot
+
+
+def kda_prefix_cache_forget(handle: ctypes.c_void_p, slot: int) -> None:
+    _check(lib().kda_prefix_cache_forget(handle, int(slot)), "kda_prefix_cache_forget")
+
+
+def kda_prefix_cache_get_stats(handle: ctypes.c_void_p) -> dict:
+    st = kda_prefix_cache_stats()
+    _check(lib().kda_prefix_cache_get_stats(handle, ctypes.byref(st)), "kda_prefix_cache_get_stats")
+    return {n: getattr(st, n) for n, _ in kda_prefix_cache_stats._fields_}
+
+
+def kda_prefix_cache_saved(handle: ctypes.c_void_p) -> dict:
+    """{slot: prefix length} of the saved prefixes."""
+    n = lib().kda_prefix_cache_saved(handle, None, None, 0)
+    lens = (ctypes.c_int32 * max(n, 1))()
+    slots = (ctypes.c_int32 * max(n, 1))()
+    m = lib().kda_prefix_cache_saved(handle, lens, slots, n)
+    return {int(slots[i]): int(lens[i]) for i in range(m)}
+
+
 class PrefixCache:
-    """Prefix-state cache with second-hit admission (host only): see
-    kda_prefix_cache_plan in include/kda.h."""
+    """Owner of a kda_prefix_cache handle (destroyed with the object); the
+    methods are the kda_prefix_cache_* functions above."""
 
     def __init__(self, block: int, slots, max_tracked: int):
-        ts, ps = _host_i32(slots)
-        h = ctypes.c_void_p()
-        _check(lib().kda_prefix_cache_create(int(block), ps, int(ts.numel()), int(max_tracked), ctypes.byref(h)),
-               "kda_prefix_cache_create")
-        self.handle = h
+        self.handle = kda_prefix_cache_create(block, slots, max_tracked)
         self.block = int(block)
 
     def __del__(self):
@@ -412,24 +447,13 @@ class PrefixCache:
             self.handle = None
 
     def plan(self, tokens) -> tuple[int, int, int, int]:
-        """(hit_len, hit_slot, admit_pos, admit_slot) for a prompt of token ids."""
-        t, pt = _host_i32(tokens)
-        out = kda_prefix_plan()
-        _check(lib().kda_prefix_cache_plan(self.handle, pt, int(t.numel()), ctypes.byref(out)), "kda_prefix_cache_plan")
-        return out.hit_len, out.hit_slot, out.admit_pos, out.admit_slot
+        return kda_prefix_cache_plan(self.handle, tokens)
 
     def forget(self, slot: int) -> None:
-        _check(lib().kda_prefix_cache_forget(self.handle, int(slot)), "kda_prefix_cache_forget")
+        kda_prefix_cache_forget(self.handle, slot)
 
     def stats(self) -> dict:
-        st = kda_prefix_cache_stats()
-        _check(lib().kda_prefix_cache_get_stats(self.handle, ctypes.byref(st)), "kda_prefix_cache_get_stats")
-        return {n: getattr(st, n) for n, _ in kda_prefix_cache_stats._fields_}
+        return kda_prefix_cache_get_stats(self.handle)
 
     def saved(self) -> dict:
-        """{slot: prefix length} of the saved prefixes."""
-        n = lib().kda_prefix_cache_saved(self.handle, None, None, 0)
-        lens = (ctypes.c_int32 * max(n, 1))()
-        slots = (ctypes.c_int32 * max(n, 1))()
-        m = lib().kda_prefix_cache_saved(self.handle, lens, slots, n)
-        return {int(slots[i]): int(lens[i]) for i in range(m)}
+        return kda_prefix_cache_saved(self.handle)

@@ -84,3 +84,9 @@ def test_binding_status_checks_name_their_entry_point():
     assert calls
     for c in calls:
         assert len(c.args) == 2 and isinstance(c.args[1], ast.Constant), f"line {c.lineno}"
+
+
+def test_binding_has_a_function_per_entry_point():
+    """The binding is the C ABI under the same names."""
+    missing = [n for n in kda.EXPORTS if not callable(getattr(kda, n, None))]
+    assert not missing, missing
