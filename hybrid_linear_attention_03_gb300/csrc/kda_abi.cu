@@ -2,6 +2,8 @@
 // dispatch to the kernels.  Declarations and contracts are in include/kda.h.
 #include "kda_internal.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -9,6 +11,16 @@
 #include <vector>
 
 namespace {
+
+// An NVTX range over an entry point that enqueues device work, so a profiler
+// timeline shows the library's calls around their kernels (a no-op unless a
+// tool is attached).
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
 
 constexpr size_t kAlign = 256;
 constexpr size_t kHeaderBytes = 256;
@@ -167,11 +179,13 @@ static kda_status run_step(kda_pool *pool, const kda_weights *w, const kda_io *i
 
 kda_status kda_decode(kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *slots, int32_t B,
                       kda_stream_t stream) {
+    const CallRange range("kda_decode");
     return run_step(pool, w, io, slots, slots, B, 1, stream);
 }
 
 kda_status kda_verify(kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *in_slots,
                       const int32_t *snap_slots, int32_t B, int32_t T, kda_stream_t stream) {
+    const CallRange range("kda_verify");
     return run_step(pool, w, io, in_slots, snap_slots, B, T, stream);
 }
 
@@ -222,6 +236,7 @@ kda_status kda_prefill_chunked_dev(kda_pool *pool, const kda_weights *w, const k
                                    const int32_t *slots, const uint8_t *has_initial_state, int32_t N,
                                    int32_t max_tokens, int32_t chunk, const kda_ckpt_req *reqs, int32_t n_reqs,
                                    void *workspace, size_t workspace_bytes, kda_stream_t stream) {
+    const CallRange range("kda_prefill_chunked_dev");
     if (!pool || !valid_weights(w) || !valid_io(io) || N < 0 || n_reqs < 0 || max_tokens < 0 ||
         (n_reqs > 0 && !reqs) || (N > 0 && (!cu_seqlens || !slots || !has_initial_state)))
         return KDA_ERR_INVALID_ARG;
@@ -234,6 +249,7 @@ kda_status kda_prefill_chunked_noalloc(kda_pool *pool, const kda_weights *w, con
                                        const int32_t *cu_seqlens, const int32_t *slots,
                                        const uint8_t *has_initial_state, int32_t N, int32_t chunk,
                                        const kda_ckpt_req *reqs, int32_t n_reqs, kda_stream_t stream) {
+    const CallRange range("kda_prefill_chunked_noalloc");
     const kda_status st = check_prefill_args(pool, w, io, cu_seqlens, slots, has_initial_state, N, chunk, reqs, n_reqs);
     if (st != KDA_OK || N == 0) return st;
     return kda::launch_prefill_noalloc(pool, w, io, cu_seqlens, slots, has_initial_state, N, chunk, reqs, n_reqs,
@@ -244,6 +260,7 @@ kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, const kda_i
                                const int32_t *slots, const uint8_t *has_initial_state, int32_t N, int32_t chunk,
                                const kda_ckpt_req *reqs, int32_t n_reqs, void *workspace, size_t workspace_bytes,
                                kda_stream_t stream) {
+    const CallRange range("kda_prefill_chunked");
     if (!pool || !valid_weights(w) || !valid_io(io) || N < 0 || n_reqs < 0 || (n_reqs > 0 && !reqs) ||
         (N > 0 && (!cu_seqlens || !slots || !has_initial_state)))
         return KDA_ERR_INVALID_ARG;
@@ -274,6 +291,7 @@ kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, const kda_i
 
 kda_status kda_state_checkpoint(kda_pool *pool, const int32_t *src_slots, const int32_t *dst_slots, int32_t n,
                                 kda_stream_t stream) {
+    const CallRange range("kda_state_checkpoint");
     if (!pool || n < 0 || (n > 0 && (!src_slots || !dst_slots))) return KDA_ERR_INVALID_ARG;
     if (n == 0) return KDA_OK;
     const int32_t ns = pool->desc.num_slots;
@@ -313,10 +331,12 @@ static kda_status slot_transfer(kda_pool *pool, int32_t slot, void *host, size_t
 }
 
 kda_status kda_state_export(kda_pool *pool, int32_t slot, void *host, size_t bytes, kda_stream_t stream) {
+    const CallRange range("kda_state_export");
     return slot_transfer(pool, slot, host, bytes, true, stream);
 }
 
 kda_status kda_state_import(kda_pool *pool, int32_t slot, const void *host, size_t bytes, kda_stream_t stream) {
+    const CallRange range("kda_state_import");
     return slot_transfer(pool, slot, const_cast<void *>(host), bytes, false, stream);
 }
 
