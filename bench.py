@@ -102,6 +102,15 @@ def dist_env():
 
 # The layer has no exchange step: under torchrun every rank runs its own
 # replica of the workload, and the ranks meet only around the timed region.
+def settle(kda, stream, limit_s=300.0):
+    """Waits for the stream with the library's watchdog (a bench that stops
+    making progress fails with a message instead of hanging), then for the
+    whole device."""
+    if kda.kda_stream_wait(stream, limit_s) != kda.KDA_OK:
+        raise RuntimeError(f"bench: the timed stream had not finished after {limit_s:.0f} s")
+    torch.cuda.synchronize()
+
+
 def rank_barrier(world):
     if world > 1:
         torch.distributed.barrier()
@@ -274,7 +283,7 @@ def run_ours(a, rank, world, local):
     rank_barrier(world)
     torch.cuda.synchronize()
     evs = [one_step() for _ in range(a.steps)]
-    torch.cuda.synchronize()
+    settle(kda, stream)
     rank_barrier(world)
     ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs), world, dev)
     value = job_throughput(a.steps * n_steps, world, ms)
@@ -307,7 +316,7 @@ def run_ours(a, rank, world, local):
     torch.cuda.synchronize()
     rank_barrier(world)
     evs2 = [e2e_step() for _ in range(a.steps)]
-    torch.cuda.synchronize()
+    settle(kda, stream)
     rank_barrier(world)
     ms2 = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs2), world, dev)
     e2e_value = job_throughput(a.steps * n_steps, world, ms2)

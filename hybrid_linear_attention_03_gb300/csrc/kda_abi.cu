@@ -4,9 +4,11 @@
 
 #include <nvtx3/nvToolsExt.h>
 
+#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <thread>
 #include <unordered_map>
 #include <vector>
 
@@ -351,6 +353,23 @@ kda_status kda_poll_device_error(kda_pool *pool, kda_stream_t stream, uint32_t *
     return word ? KDA_ERR_DEVICE : KDA_OK;
 }
 
+kda_status kda_stream_wait(kda_stream_t stream, double timeout_s) {
+    if (!(timeout_s >= 0.0) || !std::isfinite(timeout_s)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        const cudaError_t q = cudaStreamQuery(s);
+        if (q == cudaSuccess) return KDA_OK;
+        if (q != cudaErrorNotReady) {
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+        if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > timeout_s)
+            return KDA_ERR_TIMEOUT;
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
+}
+
 const char *kda_status_string(kda_status s) {
     switch (s) {
         case KDA_OK: return "ok";
@@ -362,6 +381,7 @@ const char *kda_status_string(kda_status s) {
         case KDA_ERR_DEVICE: return "device error word set";
         case KDA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case KDA_ERR_HOST_MEMORY: return "host allocation failed";
+        case KDA_ERR_TIMEOUT: return "the stream had not finished within the time limit";
     }
     return "unknown status";
 }

@@ -26,6 +26,7 @@ KDA_ERR_CUDA = 5
 KDA_ERR_DEVICE = 6
 KDA_ERR_WORKSPACE = 7
 KDA_ERR_HOST_MEMORY = 8
+KDA_ERR_TIMEOUT = 9
 KDA_F32 = 0
 KDA_BF16 = 1
 KDA_DEVERR_SLOT_RANGE = 0x1
@@ -38,7 +39,7 @@ EXPORTS = ("kda_state_pool_bytes", "kda_state_pool_create", "kda_state_pool_dest
            "kda_state_checkpoint", "kda_poll_device_error", "kda_status_string", "kda_prefill_chunked_noalloc",
            "kda_state_slot_bytes", "kda_state_export", "kda_state_import", "kda_prefill_workspace_bytes_bound",
            "kda_prefill_chunked_dev", "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_plan",
-           "kda_prefix_cache_forget", "kda_prefix_cache_get_stats", "kda_prefix_cache_saved")
+           "kda_prefix_cache_forget", "kda_prefix_cache_get_stats", "kda_prefix_cache_saved", "kda_stream_wait")
 
 KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -146,10 +147,21 @@ def lib() -> ctypes.CDLL:
         L.kda_prefix_cache_get_stats.restype = i32
         L.kda_prefix_cache_saved.argtypes = [vp, vp, vp, i32]
         L.kda_prefix_cache_saved.restype = i32
+        L.kda_stream_wait.argtypes = [vp, ctypes.c_double]
+        L.kda_stream_wait.restype = i32
         L.kda_status_string.argtypes = [i32]
         L.kda_status_string.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
+
+
+def kda_stream_wait(stream=None, timeout_s: float = 60.0) -> int:
+    """Waits at most timeout_s for the stream's work; KDA_OK or KDA_ERR_TIMEOUT
+    (raises on any other status)."""
+    st = lib().kda_stream_wait(_stream(stream), float(timeout_s))
+    if st not in (KDA_OK, KDA_ERR_TIMEOUT):
+        raise KdaError(st, "kda_stream_wait")
+    return st
 
 
 def kda_status_string(status: int) -> str:

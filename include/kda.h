@@ -72,7 +72,8 @@ typedef enum {
     KDA_ERR_CUDA = 5,        /* a CUDA runtime call failed */
     KDA_ERR_DEVICE = 6,      /* the device error word was set (kda_poll_device_error) */
     KDA_ERR_WORKSPACE = 7,   /* workspace missing, misaligned or too small */
-    KDA_ERR_HOST_MEMORY = 8  /* a host allocation failed */
+    KDA_ERR_HOST_MEMORY = 8, /* a host allocation failed */
+    KDA_ERR_TIMEOUT = 9      /* kda_stream_wait: the stream's work had not finished in time */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -361,6 +362,15 @@ KDA_API int32_t kda_prefix_cache_saved(const kda_prefix_cache *cache, int32_t *l
 /* Waits for `stream`, reads the device error word into *flags (may be NULL)
  * and clears it.  Returns KDA_ERR_DEVICE if any bit was set, else KDA_OK. */
 KDA_API kda_status kda_poll_device_error(kda_pool *pool, kda_stream_t stream, uint32_t *flags);
+
+/* Host watchdog: waits for the work enqueued on `stream` (NULL: the legacy
+ * default stream) by polling it, for at most timeout_s seconds, instead of
+ * blocking without limit.  KDA_OK once it has finished; KDA_ERR_TIMEOUT if it
+ * has not (the work is still in flight and may yet finish; the caller
+ * decides); KDA_ERR_CUDA if the stream reports an error; KDA_ERR_INVALID_ARG
+ * for a negative or non-finite limit.  Every wait inside the kernels is
+ * bounded too, so a stream the library alone feeds always finishes. */
+KDA_API kda_status kda_stream_wait(kda_stream_t stream, double timeout_s);
 
 /* Static text for a status code. */
 KDA_API const char *kda_status_string(kda_status s);

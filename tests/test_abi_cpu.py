@@ -53,7 +53,7 @@ def test_pool_bytes_rejects_bad_descriptions(lib, bad):
 
 
 def test_status_strings(lib):
-    for code in range(9):
+    for code in range(10):
         s = kda.kda_status_string(code)
         assert s and s != "unknown status"
     assert kda.kda_status_string(99) == "unknown status"
@@ -90,3 +90,9 @@ def test_binding_has_a_function_per_entry_point():
     """The binding is the C ABI under the same names."""
     missing = [n for n in kda.EXPORTS if not callable(getattr(kda, n, None))]
     assert not missing, missing
+
+
+def test_stream_wait_rejects_bad_limits(lib):
+    # checked before any CUDA call
+    for bad in (-1.0, float("nan"), float("inf")):
+        assert lib.kda_stream_wait(None, bad) == kda.KDA_ERR_INVALID_ARG

@@ -192,3 +192,17 @@ def test_prefill_results_do_not_depend_on_batch_composition():
     assert torch.equal(out[37:137], alone)
     assert torch.equal(m.gpu.states()[2], m.gpu.states()[0])
     assert torch.equal(m.gpu.tails()[2], m.gpu.tails()[0])
+
+
+def test_stream_wait_reports_a_timeout_then_completion():
+    """The host watchdog returns KDA_ERR_TIMEOUT while a long prefill is still
+    in flight (a zero limit), then KDA_OK once it has finished."""
+    H, act, L = 64, torch.bfloat16, 8192
+    m = Mirror(2, H, D, act, I.layer_weights(59, H, D, D, 4, act))
+    inp = hp.to_device(I.token_inputs(59, 0, L, H, D, D, 2.0, act))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    prefill_gpu(m, inp, [L], [0], [0], stream=stream)
+    assert kda.kda_stream_wait(stream, 0.0) == kda.KDA_ERR_TIMEOUT
+    assert kda.kda_stream_wait(stream, 120.0) == kda.KDA_OK
+    assert kda.kda_poll_device_error(m.gpu, stream) == (kda.KDA_OK, 0)
