@@ -23,7 +23,12 @@
 // MMAs are M = 128 (the chunk-pair trick and transposed products below), with
 // operands in the 128-byte-swizzle K-major layout (kda_sm100.cuh).
 //
-// Kernels (one stream, in order):
+// Kernels (per window of chunks: intra on the caller's stream, then the
+// window's chain on a high-priority side stream and its out on a third, so
+// the chain and the norm of one window overlap intra of the next; the tails
+// run on the caller's stream after the join):
+//   meta   (device-built tables only, one CTA): sequence, chunk and
+//          checkpoint tables from device arrays.
 //   intra  (chunk, head): TMA loads the raw q, k, v, alpha tiles (with the
 //          3-token conv halo); conv + SiLU, L2 of q and k, G, beta in shared
 //          memory; [K exp(G-c); Q exp(G-c)] x (K exp(c-G))^T -> A, P (one
