@@ -63,6 +63,19 @@ def source_sha(paths):
     return h.hexdigest()[:16]
 
 
+PREFILL_SOURCES = ("hybrid_linear_attention_03_gb300/csrc/kda_prefill.cu",
+                   "hybrid_linear_attention_03_gb300/csrc/kda_sm100.cuh",
+                   "hybrid_linear_attention_03_gb300/csrc/kda_internal.h")
+# Algorithmic FLOP per (chunk, head) at C = 64, d_k = d_v = 128 (full-square products):
+# intra-chunk A, P, W, Ut (2 C^2 d each) and the triangular inverse (C^3 / 3);
+# chain W S, Q S, K^T U (2 C d^2 each) and P U (2 C^2 d).
+C_, D_ = 64, 128
+INTRA_FLOP_PER_CHUNK_HEAD = 4 * 2 * C_ * C_ * D_ + C_ ** 3 // 3
+CHAIN_FLOP_PER_CHUNK_HEAD = 3 * 2 * C_ * D_ * D_ + 2 * C_ * C_ * D_
+# Algorithmic HBM bytes per prefill token at H = 64, d = 128, bf16: q, k, v, alpha, gate in, beta in, y out
+PREFILL_BYTES_PER_TOKEN = 64 * (5 * 128 * 2 + 2 + 128 * 2)
+
+
 def profiled_traffic(profile):
     """DRAM bytes per launch that an ncu summary under profiles/ records for
     the step kernel, or None if the kernel's sources changed since."""
@@ -78,6 +91,23 @@ def profiled_traffic(profile):
     return int(tr.group(1))
 
 
+def profiled_prefill_traffic(profile):
+    """DRAM bytes per (chunk, head) that an ncu summary under profiles/
+    records for the intra-chunk kernel (measured on a small case; traffic
+    grows in proportion to the chunk-heads a launch processes), or None if
+    the prefill sources changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", profile)) as f:
+            text = f.read()
+    except OSError:
+        return None
+    sha = re.search(r"^source_sha256_16: ([0-9a-f]{16})", text, re.M)
+    tr = re.search(r"^traffic_bytes_per_chunk_head: (\d+)", text, re.M)
+    if not sha or not tr or sha.group(1) != source_sha(PREFILL_SOURCES):
+        return None
+    return int(tr.group(1))
+
+
 def args_():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -87,9 +117,8 @@ def args_():
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
     ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "decode_b1_l2_flushed", "prefill", "mixed",
-                                       "next_rows", "mma_rates"], default=None,
-                    help="run one secondary case alone (for profiling) and print its numbers; mma_rates times "
-                         "the prefill's tensor-core MMA groups in a separately built timing library")
+                                       "next_rows"], default=None,
+                    help="run one secondary case alone (for profiling) and print its numbers")
     ap.add_argument("--prefill-tokens", type=int, default=None,
                     help="with --only prefill: a shorter sequence of the same workload (small profiling case)")
     return ap.parse_args()
@@ -208,9 +237,7 @@ def run_ours(a, rank, world, local):
     hbm_peak, tf_peak, _, peak_kind = load_peaks()
     if a.only:
         kbuild.build()
-        if a.only == "mma_rates":
-            res = mma_rates(kbuild, kda, dev, tf_peak, peak_kind, L=a.prefill_tokens or 8192)
-        elif a.only == "prefill":
+        if a.only == "prefill":
             res = prefill_case(kda, dev, iters=a.steps, warmup=a.warmup, L=a.prefill_tokens)
         elif a.only == "next_rows":
             res = next_rows_case(kda, dev, iters=a.steps)
@@ -256,18 +283,29 @@ def run_ours(a, rank, world, local):
             kda.kda_decode(pool, w, ios[i], slot_t, 1)
         kda.kda_state_checkpoint(pool, [spare], [slot])
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(n_steps):
-            kda.kda_decode(pool, w, ios[i], slot_t, 1)
+    # The chain's inputs are staged before it runs, so no kernel of the chain
+    # writes a decode's inputs: the pool may let each launch fetch its inputs
+    # under the previous launch (KDA_POOL_OVERLAP_INPUTS).  The same chain in
+    # the default order (every read after the previous launch completes) is
+    # timed beside it.
+    graphs = {}
+    for name, flags in (("overlap_inputs", kda.KDA_POOL_OVERLAP_INPUTS), ("default_order", 0)):
+        kda.kda_state_pool_set_flags(pool, flags)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_steps):
+                kda.kda_decode(pool, w, ios[i], slot_t, 1)
+        graphs[name] = g
+    kda.kda_state_pool_set_flags(pool, 0)
+    graph = graphs["overlap_inputs"]
 
-    def one_step():
+    def one_step(g=None):
         with torch.cuda.stream(stream):
             kda.kda_state_checkpoint(pool, [spare], [slot])
             flush_l2(flush)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
-            graph.replay()
+            (g or graph).replay()
             e.record(stream)
         return s, e
 
@@ -287,6 +325,11 @@ def run_ours(a, rank, world, local):
     rank_barrier(world)
     ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs), world, dev)
     value = job_throughput(a.steps * n_steps, world, ms)
+    for _ in range(2):
+        one_step(graphs["default_order"])
+    evs_d = [one_step(graphs["default_order"]) for _ in range(a.steps)]
+    settle(kda, stream)
+    ms_d = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs_d), world, dev)
     bytes_b1 = step_bytes(H, D, 1, 1)
     launch_us = ms * 1e3 / (a.steps * n_steps)
     achieved = bytes_b1 / (launch_us * 1e-6) / 1e9
@@ -329,6 +372,8 @@ def run_ours(a, rank, world, local):
         "config": {"workload": wl.name, "batch": 1, "heads": H, "d_k": D, "d_v": D, "io_dtype": "bf16",
                    "state_dtype": "f32", "pool_slots": wl.num_slots, "warm_tokens": wl.extra["warm"],
                    "decode_steps_per_bench_step": n_steps, "cuda_graph": True,
+                   "launch_order": "KDA_POOL_OVERLAP_INPUTS (inputs staged before the chain; each launch fetches "
+                                   "them under the previous one)",
                    "l2": "flushed between timed steps (512 MiB written, then read); within a step the 4 MiB "
                          "state of the single sequence stays L2-resident across its 1000 chained decodes",
                    "parallelism": f"replicas x{world}"},
@@ -341,6 +386,11 @@ def run_ours(a, rank, world, local):
                              "launch is latency-bound; the HBM rooflines of this kernel are the batch-64 entries "
                              "under secondary"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "default_launch_order": {"value": round(job_throughput(a.steps * n_steps, world, ms_d), 1), "unit": UNIT,
+                                 "launch_us": round(ms_d * 1e3 / (a.steps * n_steps), 3),
+                                 "note": "the same chain with the pool's default launch order: each decode reads "
+                                         "its inputs only after the previous launch has completed (what a caller "
+                                         "whose inputs come from the kernel right before must use)"},
         "clocks": clk,
     }
     if not a.no_secondary:
@@ -449,22 +499,42 @@ def prefill_case(kda, dev, iters=3, warmup=1, L=None):
         e.synchronize()
         times.append(s.elapsed_time(e))
     ms = float(np.mean(times))
+    # one more call with the library's event profile: each kernel's device time
+    # as it ran in the windowed schedule (events on the stream it launches on)
+    kda.kda_profile_start(4096)
+    launch()
+    prof = kda.kda_profile_stop()
     st, flags = kda.kda_poll_device_error(pool)
     assert st == 0, f"device error word {flags:#x}"
-    # tensor-core work issued per (chunk, head): intra [A; P] 128x64x128 and W^T, Ut^T 2 x 128x64x64;
-    # chain 128x128x128 and 128x192x64; each a split product of three bf16 MMAs
-    chunk_heads = ((L + 63) // 64) * H
-    flop = chunk_heads * 2 * 3 * (128 * 64 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 128 + 128 * 192 * 64)
     _, tf_peak, _, peak_kind = load_peaks()
-    tflops = flop / (ms * 1e-3) / 1e12
-    return {"workload": wl.name if L == wl.extra["L"] else f"{wl.name} (first {L} tokens)", "tok_per_s": round(L / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
+    hbm_peak = load_peaks()[0]
+    chunk_heads = ((L + 63) // 64) * H
+    n_intra, intra_ms = prof["prefill_intra"]
+    intra_flop = chunk_heads * INTRA_FLOP_PER_CHUNK_HEAD
+    intra_tf = intra_flop / (intra_ms * 1e-3) / 1e12
+    tr = profiled_prefill_traffic("kda_prefill_intra_dram.md")
+    call_flop = chunk_heads * (INTRA_FLOP_PER_CHUNK_HEAD + CHAIN_FLOP_PER_CHUNK_HEAD)
+    call_bytes = L * PREFILL_BYTES_PER_TOKEN
+    return {"workload": wl.name if L == wl.extra["L"] else f"{wl.name} (first {L} tokens)",
+            "tok_per_s": round(L / (ms / 1e3), 1), "ms_per_call": round(ms, 3),
             "workspace_bytes": ws.numel(),
-            "tensor": {"issued_bf16_tflop_per_call": round(flop / 1e12, 4), "tflops": round(tflops, 1),
-                       "peak": tf_peak, "frac": round(tflops / tf_peak, 4), "peak_kind": peak_kind,
-                       "note": "issued bf16 MMA FLOP of the intra and chain kernels (three per split product) "
-                               "over the whole call; bench.py --only mma_rates gives each MMA group's rate "
-                               "while it runs"},
-            "l2": "inputs (3.2 GB) and workspace exceed L2; not flushed between calls"}
+            "kernels_ms_per_call": {k: round(v[1], 4) for k, v in prof.items() if k != "dropped" and v[0]},
+            "kernel_launches_per_call": {k: v[0] for k, v in prof.items() if k != "dropped" and v[0]},
+            "roofline": {"bound": "tensor", "kernel": "prefill_intra_kernel", "achieved": round(intra_tf, 2),
+                         "peak": tf_peak, "unit": "TFLOP/s", "frac": round(intra_tf / tf_peak, 4),
+                         "traffic": None if tr is None else tr * chunk_heads // max(n_intra, 1),
+                         "flop_per_launch": intra_flop // max(n_intra, 1),
+                         "launch_us": round(intra_ms * 1e3 / max(n_intra, 1), 2),
+                         "note": f"algorithmic intra-chunk FLOP (A, P, W, Ut and the triangular inverse: "
+                                 f"{INTRA_FLOP_PER_CHUNK_HEAD} per chunk-head) over the intra kernel's device time, "
+                                 f"CUDA events around each of its launches inside the call; peak = {peak_kind} "
+                                 f"dense bf16 (burst); traffic = ncu DRAM bytes per chunk-head of a small case x "
+                                 f"the chunk-heads of one launch"},
+            "whole_call": {"algorithmic_flop": call_flop, "tflops": round(call_flop / (ms * 1e-3) / 1e12, 2),
+                           "frac_bf16": round(call_flop / (ms * 1e-3) / 1e12 / tf_peak, 4),
+                           "algorithmic_bytes": call_bytes, "gbs": round(call_bytes / (ms * 1e-3) / 1e9, 1),
+                           "frac_hbm": round(call_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4)},
+            "l2": "inputs (3.2 GB) exceed L2; not flushed between calls"}
 
 
 def _event_us(stream, fn, iters):
@@ -523,7 +593,26 @@ def next_rows_case(kda, dev, iters=20):
                 graph.replay()
 
         dev_us = _event_us(stream, replay, iters)
-        meta[f"n{N}_x64_tokens"] = {"host_tables_us": round(host_us, 2), "device_tables_graph_us": round(dev_us, 2)}
+        # the metadata alone: the device builder kernel, against the host call's
+        # table build (host wall time of the call, launches included) and the
+        # device time of its tables' copies; library event profile
+        kda.kda_profile_start(1024)
+        for _ in range(iters):
+            kda.kda_prefill_chunked_dev(pool, w, io, cu_d, sl_d, hi_d, L, None, ws_d, stream=stream)
+        prof_dev = kda.kda_profile_stop()
+        kda.kda_profile_start(1024)
+        t0 = time.perf_counter()
+        for _ in range(iters):
+            kda.kda_prefill_chunked(pool, w, io, cu, slots, has, 64, (), ws_h, stream)
+        host_call_us = (time.perf_counter() - t0) / iters * 1e6
+        prof_host = kda.kda_profile_stop()
+        stream.synchronize()
+        meta[f"n{N}_x64_tokens"] = {
+            "host_tables_us": round(host_us, 2), "device_tables_graph_us": round(dev_us, 2),
+            "meta_kernel_us": round(prof_dev["prefill_meta"][1] * 1e3 / max(prof_dev["prefill_meta"][0], 1), 2),
+            "host_tables_copy_us": round(prof_host["prefill_meta"][1] * 1e3 / max(prof_host["prefill_meta"][0], 1),
+                                         2),
+            "host_call_wall_us": round(host_call_us, 2)}
         del graph
     res["device_metadata"] = meta
     # (2) prefix cache: a 32768-token prompt whose first 32704 tokens are saved
@@ -633,92 +722,74 @@ def mixed_case(kda, dev, iters=3, warmup=1):
 
 # ----------------------------------------------------------------------- oracle
 
-def mma_rates(kbuild, kda, dev, tf_peak, peak_kind, L=8192):
-    """Tensor-core rate of each prefill MMA group while it runs.  A timing build
-    of the library (-DKDA_MMA_TIMING) has thread 0 wait for each group right
-    after issuing it and accumulate clock64 cycles from the first issue to the
-    completion.  FLOP are the issued bf16 products (three per split product:
-    hi.hi + hi.lo + lo.hi); the rate is per SM at the SM clock sampled during
-    the run, compared with the measured dense bf16 peak per SM."""
-    import ctypes
-    from pathlib import Path
-
-    lib_path = kbuild.build_mma_timing()
-    kda._LIB_PATH = Path(lib_path)
-    kda._LIB = None
-    L_ = kda.lib()
-    L_.kda_mma_timing_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
-    wl = I.PREFILL_32K
-    H, D, act = wl.H, wl.dk, wl.act
-    w_dev = {k: v.to(dev) for k, v in wl.weights().items()}
-    w = kda.make_weights(w_dev["conv_w"], w_dev["norm_w"], wl.eps_l2, wl.eps_rms)
-    pool = kda.StatePool(4, H, D, D, act)
-    toks = {k: v.to(dev) for k, v in wl.tokens(300, L).items()}
-    out = torch.empty(L, H, D, dtype=act, device=dev)
-    ws = torch.empty(kda.kda_prefill_workspace_bytes(pool, [0, L]), dtype=torch.uint8, device=dev)
-    io = kda.make_io(toks, out)
-    kda.kda_prefill_chunked(pool, w, io, [0, L], [0], [0], 64, (), ws)
-    torch.cuda.synchronize()
-    buf = (ctypes.c_ulonglong * 8)()
-    assert L_.kda_mma_timing_read(buf, 1) == 0
-    clocks = ClockSampler(dev.index or 0)
-    clocks.start()
-    time.sleep(0.25)
-    for _ in range(5):
-        kda.kda_prefill_chunked(pool, w, io, [0, L], [0], [0], 64, (), ws)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    assert L_.kda_mma_timing_read(buf, 1) == 0
-    mhz = float(clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0)
-    max_mhz = float(clk.get("sm_max_mhz") or mhz)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    peak_fpc = tf_peak * 1e12 / sms / (mhz * 1e6)  # measured peak, FLOP per cycle per SM at this clock
-    nominal_fpc = 2.25e15 / sms / (max_mhz * 1e6)  # nominal dense bf16 (2.25 PFLOP/s) at the maximum clock
-    groups = [("intra [A; P] = [K~; Q~] Kb^T", 0, 4, 3 * 128 * 64 * 128),
-              ("intra W^T and Ut^T", 1, 4, 2 * 3 * 128 * 64 * 64),
-              ("chain (W S | Q S)^T", 2, 5, 3 * 128 * 128 * 128),
-              ("chain (K^T U | P U)^T", 3, 5, 3 * 128 * 192 * 64)]
-    res = {"workload": f"prefill_l{L}_h{H}_d{D}_c64 (timing build)", "sm_mhz": mhz, "peak_tflops": tf_peak,
-           "peak_kind": peak_kind, "groups": {}}
-    for name, slot, cnt_slot, mac in groups:
-        n = max(int(buf[cnt_slot]), 1)
-        cyc = buf[slot] / n
-        fpc = 2 * mac / cyc
-        res["groups"][name] = {"count": int(buf[cnt_slot]), "cycles_issue_to_done": round(cyc, 1),
-                               "issued_flop": 2 * mac, "flop_per_cycle_per_sm": round(fpc, 1),
-                               "frac_of_peak": round(fpc / peak_fpc, 4),
-                               "frac_of_nominal": round(fpc / nominal_fpc, 4)}
-    res["clocks"] = clk
-    return res
-
-
-def oracle_decode_run(o, wl, w, tok, n):
-    """The CPU oracle over n chained decode tokens of the batch-1 sequence."""
+def oracle_warm_state(o, wl, w):
+    """The batch-1 sequence's state and conv tail after its 512 warm-up
+    tokens, by the oracle: the start state of the timed decode steps, as in
+    the GPU arm (which warms its slot with the same tokens)."""
     S = np.zeros((wl.H, wl.dk, wl.dv))
     tail = np.zeros((3, wl.H * (2 * wl.dk + wl.dv)))
+    warm = {k: v.double().numpy() for k, v in wl.tokens(0, wl.extra["warm"]).items()}
+    _, S, tail, _, _ = o.layer(warm, w, S, tail, eps_l2=wl.eps_l2, eps_rms=wl.eps_rms)
+    return S, tail
+
+
+def oracle_decode_run(o, wl, w, tok, n, start, n_threads=0):
+    """The CPU oracle over n chained decode tokens of the batch-1 sequence,
+    from the warm state `start`; returns the seconds it took."""
+    S, tail = start
     part = {k: v[:n] for k, v in tok.items()}
     t0 = time.perf_counter()
-    o.layer(part, w, S, tail, eps_l2=wl.eps_l2, eps_rms=wl.eps_rms)
+    o.layer(part, w, S, tail, eps_l2=wl.eps_l2, eps_rms=wl.eps_rms, n_threads=n_threads)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(sample_tokens=1000, min_s=10.0, max_s=30.0):
+def cpu_baseline(sample_tokens=1000, min_s=6.0, max_s=12.0):
+    """The oracle as it stands on the host cores: chained batch-1 decode on
+    all cores and on one thread (tok/s), and the 32K-token prefill's
+    sequential token loop on a sample of heads and tokens, scaled to 64
+    heads (tok/s).  A baseline, not the target."""
     from oracle import kda_oracle as ko
 
     o = ko.Oracle(ko.build())
     wl = I.DECODE_B1
     w = {k: v.double().numpy() for k, v in wl.weights().items()}
     tok = {k: v.double().numpy() for k, v in wl.tokens(100, sample_tokens).items()}
+    start = oracle_warm_state(o, wl, w)
     total, n, runs = 0.0, 0, 0
     while total < min_s and runs < 100:
-        total += oracle_decode_run(o, wl, w, tok, sample_tokens)
+        total += oracle_decode_run(o, wl, w, tok, sample_tokens, start)
         n += sample_tokens
         runs += 1
         if total > max_s:
             break
-    return {"value": round(n / total, 2), "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
-            "sample": f"{runs} x {sample_tokens} chained decode tokens of the batch-1 workload "
-                      f"(float64 token loop, OpenMP over the 64 heads)"}
+    one_n = 100
+    one_s = oracle_decode_run(o, wl, w, tok, one_n, start, n_threads=1)
+    # prefill: the token loop (the oracle's definition) over the first L_s tokens of
+    # H_s heads of the 32K-token workload; heads are independent, so the 64-head
+    # rate is the sampled rate x H_s / 64
+    pw = I.PREFILL_32K
+    H_s, L_s = 16, 1024
+    wp = {k: v.double().numpy() for k, v in pw.weights().items()}
+    heads = list(range(H_s))
+    chans = np.array([h * pw.dk + i for h in heads for i in range(pw.dk)] +
+                     [pw.H * pw.dk + h * pw.dk + i for h in heads for i in range(pw.dk)] +
+                     [2 * pw.H * pw.dk + h * pw.dv + j for h in heads for j in range(pw.dv)])
+    ptok = {k: v[:, :H_s].double().numpy() for k, v in pw.tokens(300, L_s).items()}
+    wps = {"conv_w": wp["conv_w"][chans], "norm_w": wp["norm_w"]}
+    t0 = time.perf_counter()
+    o.layer(ptok, wps, np.zeros((H_s, pw.dk, pw.dv)), np.zeros((3, H_s * (2 * pw.dk + pw.dv))),
+            eps_l2=pw.eps_l2, eps_rms=pw.eps_rms)
+    pf_s = time.perf_counter() - t0
+    cores = o.max_threads()
+    return {"value": round(n / total, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{runs} x {sample_tokens} chained decode tokens of the batch-1 workload from its 512-token "
+                      f"warm state (float64 token loop, OpenMP over the 64 heads)",
+            "one_thread": {"value": round(one_n / one_s, 2), "unit": UNIT, "cores": 1,
+                           "sample": f"{one_n} chained decode tokens, one thread"},
+            "prefill": {"value": round(L_s / pf_s * H_s / pw.H, 1), "unit": "tok/s", "cores": min(cores, H_s),
+                        "sample": f"token loop over the first {L_s} tokens of {H_s} of the 64 heads of the "
+                                  f"32768-token prefill workload, rate scaled by {H_s}/64 (heads are independent)"},
+            "note": "CPU baseline, not the target"}
 
 
 def run_reference(a, rank, world):
@@ -731,18 +802,20 @@ def run_reference(a, rank, world):
     n = wl.extra["steps"]
     w = {k: v.double().numpy() for k, v in wl.weights().items()}
     tok = {k: v.double().numpy() for k, v in wl.tokens(100, n).items()}
+    start = oracle_warm_state(o, wl, w)
     for _ in range(a.warmup):
-        oracle_decode_run(o, wl, w, tok, n)
-    total = sum(oracle_decode_run(o, wl, w, tok, n) for _ in range(a.steps))
+        oracle_decode_run(o, wl, w, tok, n, start)
+    total = sum(oracle_decode_run(o, wl, w, tok, n, start) for _ in range(a.steps))
     value = a.steps * n / total
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": 1,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(total * 1e3 / a.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy, value recipe of the workload)",
             "config": {"workload": wl.name, "batch": 1, "heads": wl.H, "d_k": wl.dk, "d_v": wl.dv,
-                       "decode_steps_per_bench_step": n},
+                       "warm_tokens": wl.extra["warm"], "decode_steps_per_bench_step": n},
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": o.max_threads(), "kind": "oracle",
-                             "sample": f"{a.steps} x {n} chained decode tokens (the whole workload per step)"},
+                             "sample": f"{a.steps} x {n} chained decode tokens from the 512-token warm state "
+                                       f"(the whole workload per step)"},
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -76,30 +76,5 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     return LIB
 
 
-def build_mma_timing() -> Path:
-    """Builds a separate _build/timing/libkda_mma_timing.so with -DKDA_MMA_TIMING:
-    the prefill kernels also time each tensor-core MMA group (thread 0 waits for
-    its completion right after issuing it), readable via kda_mma_timing_read.
-    For measurement only; the product library is untouched."""
-    out = BUILD / "timing"
-    out.mkdir(parents=True, exist_ok=True)
-    cc = nvcc()
-    objs = []
-    for src in sources():
-        obj = out / (src.stem + ".o")
-        cmd = [cc, *ARCH, *FLAGS, "-DKDA_MMA_TIMING", "-I", str(INCLUDE), "-I", str(CSRC), "-c", str(src), "-o", str(obj)]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            sys.stderr.write(r.stdout + r.stderr)
-            raise RuntimeError(f"nvcc failed on {src.name}")
-        objs.append(obj)
-    lib = out / "libkda_mma_timing.so"
-    r = subprocess.run([cc, *ARCH, "-shared", "-o", str(lib), *map(str, objs)], capture_output=True, text=True)
-    if r.returncode != 0:
-        sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("nvcc link failed")
-    return lib
-
-
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

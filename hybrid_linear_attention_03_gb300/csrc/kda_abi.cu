@@ -103,7 +103,14 @@ kda_status kda_state_pool_create(const kda_pool_desc *desc, void *dev_buf, size_
     p->n_ch = int(L.n_ch);
     p->act_bytes = act_bytes(desc->act);
     p->device = attr.device;
+    p->flags = 0;
     *out = p;
+    return KDA_OK;
+}
+
+kda_status kda_state_pool_set_flags(kda_pool *pool, uint32_t flags) {
+    if (!pool || (flags & ~uint32_t(KDA_POOL_OVERLAP_INPUTS)) != 0) return KDA_ERR_INVALID_ARG;
+    pool->flags = flags;
     return KDA_OK;
 }
 
@@ -174,6 +181,7 @@ static kda_status run_step(kda_pool *pool, const kda_weights *w, const kda_io *i
     p.H = pool->desc.num_heads;
     p.num_slots = pool->desc.num_slots;
     p.n_ch = pool->n_ch;
+    p.early_inputs = (pool->flags & KDA_POOL_OVERLAP_INPUTS) ? 1 : 0;
     p.eps_l2 = w->eps_l2;
     p.eps_rms = w->eps_rms;
     return kda::launch_step(pool, p, reinterpret_cast<cudaStream_t>(stream));
@@ -263,30 +271,8 @@ kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, const kda_i
                                const kda_ckpt_req *reqs, int32_t n_reqs, void *workspace, size_t workspace_bytes,
                                kda_stream_t stream) {
     const CallRange range("kda_prefill_chunked");
-    if (!pool || !valid_weights(w) || !valid_io(io) || N < 0 || n_reqs < 0 || (n_reqs > 0 && !reqs) ||
-        (N > 0 && (!cu_seqlens || !slots || !has_initial_state)))
-        return KDA_ERR_INVALID_ARG;
-    if (N == 0) return n_reqs == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
-    if (cu_seqlens[0] != 0) return KDA_ERR_INVALID_ARG;
-    for (int32_t n = 0; n < N; ++n)
-        if (cu_seqlens[n + 1] < cu_seqlens[n]) return KDA_ERR_INVALID_ARG;
-    const int32_t ns = pool->desc.num_slots;
-    std::vector<uint8_t> used(size_t(ns), 0);
-    for (int32_t n = 0; n < N; ++n) {
-        if (slots[n] < 0 || slots[n] >= ns) return KDA_ERR_SLOT_RANGE;
-        if (used[slots[n]]) return KDA_ERR_ALIAS;
-        used[slots[n]] = 1;
-    }
-    for (int32_t r = 0; r < n_reqs; ++r) {
-        const kda_ckpt_req &q = reqs[r];
-        if (q.seq < 0 || q.seq >= N) return KDA_ERR_INVALID_ARG;
-        const int32_t len = cu_seqlens[q.seq + 1] - cu_seqlens[q.seq];
-        if (q.token_pos <= 0 || q.token_pos > len || (q.token_pos != len && chunk > 0 && q.token_pos % chunk != 0))
-            return KDA_ERR_INVALID_ARG;
-        if (q.dst_slot < 0 || q.dst_slot >= ns) return KDA_ERR_SLOT_RANGE;
-        if (used[q.dst_slot]) return KDA_ERR_ALIAS;
-        used[q.dst_slot] = 1;
-    }
+    const kda_status st = check_prefill_args(pool, w, io, cu_seqlens, slots, has_initial_state, N, chunk, reqs, n_reqs);
+    if (st != KDA_OK || N == 0) return st;
     return kda::launch_prefill(pool, w, io, cu_seqlens, slots, has_initial_state, N, chunk, reqs, n_reqs,
                                workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }

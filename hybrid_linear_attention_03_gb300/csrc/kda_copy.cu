@@ -54,6 +54,7 @@ kda_status launch_slot_copy(const kda_pool *pool, const int32_t *src, const int3
         const unsigned want = unsigned((2 * sms + batch.n - 1) / batch.n);
         if (per_pair > want) per_pair = want;
         if (per_pair < 1) per_pair = 1;
+        const ProfScope prof(KDA_KERNEL_SLOT_COPY, stream);
         slot_copy_kernel<<<dim3(per_pair, unsigned(batch.n)), 256, 0, stream>>>(
             reinterpret_cast<float4 *>(pool->states), state_f4, reinterpret_cast<int4 *>(pool->tails),
             tail_i4, batch);

@@ -22,6 +22,7 @@ struct kda_pool {
     int n_ch;
     int act_bytes;
     int device;
+    uint32_t flags;           // KDA_POOL_* launch options (kda_state_pool_set_flags)
 };
 
 namespace kda {
@@ -49,10 +50,25 @@ struct StepParams {
     const int32_t *in_slots;    // [B]
     const int32_t *snap_slots;  // [B*T]
     int32_t B, T, H, num_slots, n_ch;
+    int32_t early_inputs;  // read inputs before the grid-dependency wait (KDA_POOL_OVERLAP_INPUTS)
     float eps_l2, eps_rms;
 };
 
 kda_status launch_step(const kda_pool *pool, const StepParams &p, cudaStream_t stream);
+
+// Brackets one kernel launch (made inside the scope) with CUDA events on its
+// stream while a profile runs (kda_profile_start); a no-op otherwise.
+class ProfScope {
+  public:
+    ProfScope(int kind, cudaStream_t s);
+    ~ProfScope();
+    ProfScope(const ProfScope &) = delete;
+    ProfScope &operator=(const ProfScope &) = delete;
+
+  private:
+    cudaStream_t s_;
+    int slot_ = -1;
+};
 
 // Slot-to-slot copy of state + tail.
 kda_status launch_slot_copy(const kda_pool *pool, const int32_t *src, const int32_t *dst, int n,

@@ -129,31 +129,6 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
     return rcp_approx(1.0f + ex2_approx(-x * 1.4426950408889634f));
 }
 
-// Timing build only (compiled with -DKDA_MMA_TIMING into a separate library):
-// per MMA group, the cycles from its first issue to its commit's completion,
-// thread 0 waiting right after the commit.  [0] intra A,P  [1] intra W,Ut
-// [2] chain stage 1  [3] chain stage 2  [4] intra CTAs  [5] chain steps.
-#ifdef KDA_MMA_TIMING
-__device__ unsigned long long g_mma_timing[8];
-#endif
-__device__ __forceinline__ unsigned long long mma_timer_start() {
-#ifdef KDA_MMA_TIMING
-    return clock64();
-#else
-    return 0;
-#endif
-}
-__device__ __forceinline__ void mma_timer_stop(unsigned long long t0, uint64_t *bar, uint32_t parity, uint32_t *err,
-                                               int slot, int count_slot) {
-#ifdef KDA_MMA_TIMING
-    mbar_wait(bar, parity, err);
-    atomicAdd(&g_mma_timing[slot], clock64() - t0);
-    if (count_slot >= 0) atomicAdd(&g_mma_timing[count_slot], 1ull);
-#else
-    (void)t0; (void)bar; (void)parity; (void)err; (void)slot; (void)count_slot;
-#endif
-}
-
 __device__ __forceinline__ char *rec_ptr(const PrefillParams &p, int g, int h) {
     return p.rec + (size_t(g) * p.H + h) * Rec::BYTES;
 }
@@ -671,11 +646,9 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            const unsigned long long t0 = mma_timer_start();
             mma3(tm, sbase + is::X_HI, sbase + is::X_LO, sbase + is::KB_HI, sbase + is::KB_LO, 128, CH, D,
                  idesc_bf16_f32(128, CH), false);
             mma_commit(bar_mma);
-            mma_timer_stop(t0, bar_mma, mma_phase, p.err, 0, 4);
         }
     }
     // chain images that need no MMA: exp(G) . q (rows r; above when !exact) and
@@ -840,11 +813,9 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_kernel(const PrefillP
     tc_fence_after();
     if (tid == 0 && ok) {
         const uint32_t id = idesc_bf16_f32(128, CH);
-        const unsigned long long t0 = mma_timer_start();
         mma3(tm + 64, sbase + is::AK_HI, sbase + is::AK_LO, sbase + is::T_HI, sbase + is::T_LO, D, CH, CH, id, false);
         mma3(tm + 128, sbase + is::AV_HI, sbase + is::AV_LO, sbase + is::T_HI, sbase + is::T_LO, D, CH, CH, id, false);
         mma_commit(bar_mma);
-        mma_timer_stop(t0, bar_mma, mma_phase, p.err, 1, -1);
     }
     ok = __syncthreads_and(ok && mbar_wait(bar_mma, mma_phase, p.err));
     tc_fence_after();
@@ -982,11 +953,9 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         if (!ok) break;
         if (tid == 0) {
             tc_fence_after();
-            const unsigned long long t0 = mma_timer_start();
             mma3(tm + 0, sbase + cs::A1_HI, sbase + cs::A1_LO, sbase + cs::WQ_HI, sbase + cs::WQ_LO, D, 2 * CH, D,
                  id128, false);
             mma_commit(bar_m1);
-            mma_timer_stop(t0, bar_m1, par, p.err, 2, 5);
         }
         // Ut row entries (r = uc0 .. uc0 + 31, column j) while the MMAs run
         float ut[32];
@@ -1026,11 +995,9 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            const unsigned long long t0 = mma_timer_start();
             mma3(tm + 128, sbase + cs::A2_HI, sbase + cs::A2_LO, sbase + cs::KP_HI, sbase + cs::KP_LO, D, D + CH, CH,
                  id192, false);
             mma_commit(bar_m2);
-            mma_timer_stop(t0, bar_m2, par, p.err, 3, -1);
         }
         ok = __syncthreads_and(mbar_wait(bar_m2, par, p.err));
         if (!ok) break;
@@ -1449,33 +1416,52 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
     const long long per = (n_chunks + n_win - 1) / n_win;
     cudaStream_t cs = side ? side->s : stream, os = side ? side->o : stream;
     constexpr int W = kMaxWindows;
+    // An event call that fails after kernels are queued on the side streams:
+    // join them to the caller's stream as far as the runtime still allows, so
+    // nothing of this call runs after the caller's stream has moved past it
+    // (the caller may free the workspace once it sees the error).
+    auto fail = [&]() {
+        if (side) {
+            cudaEventRecord(side->ev[2 * W + 1], cs);
+            cudaEventRecord(side->ev[2 * W + 2], os);
+            cudaStreamWaitEvent(stream, side->ev[2 * W + 1], 0);
+            cudaStreamWaitEvent(stream, side->ev[2 * W + 2], 0);
+        }
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    };
     if (side) {  // the chain stream starts after everything already on the caller's stream
         if (cudaEventRecord(side->ev[2 * W], stream) != cudaSuccess ||
             cudaStreamWaitEvent(cs, side->ev[2 * W], 0) != cudaSuccess)
-            return KDA_ERR_CUDA;
+            return fail();
     }
     for (int w = 0; w < n_win; ++w) {
         const long long lo = std::min(n_chunks, w * per), hi = std::min(n_chunks, (w + 1) * per);
         if (hi > lo) {
             p.chunk_base = int(lo);
             const dim3 grid(unsigned(hi - lo), unsigned(p.H));
+            const ProfScope prof(KDA_KERNEL_PREFILL_INTRA, stream);
             prefill_intra_kernel<Act><<<grid, is::NT, intra_smem<Act>(), stream>>>(p, mq, mk, mv, ma);
         }
         p.win_lo = int(lo);
         p.win_hi = (w + 1 == n_win) ? int(n_chunks) : int(hi);
         if (side) {
             if (cudaEventRecord(side->ev[w], stream) != cudaSuccess || cudaStreamWaitEvent(cs, side->ev[w], 0) != cudaSuccess)
-                return KDA_ERR_CUDA;
+                return fail();
         }
-        prefill_chain_kernel<<<unsigned(N) * p.H, 256, kChainSmem, cs>>>(p);
+        {
+            const ProfScope prof(KDA_KERNEL_PREFILL_CHAIN, cs);
+            prefill_chain_kernel<<<unsigned(N) * p.H, 256, kChainSmem, cs>>>(p);
+        }
         if (hi > lo) {  // gated norm of the window's chunks once their chain is done, off the chain's stream
             if (side) {
                 if (cudaEventRecord(side->ev[W + w], cs) != cudaSuccess ||
                     cudaStreamWaitEvent(os, side->ev[W + w], 0) != cudaSuccess)
-                    return KDA_ERR_CUDA;
+                    return fail();
             }
             PrefillParams po = p;
             po.chunk_base = int(lo);
+            const ProfScope prof(KDA_KERNEL_PREFILL_OUT, os);
             prefill_out_kernel<Act><<<dim3(unsigned(hi - lo), unsigned(p.H)), 128, 0, os>>>(po);
         }
     }
@@ -1484,11 +1470,14 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
             cudaEventRecord(side->ev[2 * W + 2], os) != cudaSuccess ||
             cudaStreamWaitEvent(stream, side->ev[2 * W + 1], 0) != cudaSuccess ||
             cudaStreamWaitEvent(stream, side->ev[2 * W + 2], 0) != cudaSuccess)
-            return KDA_ERR_CUDA;
+            return fail();
     }
     p.chunk_base = 0;
-    if (n_reqs > 0) prefill_tails_kernel<Act><<<n_reqs, 256, 0, stream>>>(p, 1);
-    prefill_tails_kernel<Act><<<N, 256, 0, stream>>>(p, 0);
+    {
+        const ProfScope prof(KDA_KERNEL_PREFILL_TAILS, stream);
+        if (n_reqs > 0) prefill_tails_kernel<Act><<<n_reqs, 256, 0, stream>>>(p, 1);
+        prefill_tails_kernel<Act><<<N, 256, 0, stream>>>(p, 0);
+    }
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -1578,15 +1567,18 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
     }
     if (ck != cks.size()) return KDA_ERR_INVALID_ARG;
     char *ws = static_cast<char *>(workspace);
-    if (N > 0 && cudaMemcpyAsync(ws + L.seqs, seqs.data(), sizeof(SeqMeta) * seqs.size(), cudaMemcpyHostToDevice,
-                                 stream) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    if (!chunks.empty() && cudaMemcpyAsync(ws + L.chunks, chunks.data(), sizeof(ChunkMeta) * chunks.size(),
-                                           cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    if (!cks.empty() && cudaMemcpyAsync(ws + L.ckpts, cks.data(), sizeof(CkptMeta) * cks.size(),
-                                        cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        return KDA_ERR_CUDA;
+    {
+        const ProfScope prof(KDA_KERNEL_PREFILL_META, stream);  // the host tables' copies to the device
+        if (N > 0 && cudaMemcpyAsync(ws + L.seqs, seqs.data(), sizeof(SeqMeta) * seqs.size(),
+                                     cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (!chunks.empty() && cudaMemcpyAsync(ws + L.chunks, chunks.data(), sizeof(ChunkMeta) * chunks.size(),
+                                               cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (!cks.empty() && cudaMemcpyAsync(ws + L.ckpts, cks.data(), sizeof(CkptMeta) * cks.size(),
+                                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
     return launch_tables(pool, w, io, ws, L, N, n_reqs, n_chunks, cu_seqlens[N], stream);
 }
 
@@ -1624,7 +1616,10 @@ kda_status launch_prefill_dev(const kda_pool *pool, const kda_weights *w, const 
     a.ckpts = reinterpret_cast<CkptMeta *>(ws + LD.L.ckpts);
     a.used = reinterpret_cast<uint32_t *>(ws + LD.used);
     a.err = pool->err;
-    prefill_meta_kernel<<<1, kMetaThreads, 0, stream>>>(a);
+    {
+        const ProfScope prof(KDA_KERNEL_PREFILL_META, stream);
+        prefill_meta_kernel<<<1, kMetaThreads, 0, stream>>>(a);
+    }
     return launch_tables(pool, w, io, ws, LD.L, N, n_reqs, max_chunks, max_tokens, stream);
 }
 
@@ -1634,30 +1629,21 @@ kda_status launch_prefill_dev(const kda_pool *pool, const kda_weights *w, const 
 // their own.  It lives in the module image, so every GPU that loads the
 // library holds it until the process exits.  Host code must not use the
 // array's name as a device address: the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress with the call's device current.  It is looked up on
+// every call (a table lookup once the module is loaded), so a device reset
+// that reloads the module at another address leaves no stale pointer behind;
+// the first lookup on a device may load the module, which is why the first
+// call should come before any stream capture.
 static __device__ __align__(256) unsigned char g_prefill_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
 kda_status launch_prefill_noalloc(const kda_pool *pool, const kda_weights *w, const kda_io *io,
                                   const int32_t *cu_seqlens, const int32_t *slots,
                                   const uint8_t *has_initial_state, int N, int chunk, const kda_ckpt_req *reqs,
                                   int n_reqs, cudaStream_t stream) {
-    constexpr int kMaxDevices = 64;
-    static std::mutex mu;
-    static void *scratch[kMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
     void *ptr = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!scratch[dev]) {
-            void *addr = nullptr;
-            if (cudaGetSymbolAddress(&addr, g_prefill_noalloc_scratch) != cudaSuccess || !addr) {
-                cudaGetLastError();
-                return KDA_ERR_CUDA;
-            }
-            scratch[dev] = addr;
-        }
-        ptr = scratch[dev];
+    if (cudaGetSymbolAddress(&ptr, g_prefill_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
     }
     // Every byte of the scratch is written before it is read, so nothing is
     // cleared; a call that needs more than the array returns KDA_ERR_WORKSPACE.
@@ -1666,15 +1652,3 @@ kda_status launch_prefill_noalloc(const kda_pool *pool, const kda_weights *w, co
 }
 
 }  // namespace kda
-
-#ifdef KDA_MMA_TIMING
-// Timing build only: copies (and optionally clears) the MMA group counters.
-extern "C" KDA_API int kda_mma_timing_read(unsigned long long *host, int reset) {
-    if (cudaMemcpyFromSymbol(host, kda::g_mma_timing, sizeof(unsigned long long) * 8) != cudaSuccess) return 1;
-    if (reset) {
-        const unsigned long long z[8] = {};
-        if (cudaMemcpyToSymbol(kda::g_mma_timing, z, sizeof(z)) != cudaSuccess) return 1;
-    }
-    return 0;
-}
-#endif

@@ -149,10 +149,21 @@ kda_step_kernel(const StepParams p) {
     const size_t slot_elems = size_t(p.H) * head_elems;
     const Act *beta = static_cast<const Act *>(p.beta);
 
-    // The slot indices and beta go into registers first; nothing reads them
-    // before the grid-dependency wait, so their latency overlaps the copies
-    // below and the wait (consuming them here cost two dependent memory
-    // round trips ahead of the wait: 2.4K of 8.7K cycles per batch-1 step).
+    // Programmatic dependent launch: this grid may start before the
+    // preceding kernel on the stream has completed, and only
+    // griddepcontrol.wait makes that kernel's writes visible.  By default
+    // every input is read after the wait, so any kernel may produce them
+    // right before this launch (the q/k/v projection of a serving step).
+    // With KDA_POOL_OVERLAP_INPUTS the caller guarantees the preceding kernel
+    // writes none of the inputs (a chain of steps over staged inputs), and
+    // the slot tables, beta, weights and token rows are fetched ahead of the
+    // wait, so their latency overlaps it; only the pool (state and conv
+    // tail, which the preceding step writes) is read after it.
+    if (!p.early_inputs) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The slot indices and beta go into registers first; nothing consumes
+    // them before the copies below are issued, so their latency overlaps the
+    // copies (consuming them here cost two dependent memory round trips
+    // ahead of the wait: 2.4K of 8.7K cycles per batch-1 step).
     const int sub = lane / C::LPR, c4 = lane % C::LPR;
     const int n_own = c4 / C::OWN;
     const bool owner = (c4 % C::OWN) == 0;
@@ -167,9 +178,9 @@ kda_step_kernel(const StepParams p) {
         beta_r = beta[(size_t(b) * T + threadIdx.x) * p.H + h];
     }
 
-    // Per-token inputs of all T tokens (never written by the preceding step
-    // launch): 16-byte asynchronous copies into shared memory, issued first
-    // so the whole prologue costs one memory latency.  Every (token, head)
+    // Per-token inputs of all T tokens: 16-byte asynchronous copies into
+    // shared memory, issued first so the whole prologue costs one memory
+    // latency.  Every (token, head)
     // row of D activations starts on a 16-byte boundary (16-byte aligned
     // bases, D * sizeof(Act) a multiple of 16).
     constexpr int CPR = int(D * sizeof(Act) / 16);  // 16-byte chunks per row
@@ -193,7 +204,7 @@ kda_step_kernel(const StepParams p) {
 
     // The pool's state and tail may have been written by the preceding step
     // launch: wait for it to complete before reading them.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.early_inputs) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x < T) {
         bsm[threadIdx.x] = to_f32(beta_r);
         snap_sm[threadIdx.x] = snap_r;
@@ -412,6 +423,7 @@ kda_status launch_d(const StepParams &p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    const ProfScope prof(KDA_KERNEL_STEP, stream);
     return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

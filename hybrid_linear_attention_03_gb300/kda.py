@@ -32,6 +32,7 @@ KDA_BF16 = 1
 KDA_DEVERR_SLOT_RANGE = 0x1
 KDA_DEVERR_META = 0x2
 KDA_DEVERR_TIMEOUT = 0x4
+KDA_POOL_OVERLAP_INPUTS = 0x1
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_state_pool_bytes", "kda_state_pool_create", "kda_state_pool_destroy", "kda_state_pool_layout",
@@ -39,7 +40,11 @@ EXPORTS = ("kda_state_pool_bytes", "kda_state_pool_create", "kda_state_pool_dest
            "kda_state_checkpoint", "kda_poll_device_error", "kda_status_string", "kda_prefill_chunked_noalloc",
            "kda_state_slot_bytes", "kda_state_export", "kda_state_import", "kda_prefill_workspace_bytes_bound",
            "kda_prefill_chunked_dev", "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_plan",
-           "kda_prefix_cache_forget", "kda_prefix_cache_get_stats", "kda_prefix_cache_saved", "kda_stream_wait")
+           "kda_prefix_cache_forget", "kda_prefix_cache_get_stats", "kda_prefix_cache_saved", "kda_stream_wait",
+           "kda_state_pool_set_flags", "kda_profile_start", "kda_profile_stop")
+
+# kda_kernel_kind
+KERNEL_KINDS = ("step", "slot_copy", "prefill_meta", "prefill_intra", "prefill_chain", "prefill_out", "prefill_tails")
 
 KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -79,6 +84,11 @@ class kda_prefix_cache_stats(ctypes.Structure):
                                                "n_free")]
 
 
+class kda_profile(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64 * len(KERNEL_KINDS)), ("ms", ctypes.c_double * len(KERNEL_KINDS)),
+                ("dropped", ctypes.c_int64)]
+
+
 class KdaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -104,6 +114,8 @@ def lib() -> ctypes.CDLL:
         L.kda_state_pool_create.restype = i32
         L.kda_state_pool_destroy.argtypes = [vp]
         L.kda_state_pool_destroy.restype = None
+        L.kda_state_pool_set_flags.argtypes = [vp, ctypes.c_uint32]
+        L.kda_state_pool_set_flags.restype = i32
         L.kda_state_pool_layout.argtypes = [vp, P(kda_pool_layout)]
         L.kda_state_pool_layout.restype = i32
         L.kda_check_slots.argtypes = [vp, vp, i32, vp, i32]
@@ -149,6 +161,10 @@ def lib() -> ctypes.CDLL:
         L.kda_prefix_cache_saved.restype = i32
         L.kda_stream_wait.argtypes = [vp, ctypes.c_double]
         L.kda_stream_wait.restype = i32
+        L.kda_profile_start.argtypes = [i32]
+        L.kda_profile_start.restype = i32
+        L.kda_profile_stop.argtypes = [P(kda_profile)]
+        L.kda_profile_stop.restype = i32
         L.kda_status_string.argtypes = [i32]
         L.kda_status_string.restype = ctypes.c_char_p
         _LIB = L
@@ -162,6 +178,21 @@ def kda_stream_wait(stream=None, timeout_s: float = 60.0) -> int:
     if st not in (KDA_OK, KDA_ERR_TIMEOUT):
         raise KdaError(st, "kda_stream_wait")
     return st
+
+
+def kda_profile_start(max_launches: int = 4096) -> None:
+    """Starts timing every kernel the library launches (CUDA events on the
+    launching stream) on the current device."""
+    _check(lib().kda_profile_start(int(max_launches)), "kda_profile_start")
+
+
+def kda_profile_stop() -> dict:
+    """Stops the profile: {kind: (launches, total ms)} plus "dropped"."""
+    out = kda_profile()
+    _check(lib().kda_profile_stop(ctypes.byref(out)), "kda_profile_stop")
+    res = {k: (int(out.launches[i]), float(out.ms[i])) for i, k in enumerate(KERNEL_KINDS)}
+    res["dropped"] = int(out.dropped)
+    return res
 
 
 def kda_status_string(status: int) -> str:
@@ -217,6 +248,11 @@ def kda_state_pool_create(desc: kda_pool_desc, buf: torch.Tensor) -> ctypes.c_vo
 def kda_state_pool_destroy(handle) -> None:
     if handle:
         lib().kda_state_pool_destroy(handle)
+
+
+def kda_state_pool_set_flags(pool: "StatePool", flags: int) -> None:
+    """Launch options of the pool's decode / verify calls (KDA_POOL_* flags)."""
+    _check(lib().kda_state_pool_set_flags(pool.handle, int(flags)), "kda_state_pool_set_flags")
 
 
 def kda_state_pool_layout(handle) -> kda_pool_layout:

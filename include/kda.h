@@ -151,6 +151,20 @@ KDA_API kda_status kda_state_pool_create(const kda_pool_desc *desc, void *dev_bu
 /* Frees the handle (not the caller's buffer).  NULL is ignored. */
 KDA_API void kda_state_pool_destroy(kda_pool *pool);
 
+/* Launch options of a pool's kda_decode / kda_verify calls (flags of
+ * kda_state_pool_set_flags; 0, the default, sets none).
+ * KDA_POOL_OVERLAP_INPUTS: each launch starts under the preceding kernel on
+ *   its stream (programmatic dependent launch) and reads its slot tables,
+ *   beta, weights and token inputs before that kernel has completed; only the
+ *   pool (state and conv tail) is read after it.  The caller guarantees that
+ *   the preceding kernel on the stream writes none of those inputs, e.g. a
+ *   chain of decode steps whose inputs were staged beforehand.  Without the
+ *   flag every input is read after the preceding kernel has completed, so any
+ *   kernel (a q/k/v projection) may produce the inputs right before the call.
+ * Returns KDA_ERR_INVALID_ARG for a null pool or an unknown flag. */
+#define KDA_POOL_OVERLAP_INPUTS 0x1u
+KDA_API kda_status kda_state_pool_set_flags(kda_pool *pool, uint32_t flags);
+
 /* Byte offsets of the pool regions (see the layout above). */
 KDA_API kda_status kda_state_pool_layout(const kda_pool *pool, kda_pool_layout *out);
 
@@ -169,11 +183,10 @@ KDA_API kda_status kda_check_slots(const kda_pool *pool, const int32_t *in_slots
  * pool sets KDA_DEVERR_SLOT_RANGE and that sequence is skipped.  Slots must be
  * distinct (check with kda_check_slots).  B = 0 is a no-op.
  * One launch: conv, L2, update, readout and gated norm are fused.
- * Consecutive kda_decode / kda_verify launches on one stream overlap by
- * programmatic dependent launch: a launch reads its slot tables, weights and
- * token inputs while the previous one finishes, and reads the pool only
- * after it has completed.  So token inputs must not be written by the
- * immediately preceding kda_decode / kda_verify launch on the stream.
+ * The launch may start while the preceding kernel on its stream finishes
+ * (programmatic dependent launch); it reads nothing until that kernel has
+ * completed, unless the pool has KDA_POOL_OVERLAP_INPUTS set (see
+ * kda_state_pool_set_flags for that contract).
  * Source: "vLLM Kimi K3 지원", section "Fused Kernels 및 메타데이터 최적화",
  * KDA Decode bullet. */
 KDA_API kda_status kda_decode(kda_pool *pool, const kda_weights *w, const kda_io *io,
@@ -234,8 +247,10 @@ KDA_API kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, con
  * A call that needs more scratch than that (its kda_prefill_workspace_bytes
  * figure for its own requests; with d = 128 about 370 (chunk, head) pairs of
  * 64 tokens) returns KDA_ERR_WORKSPACE and enqueues nothing.
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.
+ * Every call looks up the array's device address with the call's device
+ * current (so a device reset that reloads the library's module leaves no
+ * stale address behind).  The first lookup on a device may load the module:
+ * make the first call on each device before any stream capture.
  * Every call uses the same array and leaves its contents behind; each call
  * writes every scratch byte it reads, so nothing needs clearing.  Calls that
  * overlap on one GPU (other streams, other threads) race on the array:
@@ -371,6 +386,40 @@ KDA_API kda_status kda_poll_device_error(kda_pool *pool, kda_stream_t stream, ui
  * for a negative or non-finite limit.  Every wait inside the kernels is
  * bounded too, so a stream the library alone feeds always finishes. */
 KDA_API kda_status kda_stream_wait(kda_stream_t stream, double timeout_s);
+
+/* ---- Device-time profile of the library's own kernels -------------------
+ * A measurement aid; the pages have no counterpart.  Between
+ * kda_profile_start and kda_profile_stop every kernel this library launches
+ * (outside stream capture) is bracketed by two CUDA events recorded on the
+ * stream it is launched on, so each interval is that kernel's device time as
+ * it ran in the caller's schedule.  kda_profile_stop waits for the events
+ * and reports, per kernel kind, the launches timed and their summed time.
+ * max_launches (1 .. 2^20) bounds the events created (two per launch);
+ * launches beyond it are counted in `dropped` and not timed.  One profile
+ * per process at a time; the events belong to the device current at
+ * kda_profile_start, so profile launches on that device only.  The events
+ * serialise the launches they bracket with their neighbours on the stream
+ * (a timed step launch no longer overlaps the one before it).
+ * Errors: KDA_ERR_INVALID_ARG (a bad limit, start while running, stop while
+ * stopped), KDA_ERR_CUDA (event creation or timing failed). */
+typedef enum {
+    KDA_KERNEL_STEP = 0,       /* kda_decode / kda_verify */
+    KDA_KERNEL_SLOT_COPY,      /* kda_state_checkpoint */
+    KDA_KERNEL_PREFILL_META,   /* prefill tables: the device builder (kda_prefill_chunked_dev), or the
+                                  copies of the host-built tables (kda_prefill_chunked) */
+    KDA_KERNEL_PREFILL_INTRA,  /* intra-chunk prefill kernel */
+    KDA_KERNEL_PREFILL_CHAIN,  /* the chunk chain (state passing) */
+    KDA_KERNEL_PREFILL_OUT,    /* gated norm of the prefill outputs */
+    KDA_KERNEL_PREFILL_TAILS,  /* conv tails of checkpoints and ends */
+    KDA_KERNEL_COUNT
+} kda_kernel_kind;
+typedef struct {
+    int64_t launches[KDA_KERNEL_COUNT];
+    double ms[KDA_KERNEL_COUNT];
+    int64_t dropped;
+} kda_profile;
+KDA_API kda_status kda_profile_start(int32_t max_launches);
+KDA_API kda_status kda_profile_stop(kda_profile *out);
 
 /* Static text for a status code. */
 KDA_API const char *kda_status_string(kda_status s);

@@ -74,6 +74,31 @@ class Mirror:
         return bool(np.array_equal(g, self.ora.get(int(slot))[1]))
 
 
+class OracleMirror:
+    """The oracle side of a Mirror alone, for tests that drive the GPU pools
+    themselves: a float64 slot pool started from the GPU pool's states and
+    tails (read once, before any GPU call of the test), and the layer weights.
+    prefill_oracle accepts it in place of a Mirror."""
+
+    def __init__(self, H, D, act, weights: dict, states=None, tails=None, eps_l2=1e-6, eps_rms=1e-5):
+        self.H, self.D, self.act = H, D, act
+        self.ora = ko.OraclePool(H, D, D, 4, eps_l2, eps_rms)
+        self.w_ora = hp.oracle_weights(weights)
+        if states is not None:
+            for s in range(states.shape[0]):
+                self.ora.put(s, hp.gpu_state_as_oracle(states[s]), hp.f64(tails[s]))
+
+    def check_slots(self, pool, slots, tol=hp.STATE_TOL):
+        """Every listed slot of the GPU pool against the oracle pool: state
+        within tol (block relative error), conv tail bit for bit."""
+        for s in slots:
+            g = hp.gpu_state_as_oracle(pool.states()[int(s)])
+            S, t = self.ora.get(int(s))
+            err = hp.block_rel_err(g, S, 2)
+            assert err <= tol, f"state of slot {s}: {err:.3e}"
+            assert np.array_equal(hp.f64(pool.tails()[int(s)]), t), f"tail of slot {s}"
+
+
 def prefill_gpu(m: Mirror, inp_dev: dict, lens, slots, has_init, reqs=(), stream=None):
     """Run kda_prefill_chunked on the mirror's GPU pool; returns the output."""
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
@@ -81,6 +106,11 @@ def prefill_gpu(m: Mirror, inp_dev: dict, lens, slots, has_init, reqs=(), stream
     ws_bytes = kda.kda_prefill_workspace_bytes(m.gpu, cu)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
     kda.kda_prefill_chunked(m.gpu, m.w, kda.make_io(inp_dev, out), cu, slots, has_init, 64, reqs, ws, stream)
+    if stream is not None:
+        # the workspace was allocated on the current stream but is used on
+        # `stream`: keep the caching allocator from reusing it before that
+        # stream's prefill has finished
+        ws.record_stream(stream)
     return out
 
 

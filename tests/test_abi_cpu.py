@@ -96,3 +96,16 @@ def test_stream_wait_rejects_bad_limits(lib):
     # checked before any CUDA call
     for bad in (-1.0, float("nan"), float("inf")):
         assert lib.kda_stream_wait(None, bad) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_profile_argument_errors(lib):
+    """kda_profile_start / kda_profile_stop reject a bad limit and a stop with
+    no profile running before touching any CUDA state."""
+    assert lib.kda_profile_start(0) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_profile_start((1 << 20) + 1) == kda.KDA_ERR_INVALID_ARG
+    out = kda.kda_profile()
+    assert lib.kda_profile_stop(ctypes.byref(out)) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_pool_flags_reject_a_null_pool_and_unknown_bits(lib):
+    assert lib.kda_state_pool_set_flags(None, 0) == kda.KDA_ERR_INVALID_ARG

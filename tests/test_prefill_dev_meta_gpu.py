@@ -1,7 +1,8 @@
 """The chunked prefill with its sequence metadata in device memory
-(kda_prefill_chunked_dev): its tables are built on the GPU, so it must give
-bit for bit what the host-metadata call gives, run inside a CUDA graph, and
-reject bad metadata on the device without touching any slot or output."""
+(kda_prefill_chunked_dev): its tables are built on the GPU, so it must match
+the oracle (outputs, states and tails of every sequence and checkpoint slot),
+give bit for bit what the host-metadata call gives, run inside a CUDA graph,
+and reject bad metadata on the device without touching any slot or output."""
 
 from __future__ import annotations
 
@@ -14,6 +15,7 @@ from hybrid_linear_attention_03_gb300 import inputs as I
 from hybrid_linear_attention_03_gb300 import kda
 
 import helpers as hp
+from mirror import OracleMirror, prefill_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -28,9 +30,10 @@ def _lib():
     kda.lib()
 
 
-def _setup(act, seed, lens, max_extra=70):
+def _setup(act, seed, lens, max_extra=70, want_oracle=False):
     """Two identical pools (random warm states and tails), weights, inputs of
-    max_tokens rows (the real tokens first, then padding rows)."""
+    max_tokens rows (the real tokens first, then padding rows); with
+    want_oracle also an oracle pool holding the same start states."""
     H, num_slots = 2, 32
     w = I.layer_weights(seed, H, D, D, 4, act)
     w_dev = hp.to_device(w)
@@ -44,8 +47,23 @@ def _setup(act, seed, lens, max_extra=70):
         p.tails().copy_(tl)
     n_tok = int(sum(lens))
     max_tokens = n_tok + max_extra
-    inp = hp.to_device(I.token_inputs(seed, 0, max_tokens, H, D, D, 2.0, act))
+    inp_cpu = I.token_inputs(seed, 0, max_tokens, H, D, D, 2.0, act)
+    inp = hp.to_device(inp_cpu)
+    if want_oracle:
+        om = OracleMirror(H, D, act, w, st, tl)
+        real_cpu = {k: v[:n_tok] for k, v in inp_cpu.items()}
+        return H, wk, pools, inp, n_tok, max_tokens, om, real_cpu
     return H, wk, pools, inp, n_tok, max_tokens
+
+
+def _check_oracle(om, real_cpu, lens, slots, has_init, reqs, pool, out):
+    """The device-metadata prefill against the oracle token loop: outputs of
+    every real row, state and tail of every sequence and checkpoint slot."""
+    ref = prefill_oracle(om, real_cpu, lens, slots, has_init, reqs)
+    assert torch.isfinite(out.float()).all()
+    err = hp.block_rel_err(hp.f64(out), ref, 1)
+    assert err <= hp.out_tol(om.act), f"outputs: {err:.3e}"
+    om.check_slots(pool, list(slots) + [r[2] for r in reqs])
 
 
 def _run_dev(pool, wk, inp, lens, slots, has_init, reqs, max_tokens, out, stream=None):
@@ -66,7 +84,7 @@ def test_device_tables_match_host_tables_bitexact(act):
     has_init = [0, 1, 1, 0, 1, 0, 1, 1, 0]
     reqs = [(5, 64, 20), (5, 65, 21), (6, 64, 22), (6, 128, 23), (8, 200, 24), (3, 63, 25), (0, 1, 26),
             (8, 64, 27)]
-    H, wk, (pa, pb), inp, n_tok, max_tokens = _setup(act, 61, lens)
+    H, wk, (pa, pb), inp, n_tok, max_tokens, om, real_cpu = _setup(act, 61, lens, want_oracle=True)
     real = {k: v[:n_tok].contiguous() for k, v in inp.items()}
     out_a = torch.full((n_tok, H, D), 7.0, dtype=act, device="cuda")
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
@@ -79,6 +97,7 @@ def test_device_tables_match_host_tables_bitexact(act):
     assert torch.equal(out_b[:n_tok], out_a)
     assert torch.all(out_b[n_tok:] == 7.0), "rows past cu_seqlens[N] are never written"
     assert torch.equal(pb.states(), pa.states()) and torch.equal(pb.tails(), pa.tails())
+    _check_oracle(om, real_cpu, lens, slots, has_init, reqs, pb, out_b[:n_tok])
 
 
 def test_device_tables_inside_a_cuda_graph():
@@ -176,7 +195,7 @@ def test_random_metadata_device_equals_host_bitexact(seed):
         for pos in ends:
             if free and rng.random() < 0.4:
                 reqs.append((n, pos, free.pop()))
-    H, wk, (pa, pb), inp, n_tok, max_tokens = _setup(torch.bfloat16, seed, lens)
+    H, wk, (pa, pb), inp, n_tok, max_tokens, om, real_cpu = _setup(torch.bfloat16, seed, lens, want_oracle=True)
     real = {k: v[:n_tok].contiguous() for k, v in inp.items()}
     out_a = torch.full((max(n_tok, 1), H, D), 7.0, dtype=torch.bfloat16, device="cuda")[:n_tok]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
@@ -189,3 +208,4 @@ def test_random_metadata_device_equals_host_bitexact(seed):
     assert torch.equal(out_b[:n_tok], out_a)
     assert torch.all(out_b[n_tok:] == 7.0)
     assert torch.equal(pb.states(), pa.states()) and torch.equal(pb.tails(), pa.tails())
+    _check_oracle(om, real_cpu, lens, slots, has_init, reqs, pb, out_b[:n_tok])

@@ -304,3 +304,63 @@ def test_host_argument_errors_enqueue_nothing():
     with pytest.raises(kda.KdaError) as e:
         kda.kda_state_checkpoint(pool, [0], [9])
     assert e.value.status == kda.KDA_ERR_SLOT_RANGE
+
+
+@pytest.mark.parametrize("graph", [False, True], ids=["stream", "graph"])
+def test_inputs_written_by_the_preceding_kernel(graph):
+    """A torch kernel writes each step's inputs on the same stream right
+    before kda_decode, as the q/k/v projection of a serving step does.  With
+    the pool's default launch options the decode reads its inputs only after
+    that kernel has completed, so every output and the end states match the
+    oracle, on a plain stream and inside a captured CUDA graph.  The last
+    producer before each decode is a 64 MiB copy whose final rows are q."""
+    H, D, act, B, steps = 4, 128, torch.bfloat16, 8, 4
+    m = Mirror(16, H, D, act, _weights(91, H, D, act))
+    slots = [3, 7, 1, 12, 0, 9, 5, 14]
+    sl = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    toks = [_tokens(91, 20 + s, B, H, D, act) for s in range(steps)]
+    pad_rows = (64 << 20) // (H * D * 2)  # q's producer writes 64 MiB ahead of the real rows
+    order = ("alpha", "beta", "gate", "v", "k", "q")  # q last: its copy is the kernel right before the decode
+    big = {k: torch.full((pad_rows + B,) + tuple(toks[0][k].shape[1:]), float("nan"), dtype=act, device="cuda")
+           if k == "q" else torch.full(tuple(toks[0][k].shape), float("nan"), dtype=act, device="cuda")
+           for k in order}
+    staged = []
+    for t in toks:
+        d = {k: t[k].cuda() for k in order}
+        d["q"] = torch.cat([torch.zeros(pad_rows, H, D, dtype=act), t["q"]]).cuda()
+        staged.append(d)
+    view = {k: (big[k][pad_rows:] if k == "q" else big[k]) for k in order}
+    outs = [torch.empty(B, H, D, dtype=act, device="cuda") for _ in range(steps)]
+    ios = [kda.make_io(view, o) for o in outs]
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def run_all():
+        for s in range(steps):
+            for k in order:
+                big[k].copy_(staged[s][k])
+            kda.kda_decode(m.gpu, m.w, ios[s], sl, B, stream)
+
+    if graph:
+        m.decode([15], _tokens(91, 99, 1, H, D, act))  # the first launch sets attributes, outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run_all()
+        torch.cuda.synchronize()
+        assert torch.all(m.gpu.states()[slots] == 0), "capture enqueued nothing"
+        g.replay()
+    else:
+        with torch.cuda.stream(stream):
+            run_all()
+    torch.cuda.synchronize()
+    for s in range(steps):
+        oi = hp.oracle_inputs(toks[s])
+        ref = np.zeros((B, H, D))
+        for b, slot in enumerate(slots):
+            ref[b] = m.ora.run(slot, {k: v[b:b + 1] for k, v in oi.items()}, m.w_ora)[0]
+        assert hp.block_rel_err(hp.f64(outs[s]), ref, 1) <= hp.OUT_TOL_BF16, f"step {s}"
+    for slot in slots:
+        assert m.state_err(slot) <= hp.STATE_TOL
+        assert m.tail_equal(slot)
+    assert kda.kda_poll_device_error(m.gpu) == (kda.KDA_OK, 0)

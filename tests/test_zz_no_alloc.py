@@ -5,10 +5,14 @@ reserves all device memory up front and hands none out, or a C caller with
 no device allocator).  kda_prefill_chunked_noalloc serves them by running
 the chunked prefill in a fixed 64 MiB scratch array compiled into the
 library instead of a caller workspace.  Here it is called through the C ABI
-twice in a row and must agree with kda_prefill_chunked (which takes a
-workspace) within the tolerances used by every other GPU test; a request
-larger than the array must be refused.  This file is collected last, so a
-run that stops at its first failure has already run every other test.
+twice in a row.  It runs the same deterministic kernels as
+kda_prefill_chunked (which takes a workspace), so outputs, states and tails
+must equal that call's bit for bit; the second call reuses the array the
+first left behind, which shows that no stale scratch byte is read.  Both
+calls are also held to the oracle within the tolerances every other GPU
+test uses, and a request larger than the array must be refused.  This file
+is collected last, so a run that stops at its first failure has already run
+every other test.
 """
 
 from __future__ import annotations
@@ -22,6 +26,7 @@ from hybrid_linear_attention_03_gb300 import inputs as I
 from hybrid_linear_attention_03_gb300 import kda
 
 import helpers as hp
+from mirror import OracleMirror, prefill_oracle
 
 pytestmark = pytest.mark.gpu
 H, D, act = 2, 128, torch.bfloat16
@@ -37,8 +42,9 @@ def _lib():
 
 def _pool_and_weights():
     pool = kda.StatePool(16, H, D, D, act)
-    w = {k: v.cuda() for k, v in I.layer_weights(61, H, D, D, 4, act).items()}
-    return pool, w, kda.make_weights(w["conv_w"], w["norm_w"])
+    w_cpu = I.layer_weights(61, H, D, D, 4, act)
+    w = {k: v.cuda() for k, v in w_cpu.items()}
+    return pool, w, kda.make_weights(w["conv_w"], w["norm_w"]), w_cpu
 
 
 def test_noalloc_prefill_matches_workspace_prefill_twice():
@@ -46,10 +52,12 @@ def test_noalloc_prefill_matches_workspace_prefill_twice():
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     slots = [3, 0, 7, 11]
     reqs = [(2, 64, 12), (3, 77, 13)]
-    pa, wa, wgt_a = _pool_and_weights()
-    pb, wb, wgt_b = _pool_and_weights()
+    pa, wa, wgt_a, w_cpu = _pool_and_weights()
+    pb, wb, wgt_b, _ = _pool_and_weights()
+    om = OracleMirror(H, D, act, w_cpu)  # both pools start from zeros, as the oracle pool does
     for call in range(2):  # the second call continues the first (and reuses the scratch)
-        inp = {k: v.cuda() for k, v in I.token_inputs(61, call, int(cu[-1]), H, D, D, 3.0, act).items()}
+        inp_cpu = I.token_inputs(61, call, int(cu[-1]), H, D, D, 3.0, act)
+        inp = {k: v.cuda() for k, v in inp_cpu.items()}
         init = [call] * len(lens)
         out_a = torch.empty(int(cu[-1]), H, D, dtype=act, device="cuda")
         ws = torch.empty(kda.kda_prefill_workspace_bytes(pa, cu), dtype=torch.uint8, device="cuda")
@@ -57,17 +65,19 @@ def test_noalloc_prefill_matches_workspace_prefill_twice():
         out_b = torch.full((int(cu[-1]), H, D), float("nan"), dtype=act, device="cuda")
         kda.kda_prefill_chunked_noalloc(pb, wgt_b, kda.make_io(inp, out_b), cu, slots, init, 64, reqs)
         torch.cuda.synchronize()
-        assert hp.block_rel_err(hp.f64(out_b), hp.f64(out_a), 1) <= hp.OUT_TOL_BF16, f"call {call}: outputs"
+        assert torch.equal(out_b, out_a), f"call {call}: outputs differ from the workspace prefill"
         for s in slots + [r[2] for r in reqs]:
-            ga = hp.gpu_state_as_oracle(pa.states()[s])
-            gb = hp.gpu_state_as_oracle(pb.states()[s])
-            assert hp.block_rel_err(gb, ga, 2) <= hp.STATE_TOL, f"call {call}: state of slot {s}"
-            assert torch.equal(pa.tails()[s], pb.tails()[s]), f"call {call}: tail of slot {s}"
+            assert torch.equal(pb.states()[s], pa.states()[s]), f"call {call}: state of slot {s}"
+            assert torch.equal(pb.tails()[s], pa.tails()[s]), f"call {call}: tail of slot {s}"
+        ref = prefill_oracle(om, inp_cpu, lens, slots, init, reqs)
+        err = hp.block_rel_err(hp.f64(out_b), ref, 1)
+        assert err <= hp.OUT_TOL_BF16, f"call {call}: outputs vs the oracle {err:.3e}"
+        om.check_slots(pb, slots + [r[2] for r in reqs])
     assert kda.kda_poll_device_error(pb) == (kda.KDA_OK, 0)
 
 
 def test_noalloc_prefill_refuses_requests_beyond_the_scratch():
-    pool, w, wgt = _pool_and_weights()
+    pool, w, wgt, _ = _pool_and_weights()
     L = 64 * 300  # 300 chunks x 2 heads of records: more than 64 MiB
     assert kda.kda_prefill_workspace_bytes(pool, [0, L]) > kda.KDA_NOALLOC_SCRATCH_BYTES
     inp = {k: v.cuda() for k, v in I.token_inputs(61, 9, L, H, D, D, 3.0, act).items()}
