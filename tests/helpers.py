@@ -9,7 +9,15 @@ import torch
 # Tolerances (max relative error per block, see block_rel_err).
 STATE_TOL = 1e-4      # fp32 state
 OUT_TOL_BF16 = 2e-2   # bf16 outputs
-OUT_TOL_F32 = 1e-4    # fp32 outputs (tiny fp32 workload)
+OUT_TOL_F32 = 1e-4    # fp32 outputs of the decode / verify step (fp32 CUDA-core arithmetic)
+# fp32 outputs of the chunked prefill.  Its products run on the tensor cores
+# as three bf16 products of hi/lo splits, which keep about 16 mantissa bits:
+# each product term carries a relative error near 2^-17 (7.6e-6), a 128-term
+# sum about sqrt(128) times that relative to the row's largest value
+# (8.6e-5), and O = Q S + P U adds two such sums after the state itself was
+# re-split in the same way; 5e-4 bounds that with margin.  The state keeps
+# the 1e-4 bound.
+OUT_TOL_F32_PREFILL = 5e-4
 
 
 def block_rel_err(x, ref, block_dims: int) -> float:
@@ -51,6 +59,10 @@ def to_device(inp: dict, device="cuda") -> dict:
 
 def out_tol(act: torch.dtype) -> float:
     return OUT_TOL_BF16 if act == torch.bfloat16 else OUT_TOL_F32
+
+
+def prefill_out_tol(act: torch.dtype) -> float:
+    return OUT_TOL_BF16 if act == torch.bfloat16 else OUT_TOL_F32_PREFILL
 
 
 def head_subset(inp: dict, w: dict, heads, H: int, dk: int, dv: int):

@@ -62,7 +62,7 @@ def _check_oracle(om, real_cpu, lens, slots, has_init, reqs, pool, out):
     ref = prefill_oracle(om, real_cpu, lens, slots, has_init, reqs)
     assert torch.isfinite(out.float()).all()
     err = hp.block_rel_err(hp.f64(out), ref, 1)
-    assert err <= hp.out_tol(om.act), f"outputs: {err:.3e}"
+    assert err <= hp.prefill_out_tol(om.act), f"outputs: {err:.3e}"
     om.check_slots(pool, list(slots) + [r[2] for r in reqs])
 
 

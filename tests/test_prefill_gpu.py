@@ -27,7 +27,7 @@ def _lib():
 
 def _check(m, out, ref, slots, reqs=()):
     assert torch.isfinite(out.float()).all()
-    assert hp.block_rel_err(hp.f64(out), ref, 1) <= hp.out_tol(m.act)
+    assert hp.block_rel_err(hp.f64(out), ref, 1) <= hp.prefill_out_tol(m.act)
     for s in list(slots) + [r[2] for r in reqs]:
         assert m.state_err(int(s)) <= hp.STATE_TOL, f"state of slot {s}"
         assert m.tail_equal(int(s)), f"tail of slot {s}"
