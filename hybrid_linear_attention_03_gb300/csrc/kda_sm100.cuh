@@ -205,6 +205,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Descriptor of an MN-major operand in the same 128-byte-swizzle atoms: a
+// row of an atom holds 64 consecutive M (or N) elements of one K index, 8
+// consecutive K indices form the 1024-byte atom (8-row groups at 1024 B), and
+// the next 64 M (or N) elements sit `lbo` bytes further (leading byte
+// offset).  A token-major image [rows][64-wide channel blocks] built with
+// sw128_chunk has exactly this layout when read with channels as M (or N) and
+// tokens as K: lbo is then the channel-block stride (rows * 128 bytes).  K
+// steps of 16 advance the start address by 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;  // leading byte offset: 64-element M/N block stride
+    d |= uint64_t(1024 >> 4) << 32;             // stride byte offset: 8-row K group stride
+    d |= uint64_t(1) << 46;                     // descriptor version
+    d |= uint64_t(2) << 61;                     // 128-byte swizzle
+    return d;
+}
+
 // Splits 8 fp32 values into bf16 hi = rn(x) and lo = rn(x - hi), packed as
 // two 16-byte vectors (x ~= hi + lo to about 16 mantissa bits).  Pairs are
 // converted with the packed bf16x2 round-to-nearest conversion.
@@ -229,9 +247,12 @@ __host__ __device__ __forceinline__ uint32_t sw128_chunk(int row, int c, int row
     return uint32_t(kb * rows * 128 + row * 128 + ((cc ^ (row & 7)) << 4));
 }
 
-// Instruction descriptor: kind::f16 with bf16 A and B (both K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 D; a_mn / b_mn
+// mark an operand stored MN-major (the "transpose" bits 15 and 16), else it
+// is K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u) |
+           (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
 }  // namespace sm100

@@ -77,13 +77,43 @@ def test_noalloc_prefill_matches_workspace_prefill_twice():
 
 
 def test_noalloc_prefill_refuses_requests_beyond_the_scratch():
-    pool, w, wgt, _ = _pool_and_weights()
-    L = 64 * 300  # 300 chunks x 2 heads of records: more than 64 MiB
+    """The scratch holds the tables and a ring of per-(chunk, head) records
+    whose windows shrink to fit; a layer with so many heads that even one
+    chunk's records exceed 64 MiB is refused, with nothing enqueued."""
+    Hb = 400  # one chunk of 400 heads needs 400 records of 177 KiB: more than 64 MiB
+    pool = kda.StatePool(2, Hb, D, D, act)
+    w = {k: v.cuda() for k, v in I.layer_weights(61, Hb, D, D, 4, act).items()}
+    wgt = kda.make_weights(w["conv_w"], w["norm_w"])
+    L = 64
     assert kda.kda_prefill_workspace_bytes(pool, [0, L]) > kda.KDA_NOALLOC_SCRATCH_BYTES
-    inp = {k: v.cuda() for k, v in I.token_inputs(61, 9, L, H, D, D, 3.0, act).items()}
-    out = torch.zeros(L, H, D, dtype=act, device="cuda")
+    inp = {k: v.cuda() for k, v in I.token_inputs(61, 9, L, Hb, D, D, 3.0, act).items()}
+    out = torch.zeros(L, Hb, D, dtype=act, device="cuda")
     with pytest.raises(kda.KdaError) as e:
         kda.kda_prefill_chunked_noalloc(pool, wgt, kda.make_io(inp, out), [0, L], [0], [0])
     assert e.value.status == kda.KDA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.all(out == 0) and torch.all(pool.states() == 0)
+
+
+def test_noalloc_prefill_of_a_long_prompt_runs_in_small_windows():
+    """A prompt whose preferred workspace is larger than the scratch (4096
+    tokens, 16 heads: 2 windows of 32 chunks x 16 heads of records, about
+    181 MiB) runs in the scratch with smaller windows and equals the
+    workspace prefill bit for bit."""
+    Hs, L = 16, 4096
+    pa = kda.StatePool(2, Hs, D, D, act)
+    pb = kda.StatePool(2, Hs, D, D, act)
+    w = {k: v.cuda() for k, v in I.layer_weights(67, Hs, D, D, 4, act).items()}
+    wgt = kda.make_weights(w["conv_w"], w["norm_w"])
+    cu = [0, L]
+    assert kda.kda_prefill_workspace_bytes(pa, cu) > kda.KDA_NOALLOC_SCRATCH_BYTES
+    inp = {k: v.cuda() for k, v in I.token_inputs(67, 0, L, Hs, D, D, 3.0, act).items()}
+    out_a = torch.empty(L, Hs, D, dtype=act, device="cuda")
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(pa, cu), dtype=torch.uint8, device="cuda")
+    kda.kda_prefill_chunked(pa, wgt, kda.make_io(inp, out_a), cu, [1], [0], 64, [(0, 2048, 0)], ws)
+    out_b = torch.empty(L, Hs, D, dtype=act, device="cuda")
+    kda.kda_prefill_chunked_noalloc(pb, wgt, kda.make_io(inp, out_b), cu, [1], [0], 64, [(0, 2048, 0)])
+    torch.cuda.synchronize()
+    assert torch.equal(out_b, out_a)
+    assert torch.equal(pb.states(), pa.states()) and torch.equal(pb.tails(), pa.tails())
+    assert kda.kda_poll_device_error(pb) == (kda.KDA_OK, 0)
