@@ -76,7 +76,7 @@ static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
 //   S^T     <- S^T diag(gamma) + (K^T U)^T diag(elc),  O^T = (Q S)^T + (P U)^T
 __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KiB-aligned, still shared
     uint64_t *bar_b1 = reinterpret_cast<uint64_t *>(sm + cs::BARS);
     uint64_t *bar_b2 = bar_b1 + 1, *bar_m1 = bar_b1 + 2, *bar_m2 = bar_b1 + 3;
     uint32_t *tbase = reinterpret_cast<uint32_t *>(bar_b1 + 4);
@@ -164,10 +164,10 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         }
         // Ut^T row j, entries r = uc0 .. uc0 + 31, while the MMAs run
         float ut[32];
-        const float *UTg = reinterpret_cast<const float *>(rec + Rec::UT) + size_t(j) * CH + uc0;
+        const float *UTg = reinterpret_cast<const float *>(rec + Rec::UT) + size_t(j) * CH;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-            const float4 x = ld4(UTg + e);
+            const float4 x = ld4(UTg + 4 * ut_chunk(j, (uc0 + e) >> 2));
             ut[e] = x.x; ut[e + 1] = x.y; ut[e + 2] = x.z; ut[e + 3] = x.w;
         }
         ok = __syncthreads_and(mbar_wait(bar_m1, par, p.err));

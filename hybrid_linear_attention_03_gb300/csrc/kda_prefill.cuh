@@ -13,7 +13,8 @@
 //        k^ exp(G_last - G)
 //   PP   P [64 tokens r][64 tokens s], K-major
 //   GAM  exp(G_last) per key channel;  ELC  exp(G_last - c) per key channel
-//   UT   Ut^T fp32 [128 value channels][64 tokens]
+//   UT   Ut^T fp32 [128 value channels][64 tokens]; in row j the 16-byte
+//        chunk c (tokens 4c .. 4c + 3) sits at chunk position c ^ (j mod 16)
 //   OO   O fp32 [64 tokens][128 value channels] (the chain writes it)
 // Records live in a ring: chunk g, head h uses slot (g mod ring_chunks, h).
 #pragma once
@@ -103,6 +104,10 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ float sigmoid_fast(float x) {
     return rcp_approx(1.0f + ex2_approx(-x * 1.4426950408889634f));
 }
+
+// Chunk position of tokens 4c .. 4c + 3 in row j of the record's Ut^T (the
+// XOR spreads the rows a warp writes over all shared-memory banks).
+__host__ __device__ __forceinline__ uint32_t ut_chunk(int j, int c) { return uint32_t(c ^ (j & 15)); }
 
 __device__ __forceinline__ char *rec_ptr(const PrefillParams &p, int g, int h) {
     return p.rec + (size_t(g % p.ring_chunks) * p.H + h) * Rec::BYTES;

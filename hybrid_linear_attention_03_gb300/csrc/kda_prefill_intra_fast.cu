@@ -65,6 +65,7 @@ constexpr uint32_t SCAN = IDN + 8192, TD = SCAN, XS = SCAN + 4096;
 constexpr uint32_t SMALL = SCAN + 8192;
 constexpr uint32_t LNM = SMALL, CREF = SMALL + 512, EC = SMALL + 1024, G0 = SMALL + 1536, BETA = SMALL + 2048;
 constexpr uint32_t BARS = SMALL + 2304, TBASE = BARS + 64;
+constexpr uint32_t PPS = RV;            // P image staging (hi, lo at +8192) once the v pass has consumed raw v
 constexpr uint32_t BYTES = SMALL + 2560;
 static_assert(RK >= RQ + TILE && RA >= RK + TILE && RV >= RA + CH * D * 2 && X >= RV + TILE, "raw tiles overlap");
 static_assert(VIMG_LO + 16384 <= RA, "the v image overlaps the alpha tile");
@@ -172,20 +173,22 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
                                                                     const __grid_constant__ CUtensorMap tm_v,
                                                                     const __grid_constant__ CUtensorMap tm_a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1 KiB-aligned base, kept a shared-memory pointer (offset, not an integer round trip)
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *lnm = reinterpret_cast<float *>(sm + fs::LNM);
     float *cref = reinterpret_cast<float *>(sm + fs::CREF);
     float *ec = reinterpret_cast<float *>(sm + fs::EC);
     float *g0s = reinterpret_cast<float *>(sm + fs::G0);
     float *beta = reinterpret_cast<float *>(sm + fs::BETA);
-    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + fs::BARS);
-    uint64_t *bar_v = bar_ld + 1, *bar_a = bar_ld + 2, *bar_t = bar_ld + 3, *bar_w = bar_ld + 4;
+    uint64_t *bar_a_ld = reinterpret_cast<uint64_t *>(sm + fs::BARS);  // alpha tile
+    uint64_t *bar_qk = bar_a_ld + 1, *bar_v = bar_a_ld + 2;          // q, k tiles; v tile
+    uint64_t *bar_m1 = bar_a_ld + 3, *bar_t = bar_a_ld + 4, *bar_m2 = bar_a_ld + 5;  // MMA groups
     uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + fs::TBASE);
     float *scan = reinterpret_cast<float *>(sm + fs::SCAN);
-    float *At = reinterpret_cast<float *>(sm + fs::AT);  // At[s * 64 + r] = A_rs
-    float *T = reinterpret_cast<float *>(sm + fs::TT);   // T[r * 64 + s]
-    float *TD = reinterpret_cast<float *>(sm + fs::TD);  // TD[(a * 16 + s) * 16 + r] = T[16 a + r][16 a + s]
-    float *XS = reinterpret_cast<float *>(sm + fs::XS);
+    float *At = reinterpret_cast<float *>(sm + fs::AT);   // At[s * 64 + r] = A_rs
+    float *Tt = reinterpret_cast<float *>(sm + fs::TT);   // Tt[s * 64 + r] = T_rs
+    float *XS = reinterpret_cast<float *>(sm + fs::SCAN);        // level 1: [2][16 j][16 i]
+    float *X2t = reinterpret_cast<float *>(sm + fs::SCAN + 2048);  // level 2: [32 j][32 i]
     const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const ChunkMeta cm = p.chunks[g];
     if (cm.len <= 0) return;  // a padding entry of a device-built table: no chunk here
@@ -193,12 +196,13 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     char *rec = rec_ptr(p, g, h);
     const uint32_t sbase = smem_u32(sm);
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(bar_ld + b, 1);
+        for (int b = 0; b < 6; ++b) mbar_init(bar_a_ld + b, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_ld, 2 * fs::TILE + uint32_t(CH * D * 2));
-        tma_load_3d(sm + fs::RQ, &tm_q, bar_ld, 0, h, cm.row0 - HALO);
-        tma_load_3d(sm + fs::RK, &tm_k, bar_ld, 0, h, cm.row0 - HALO);
-        tma_load_3d(sm + fs::RA, &tm_a, bar_ld, 0, h, cm.row0);
+        mbar_arrive_expect_tx(bar_a_ld, uint32_t(CH * D * 2));  // alpha first: the decay pass needs it alone
+        tma_load_3d(sm + fs::RA, &tm_a, bar_a_ld, 0, h, cm.row0);
+        mbar_arrive_expect_tx(bar_qk, 2 * fs::TILE);
+        tma_load_3d(sm + fs::RK, &tm_k, bar_qk, 0, h, cm.row0 - HALO);
+        tma_load_3d(sm + fs::RQ, &tm_q, bar_qk, 0, h, cm.row0 - HALO);
         mbar_arrive_expect_tx(bar_v, fs::TILE);
         tma_load_3d(sm + fs::RV, &tm_v, bar_v, 0, h, cm.row0 - HALO);
     }
@@ -217,11 +221,11 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tbase;
-    bool ok = __syncthreads_and(mbar_wait(bar_ld, 0, p.err));
+    bool ok = __syncthreads_and(mbar_wait(bar_a_ld, 0, p.err));
 
     // This thread's unit: tokens r0, r0 + 1 (pair pr) x channels ch0 .. ch0 + 7.
     // A warp holds pairs 2 warp (lanes 0-15) and 2 warp + 1 (lanes 16-31).
-    const int pr = 2 * warp + (lane >> 4), cb = lane & 15, r0 = 2 * pr, ch0 = 8 * cb;
+    const int pr = tid >> 4, cb = tid & 15, r0 = 2 * pr, ch0 = 8 * cb;
     const __nv_bfloat16 *tail =
         sq.has_init ? static_cast<const __nv_bfloat16 *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch + size_t(h) * D : nullptr;
 
@@ -279,7 +283,8 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     if (!ok || exact) {
         // a chunk this kernel cannot take: the generic kernel's list gets it
         if (ok && tid == 0) p.fb_list[atomicAdd(p.fb_count, 1u)] = uint32_t(g) * uint32_t(p.H) + uint32_t(h);
-        mbar_wait(bar_v, 0, p.err);  // no copy may land after the CTA is gone
+        mbar_wait(bar_qk, 0, p.err);  // no copy may land after the CTA is gone
+        mbar_wait(bar_v, 0, p.err);
         tc_fence_before();
         __syncthreads();
         if (warp == 0) tmem_dealloc(tm, 256);
@@ -296,9 +301,10 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             E1[e] = ex2_approx((pre[e] + gB[e] - cc[e]) * kLog2e);
         }
     }
+    ok = __syncthreads_and(mbar_wait(bar_qk, 0, p.err));
 
     // ---- k pass: K~ = k^ E (X rows r), K^ = k^ / E (KB rows r) ---------------
-    {
+    if (ok) {
         float y[2][8];
         conv_pair(sm + fs::RK, p, 1, h, ch0, r0, cm.pos0, cm.len, tail, y);
         l2_pair(y, p.eps_l2);
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         }
     }
     // ---- q pass: Q~ = q^ E (X rows 64 + r) -----------------------------------
-    {
+    if (ok) {
         float y[2][8];
         conv_pair(sm + fs::RQ, p, 0, h, ch0, r0, cm.pos0, cm.len, tail, y);
         l2_pair(y, p.eps_l2);
@@ -330,36 +336,44 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) {
-        const Operand xop{sbase + fs::X, sbase + fs::X_LO, false, 2 * CH * 128};
-        const Operand kbop{sbase + fs::KB, sbase + fs::KB_LO, false, CH * 128};
-        mma_split(tm, xop, kbop, D, idesc_bf16_f32(128, CH), 3, false);  // [A; P] (unmasked)
-        mma_commit(bar_a);
-        // Q~^T: Q~ (X rows 64..127) read MN-major times the identity; hi + lo is exact
-        const Operand qt{sbase + fs::X + CH * 128, sbase + fs::X_LO + CH * 128, true, 2 * CH * 128};
-        const Operand id{sbase + fs::IDN, sbase + fs::IDN, false, CH * 128};
-        mma_split(tm + 64, qt, id, CH, idesc_bf16_f32(128, CH, true, false), 2, false);
-        mma_commit(bar_t);
-        // K^ image -> record (the chain's operand), while the MMAs run
-        bulk_store(rec + Rec::KH_HI, sm + fs::KB, 16384);
-        bulk_store(rec + Rec::KH_LO, sm + fs::KB_LO, 16384);
-        bulk_commit();
+    if (warp == 0) {
+        // warp 0 issues the MMAs (the issuing lane stalls while the tensor core
+        // works through them); the other warps form v meanwhile
+        if (lane == 0 && ok) {
+            // K^ image -> record (the chain's operand)
+            bulk_store(rec + Rec::KH_HI, sm + fs::KB, 16384);
+            bulk_store(rec + Rec::KH_LO, sm + fs::KB_LO, 16384);
+            bulk_commit();
+            const Operand xop{sbase + fs::X, sbase + fs::X_LO, false, 2 * CH * 128};
+            const Operand kbop{sbase + fs::KB, sbase + fs::KB_LO, false, CH * 128};
+            mma_split(tm, xop, kbop, D, idesc_bf16_f32(128, CH), 3, false);  // [A; P] (unmasked)
+            mma_commit(bar_m1);
+            // Q~^T: Q~ (X rows 64..127) read MN-major times the identity; hi + lo is exact
+            const Operand qt{sbase + fs::X + CH * 128, sbase + fs::X_LO + CH * 128, true, 2 * CH * 128};
+            const Operand id{sbase + fs::IDN, sbase + fs::IDN, false, CH * 128};
+            mma_split(tm + 64, qt, id, CH, idesc_bf16_f32(128, CH, true, false), 2, false);
+            mma_commit(bar_t);
+        }
+        __syncwarp();
     }
-    // ---- v pass (under the MMAs): v image over the raw q, k tiles ------------
+    // ---- v pass (under the MMAs, warps 1..15): v image over the raw q, k tiles
     bool okv = mbar_wait(bar_v, 0, p.err);
-    if (okv) {
-        float y[2][8];
-        conv_pair(sm + fs::RV, p, 2, h, ch0, r0, cm.pos0, cm.len, tail, y);
+    if (okv && warp != 0) {
+        for (int u = tid - 32; u < 512; u += 480) {  // warp 1 also takes units 480..511
+            const int vpr = u >> 4, vcb = u & 15;
+            float y[2][8];
+            conv_pair(sm + fs::RV, p, 2, h, 8 * vcb, 2 * vpr, cm.pos0, cm.len, tail, y);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) store_split(sm + fs::VIMG, sm + fs::VIMG_LO, sw128_chunk(r0 + q, cb, CH), y[q]);
+            for (int q = 0; q < 2; ++q) store_split(sm + fs::VIMG, sm + fs::VIMG_LO, sw128_chunk(2 * vpr + q, vcb, CH), y[q]);
+        }
     }
-    okv = okv && mbar_wait(bar_a, 0, p.err);
-    if (tid == 0) bulk_wait_read();  // KB becomes A^T and T below
-    ok = __syncthreads_and(okv);
+    okv = okv && mbar_wait(bar_m1, 0, p.err);
+    if (tid == 0) bulk_wait_read();  // KB becomes A^T and T^T below
+    ok = __syncthreads_and(ok && okv);
     tc_fence_after();
     const int qd = warp & 3, cs = (warp >> 2) * 16;  // TMEM lane quarter, 16-column slice
     if (ok) {
-        // ---- A^T (s < r, times beta_r) -> smem; P (s <= r) -> record --------
+        // ---- A^T (s < r, times beta_r) -> smem; P (s <= r) -> staging (RV) -----
         float v[16];
         tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cs, v);
         tmem_wait_ld();
@@ -375,17 +389,23 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = (cs + 8 * hh + e <= r) ? v[8 * hh + e] : 0.f;
-                store_split(reinterpret_cast<unsigned char *>(rec + Rec::PP_HI), reinterpret_cast<unsigned char *>(rec + Rec::PP_LO),
-                            sw128_chunk(r, (cs >> 3) + hh, CH), x);
+                store_split(sm + fs::PPS, sm + fs::PPS + 8192, sw128_chunk(r, (cs >> 3) + hh, CH), x);
             }
         }
+        // T^T starts at zero: the blocks above the diagonal stay zero
+        for (int e = tid; e < CH * CH / 4; e += fs::NT) reinterpret_cast<float4 *>(Tt)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && ok) {
+        bulk_store(rec + Rec::PP_HI, sm + fs::PPS, 16384);  // PP_HI, PP_LO are adjacent
+        bulk_commit();
+    }
     bool okt = true;
     if (ok && warp < 2) {
         // ---- diagonal 16 x 16 blocks of T by forward substitution: lane =
-        // column c of block b, the column in registers
+        // column c of block b, the column in registers -> T^T row 16 b + c
         const int b = tid >> 4, c = tid & 15, b16 = 16 * b;
         float tc[16];
 #pragma unroll
@@ -395,14 +415,13 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             for (int k = 0; k < r; ++k) acc = fmaf(-At[(b16 + k) * CH + b16 + r], tc[k], acc);
             tc[r] = acc;
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) T[(b16 + r) * CH + b16 + c] = tc[r];
+        float *dst = Tt + (b16 + c) * CH + b16;
 #pragma unroll
         for (int r4 = 0; r4 < 16; r4 += 4)
-            *reinterpret_cast<float4 *>(TD + (b16 + c) * 16 + r4) = make_float4(tc[r4], tc[r4 + 1], tc[r4 + 2], tc[r4 + 3]);
+            *reinterpret_cast<float4 *>(dst + r4) = make_float4(tc[r4], tc[r4 + 1], tc[r4 + 2], tc[r4 + 3]);
     } else if (ok) {
-        // ---- meanwhile (exp(G) . q)^T rows = exp(c_i) Q~^T -> record WQ block 1;
-        // the 16 (quarter, slice) units over warps 2..15
+        // ---- meanwhile (exp(G) . q)^T rows = exp(c_i) Q~^T -> staging; the 16
+        // (quarter, slice) units over warps 2..15
         okt = mbar_wait(bar_t, 0, p.err);
         tc_fence_after();
         if (okt) {
@@ -410,6 +429,9 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             const int nk = (qd < 2 && k0 == 2) ? 2 : 1;
             const int i = qd * 32 + lane;
             const float e_c = ec[i];
+            // hi image rows -> RA; lo image rows 0..63 / 64..127 -> the Q~ rows of X's second K block
+            unsigned char *hi = sm + fs::RA;
+            unsigned char *lo = (i < CH) ? sm + fs::X + 3 * CH * 128 : sm + fs::X_LO + 3 * CH * 128 - CH * 128;
             for (int k = k0; k < k0 + nk; ++k) {
                 float v[16];
                 tmem_ld16(tm + (uint32_t(qd * 32) << 16) + 64 + 16 * k, v);
@@ -419,86 +441,95 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = v[8 * hh + e] * e_c;
-                    store_split(reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI + Rec::WQ_BLOCK),
-                                reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO + Rec::WQ_BLOCK), sw128_chunk(i, 2 * k + hh, D), x);
+                    uint4 vh, vl;
+                    split8(x, vh, vl);
+                    const uint32_t off = sw128_chunk(i, 2 * k + hh, D);
+                    *reinterpret_cast<uint4 *>(hi + off) = vh;
+                    *reinterpret_cast<uint4 *>(lo + off) = vl;
                 }
             }
-        }
-    }
-    ok = __syncthreads_and(ok && okt);
-    // ---- off-diagonal blocks, by distance d: T_ab = -T_aa sum_{b <= c < a} A_ac T_cb
-    if (ok) {
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * d * 64; e += fs::NT) {  // partial products A_ac T_cb
-                const int q4 = (e & 3) * 4, r = (e >> 2) & 15, bt = e >> 6;
-                const int blk = bt / d, c = blk + (bt - blk * d), a = blk + d;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float av = At[(16 * c + k) * CH + 16 * a + r];
-                    const float4 tv = ld4(T + (16 * c + k) * CH + 16 * blk + q4);
-                    acc.x = fmaf(av, tv.x, acc.x);
-                    acc.y = fmaf(av, tv.y, acc.y);
-                    acc.z = fmaf(av, tv.z, acc.z);
-                    acc.w = fmaf(av, tv.w, acc.w);
-                }
-                *reinterpret_cast<float4 *>(XS + (bt * 16 + r) * 16 + q4) = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nblk * 64; e += fs::NT) {  // T_ab = -T_aa X_ab
-                const int q4 = (e & 3) * 4, r = (e >> 2) & 15, blk = e >> 6, a = blk + d;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float tv = -TD[(16 * a + k) * 16 + r];
-                    float4 xv = ld4(XS + ((blk * d) * 16 + k) * 16 + q4);
-                    for (int t = 1; t < d; ++t) {
-                        const float4 x2 = ld4(XS + ((blk * d + t) * 16 + k) * 16 + q4);
-                        xv.x += x2.x;
-                        xv.y += x2.y;
-                        xv.z += x2.z;
-                        xv.w += x2.w;
-                    }
-                    acc.x = fmaf(tv, xv.x, acc.x);
-                    acc.y = fmaf(tv, xv.y, acc.y);
-                    acc.z = fmaf(tv, xv.z, acc.z);
-                    acc.w = fmaf(tv, xv.w, acc.w);
-                }
-                *reinterpret_cast<float4 *>(T + (16 * a + r) * CH + 16 * blk + q4) = acc;
-            }
-            __syncthreads();
-        }
-        // ---- (T diag beta) image [64 r][64 s] (s <= r), over Q~'s first K block
-        {
-            const int r = tid >> 3, c = tid & 7;
-            float t8[8], b8[8], x[8];
-            ld8(T + r * CH + 8 * c, t8);
-            ld8(beta + 8 * c, b8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = (8 * c + e <= r) ? t8[e] * b8[e] : 0.f;
-            store_split(sm + fs::TB, sm + fs::TB_LO, sw128_chunk(r, c, CH), x);
         }
     }
     fence_proxy_async_smem();
     tc_fence_before();
+    ok = __syncthreads_and(ok && okt);
+    if (tid == 0 && ok) {
+        bulk_store(rec + Rec::WQ_HI + Rec::WQ_BLOCK, sm + fs::RA, 16384);
+        bulk_store(rec + Rec::WQ_LO + Rec::WQ_BLOCK, sm + fs::X + 3 * CH * 128, 8192);
+        bulk_store(rec + Rec::WQ_LO + Rec::WQ_BLOCK + 8192, sm + fs::X_LO + 3 * CH * 128, 8192);
+        bulk_commit();
+    }
+    if (ok) {
+        // ---- level 1: T_ab = -T_aa A_ab T_bb for (a, b) = (1, 0), (3, 2) ------
+        {
+            const int blk = tid >> 8, j = (tid >> 4) & 15, i = tid & 15;
+            const int a16 = 16 * (2 * blk + 1), b16 = a16 - 16;
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc = fmaf(At[(b16 + k) * CH + a16 + i], Tt[(b16 + j) * CH + b16 + k], acc);
+            XS[blk * 256 + j * 16 + i] = acc;
+            __syncthreads();
+            float t = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) t = fmaf(Tt[(a16 + k) * CH + a16 + i], XS[blk * 256 + j * 16 + k], t);
+            Tt[(b16 + j) * CH + a16 + i] = -t;
+        }
+        __syncthreads();
+        // ---- level 2: T_21 = -T_22 A_21 T_11 on 32 x 32 blocks -----------------
+        {
+            const int i = lane, j0 = 2 * warp;
+            float x0 = 0.f, x1 = 0.f;
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float av = At[k * CH + 32 + i];
+                x0 = fmaf(av, Tt[j0 * CH + k], x0);
+                x1 = fmaf(av, Tt[(j0 + 1) * CH + k], x1);
+            }
+            X2t[j0 * 32 + i] = x0;
+            X2t[(j0 + 1) * 32 + i] = x1;
+            __syncthreads();
+            float t0 = 0.f, t1 = 0.f;
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float tv = Tt[(32 + k) * CH + 32 + i];
+                t0 = fmaf(tv, X2t[j0 * 32 + k], t0);
+                t1 = fmaf(tv, X2t[(j0 + 1) * 32 + k], t1);
+            }
+            Tt[j0 * CH + 32 + i] = -t0;
+            Tt[(j0 + 1) * CH + 32 + i] = -t1;
+        }
+        __syncthreads();
+        // ---- (T diag beta)^T image: row s holds beta_s T_rs for r = 0..63,
+        // MMA 2's B operand read MN-major; over Q~'s first K block
+        {
+            const int s_ = tid >> 3, c = tid & 7;
+            float t8[8], x[8];
+            ld8(Tt + s_ * CH + 8 * c, t8);
+            const float bs = beta[s_];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = t8[e] * bs;
+            store_split(sm + fs::TB, sm + fs::TB_LO, sw128_chunk(s_, c, CH), x);
+        }
+    }
+    if (tid == 0) bulk_wait_read();  // the staged P and Q^T images are read before X is staged over
+    fence_proxy_async_smem();
+    tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && ok) {
-        // W^T / exp(c) = K~^T (T diag beta)^T and Ut^T = V^T (T diag beta)^T: K~ and V read MN-major
+    if (warp == 0 && lane == 0 && ok) {
+        // W^T / exp(c) = K~^T (T diag beta)^T and Ut^T = V^T (T diag beta)^T: K~, V and (T diag beta)^T read MN-major
         const Operand kt{sbase + fs::X, sbase + fs::X_LO, true, 2 * CH * 128};
         const Operand vt{sbase + fs::VIMG, sbase + fs::VIMG_LO, true, CH * 128};
-        const Operand tb{sbase + fs::TB, sbase + fs::TB_LO, false, CH * 128};
-        const uint32_t id = idesc_bf16_f32(128, CH, true, false);
+        const Operand tb{sbase + fs::TB, sbase + fs::TB_LO, true, CH * 128};
+        const uint32_t id = idesc_bf16_f32(128, CH, true, true);
         mma_split(tm, kt, tb, CH, id, 3, false);
         mma_split(tm + 128, vt, tb, CH, id, 3, false);
-        mma_commit(bar_w);
+        mma_commit(bar_m2);
     }
-    ok = __syncthreads_and(ok && mbar_wait(bar_w, 0, p.err));
+    ok = __syncthreads_and(ok && mbar_wait(bar_m2, 0, p.err));
     tc_fence_after();
     if (ok) {
-        // ---- W^T row i (times exp(c_i)) and Ut^T row j = i -> record ---------
+        // ---- W^T row i (times exp(c_i)) and Ut^T row j = i -> staging in X ----
         const int i = qd * 32 + lane;
         float w[16], u[16];
         tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cs, w);
@@ -510,15 +541,24 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = w[8 * hh + e] * e_c;
-            store_split(reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI), reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO),
-                        sw128_chunk(i, (cs >> 3) + hh, D), x);
+            store_split(sm + fs::X, sm + fs::X + 16384, sw128_chunk(i, (cs >> 3) + hh, D), x);
         }
-        float *ut = at<float>(rec, Rec::UT) + size_t(i) * CH + cs;
+        unsigned char *ut = sm + fs::X_LO + i * (CH * 4);
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4 *>(ut + e) = make_float4(u[e], u[e + 1], u[e + 2], u[e + 3]);
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4 *>(ut + (ut_chunk(i, (cs >> 2) + q) << 4)) =
+                make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && ok) {
+        bulk_store(rec + Rec::WQ_HI, sm + fs::X, 16384);
+        bulk_store(rec + Rec::WQ_LO, sm + fs::X + 16384, 16384);
+        bulk_store(rec + Rec::UT, sm + fs::X_LO, 32768);
+        bulk_commit();
+        bulk_wait_read();  // shared memory stays until the copies have read it
+    }
     if (warp == 0) tmem_dealloc(tm, 256);
 }
 

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_generic_kernel(const 
     static_assert(is::map_ok<Act>(), "intra shared-memory map overlaps");
     static_assert(CH % (16 * is::QW) == 0 && is::NT >= 4 * D, "drain split / thread roles need these");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KiB-aligned, still shared
     float *cref = reinterpret_cast<float *>(sm + is::SMALL);  // [128] c = mid of the log-decay range
     float *beta = cref + D;                                    // [64]
     int *flag = reinterpret_cast<int *>(beta + CH);            // [1]
@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_generic_kernel(const 
             }
 #pragma unroll
             for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4 *>(UT + c0 + e) = make_float4(u[e], u[e + 1], u[e + 2], u[e + 3]);
+                *reinterpret_cast<float4 *>(UT + 4 * ut_chunk(i, (c0 + e) >> 2)) = make_float4(u[e], u[e + 1], u[e + 2], u[e + 3]);
         }
     }
     ph ^= 1;
