@@ -68,12 +68,14 @@ constexpr uint32_t BYTES = BARS + 512;
 static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
 
 // One CTA (8 warps) per (sequence, head), walking the window's chunks in
-// order.  TMEM columns: [(W S)^T | (Q S)^T] [0,128), (K^ elc-free K^T U)^T
-// [128,256), (P U)^T [256,320), S^T [320,448).
-//   stage 1  [(W S)^T | (Q S)^T] = S^T [W^T | Q^T]: the record's WQ read MN-major
+// order.  TMEM columns: [(W S)^T | (Q S)^T] [0,128), (K^^T U)^T [128,256),
+// (P U)^T [256,320), S^T [320,448).
+//   stage 1  [(W S)^T | (Q S)^T] = S^T [W; Q]^T (the record's WQ, K-major)
 //   U^T      = Ut^T - (W S)^T, split into hi / lo images
-//   stage 2  (K^T U)^T = U^T K^ (K^ read MN-major), (P U)^T = U^T P^T
-//   S^T     <- S^T diag(gamma) + (K^T U)^T diag(elc),  O^T = (Q S)^T + (P U)^T
+//   stage 2  (K^^T U)^T = U^T K^ (K^ read MN-major), (P U)^T = U^T P^T
+//   S^T     <- S^T diag(gamma) + (K^^T U)^T diag(elc),  O^T = (Q S)^T + (P U)^T
+// Without the lo halves of Q and P (q_lo = 0, bf16 outputs) the Q rows of
+// the WQ lo image stay zero in shared memory and (P U)^T takes one product.
 __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KiB-aligned, still shared
@@ -108,13 +110,29 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tbase, tl = tm + (uint32_t((warp & 3) * 32) << 16);
-    if (tid == 0 && c_hi > c_lo) {
-        const char *r0 = rec_ptr(p, sq.chunk0 + c_lo, h);
-        mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
-        bulk_load(sm + cs::B1, r0 + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
-        mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
-        bulk_load(sm + cs::B2, r0 + Rec::KH_HI, Rec::B2_BYTES, bar_b2);
+    // the record's WQ images (without the Q rows' lo half unless q_lo) and
+    // KH, PP, GAM, ELC (without PP lo unless q_lo) of chunk g
+    const uint32_t b1_bytes = p.q_lo ? Rec::B1_BYTES : 32768u + 16384u;
+    const uint32_t b2_bytes = p.q_lo ? Rec::B2_BYTES : Rec::B2_BYTES_HI;
+    auto load_rec = [&](const char *r) {
+        mbar_arrive_expect_tx(bar_b1, b1_bytes);
+        if (p.q_lo) {
+            bulk_load(sm + cs::B1, r + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
+        } else {  // hi image, then the W rows (0..63) of both K blocks of the lo image
+            bulk_load(sm + cs::WQ_HI, r + Rec::WQ_HI, 32768, bar_b1);
+            bulk_load(sm + cs::WQ_LO, r + Rec::WQ_LO, 8192, bar_b1);
+            bulk_load(sm + cs::WQ_LO + 16384, r + Rec::WQ_LO + 16384, 8192, bar_b1);
+        }
+        mbar_arrive_expect_tx(bar_b2, b2_bytes);
+        bulk_load(sm + cs::B2, r + Rec::KH_HI, b2_bytes, bar_b2);
+    };
+    if (!p.q_lo) {  // the Q rows (64..127) of both K blocks of the WQ lo image stay zero
+        for (int e = tid; e < 2 * 8192 / 16; e += 256) {
+            const int kb = e >> 9, off = (e & 511) * 16;
+            *reinterpret_cast<uint4 *>(sm + cs::WQ_LO + kb * 16384 + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
+    if (tid == 0 && c_hi > c_lo) load_rec(rec_ptr(p, sq.chunk0 + c_lo, h));
     const int sc0 = half * 64;  // this thread's 64 columns of the S^T row
     // S^T row j: fp32 into TMEM, hi/lo into the A1 images
     for (int c0 = sc0; c0 < sc0 + 64; c0 += 16) {
@@ -143,10 +161,10 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
     __syncthreads();
     tc_fence_after();
     bool ok = true;
-    const uint32_t id_s1 = idesc_bf16_f32(128, 2 * CH, false, true), id_kh = idesc_bf16_f32(128, D, false, true),
+    const uint32_t id_s1 = idesc_bf16_f32(128, 2 * CH), id_kh = idesc_bf16_f32(128, D, false, true),
                    id_pp = idesc_bf16_f32(128, CH);
     const Operand s_img{sbase + cs::A1_HI, sbase + cs::A1_LO, false, D * 128};
-    const Operand wq_img{sbase + cs::WQ_HI, sbase + cs::WQ_LO, true, uint32_t(Rec::WQ_BLOCK)};
+    const Operand wq_img{sbase + cs::WQ_HI, sbase + cs::WQ_LO, false, 2 * CH * 128};
     const Operand u_img{sbase + cs::A2_HI, sbase + cs::A2_LO, false, D * 128};
     const Operand kh_img{sbase + cs::KH_HI, sbase + cs::KH_LO, true, CH * 128};
     const Operand pp_img{sbase + cs::PP_HI, sbase + cs::PP_LO, false, CH * 128};
@@ -174,8 +192,15 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         if (!ok) break;
         tc_fence_after();
         if (tid == 0 && c + 1 < c_hi) {  // W and Q images are consumed: stream in the next chunk's
-            mbar_arrive_expect_tx(bar_b1, Rec::B1_BYTES);
-            bulk_load(sm + cs::B1, rec_ptr(p, g + 1, h) + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
+            const char *rn = rec_ptr(p, g + 1, h);
+            mbar_arrive_expect_tx(bar_b1, b1_bytes);
+            if (p.q_lo) {
+                bulk_load(sm + cs::B1, rn + Rec::WQ_HI, Rec::B1_BYTES, bar_b1);
+            } else {
+                bulk_load(sm + cs::WQ_HI, rn + Rec::WQ_HI, 32768, bar_b1);
+                bulk_load(sm + cs::WQ_LO, rn + Rec::WQ_LO, 8192, bar_b1);
+                bulk_load(sm + cs::WQ_LO + 16384, rn + Rec::WQ_LO + 16384, 8192, bar_b1);
+            }
         }
         // U^T row j = Ut^T - (W S)^T  -> hi/lo images (this thread's 32 columns)
         {
@@ -204,15 +229,15 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         tc_fence_after();
         if (tid == 0) {
             mma_split(tm + 128, u_img, kh_img, CH, id_kh, 3, false);
-            mma_split(tm + 256, u_img, pp_img, CH, id_pp, p.pu_products, false);
+            mma_split(tm + 256, u_img, pp_img, CH, id_pp, p.q_lo ? 3 : 1, false);
             mma_commit(bar_m2);
         }
         ok = __syncthreads_and(mbar_wait(bar_m2, par, p.err));
         if (!ok) break;
         tc_fence_after();
         if (tid == 0 && c + 1 < c_hi) {  // K^, P images, gamma and elc consumed
-            mbar_arrive_expect_tx(bar_b2, Rec::B2_BYTES);
-            bulk_load(sm + cs::B2, rec_ptr(p, g + 1, h) + Rec::KH_HI, Rec::B2_BYTES, bar_b2);
+            mbar_arrive_expect_tx(bar_b2, b2_bytes);
+            bulk_load(sm + cs::B2, rec_ptr(p, g + 1, h) + Rec::KH_HI, b2_bytes, bar_b2);
         }
         // O column j (rows uc0 .. uc0 + 31) = (Q S)^T + (P U)^T -> record, coalesced across the warp
         {
@@ -640,7 +665,7 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
     if ((st = set_smem(prefill_chain_kernel, kChainSmem)) != KDA_OK) return st;
     PrefillParams p = p0;
     p.ring_chunks = L.ring_windows * L.window;
-    p.pu_products = kFast ? 1 : 3;  // P U feeds only the output: bf16 outputs take one product
+    p.q_lo = kFast ? 0 : 1;  // exp(G) . q and P feed only the output: bf16 outputs keep their hi halves
     CUtensorMap mq, mk, mv, ma;
     if (n_chunks > 0) {
         const int es = int(sizeof(Act));

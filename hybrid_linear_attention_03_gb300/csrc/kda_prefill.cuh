@@ -6,12 +6,14 @@
 //
 // The record of one (chunk, head) (bytes; "image" = bf16 operand tile in the
 // 128-byte-swizzle layout of kda_sm100.cuh, hi = bf16(x), lo = bf16(x - hi)):
-//   WQ   [W^T | (exp(G) . q)^T]: two 64-token blocks of 128 key-channel rows,
-//        read by the chain MN-major (tokens as N, key channels as K)
+//   WQ   [W; exp(G) . q]: 128 token rows (W rows 0..63, exp(G) . q rows
+//        64..127) x 128 key channels, K-major; the rows of exp(G) . q feed
+//        only the output, so with bf16 outputs their lo half is not kept
+//        (q_lo = 0) and the chain reads zeros there
 //   KH   k^ exp(c - G) [64 tokens][128 key channels], token-major, read by
 //        the chain MN-major; multiplied per channel by ELC it is
 //        k^ exp(G_last - G)
-//   PP   P [64 tokens r][64 tokens s], K-major
+//   PP   P [64 tokens r][64 tokens s], K-major: PP_HI; PP_LO only when q_lo
 //   GAM  exp(G_last) per key channel;  ELC  exp(G_last - c) per key channel
 //   UT   Ut^T fp32 [128 value channels][64 tokens]; in row j the 16-byte
 //        chunk c (tokens 4c .. 4c + 3) sits at chunk position c ^ (j mod 16)
@@ -52,15 +54,17 @@ struct CkptMeta {
 };
 
 struct Rec {
-    static constexpr size_t WQ_HI = 0, WQ_LO = 32768, WQ_BLOCK = 16384;
+    static constexpr size_t WQ_HI = 0, WQ_LO = 32768;
     static constexpr size_t KH_HI = 65536, KH_LO = 81920;
-    static constexpr size_t PP_HI = 98304, PP_LO = 106496;
-    static constexpr size_t GAM = 114688, ELC = GAM + 512;
-    static constexpr size_t UT = GAM + 1024;
+    static constexpr size_t PP_HI = 98304;
+    static constexpr size_t GAM = PP_HI + 8192, ELC = GAM + 512;
+    static constexpr size_t PP_LO = GAM + 1024;
+    static constexpr size_t UT = PP_LO + 8192;
     static constexpr size_t OO = UT + 32768;
     static constexpr size_t BYTES = OO + 32768;
-    static constexpr uint32_t B1_BYTES = uint32_t(KH_HI - WQ_HI);  // WQ images
-    static constexpr uint32_t B2_BYTES = uint32_t(UT - KH_HI);     // KH, PP images, GAM, ELC
+    static constexpr uint32_t B1_BYTES = uint32_t(KH_HI - WQ_HI);     // WQ images
+    static constexpr uint32_t B2_BYTES = uint32_t(UT - KH_HI);        // KH, PP hi, GAM, ELC, PP lo
+    static constexpr uint32_t B2_BYTES_HI = uint32_t(PP_LO - KH_HI);  // the same without PP lo
 };
 static_assert(Rec::BYTES % 1024 == 0, "record keeps 1 KiB alignment");
 
@@ -82,7 +86,7 @@ struct PrefillParams {
     int32_t chunk_base;      // intra, out: global index of blockIdx.x == 0
     int32_t win_lo, win_hi;  // chain: global chunk range of this launch
     int32_t seq_base;        // chain: sequence of blockIdx.x / H == 0
-    int32_t pu_products;     // chain: bf16 products of P U (1: hi.hi; 3: also hi.lo, lo.hi)
+    int32_t q_lo;            // the record keeps the lo halves of exp(G) . q and P (fp32 outputs)
     float eps_l2, eps_rms;
 };
 

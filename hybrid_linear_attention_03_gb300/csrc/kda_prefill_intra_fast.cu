@@ -5,10 +5,10 @@
 // bullet: prefill runs chunked (FlashKDA).  Per (chunk, head), with G_r the
 // cumulative log decay per key channel and c the middle of its range over the
 // chunk, E = exp(G - c), K~ = k^ E, Q~ = q^ E, K^ = k^ / E:
-//   [A; P] = [K~; Q~] K^^T                       (A_rs times beta_r, s < r; P_rs, s <= r)
-//   T = (I + A)^-1                                (blocked, CUDA cores)
-//   W^T = diag(exp(c)) K~^T (T diag(beta))^T      Ut^T = V^T (T diag(beta))^T
-//   (exp(G) . q)^T = diag(exp(c)) Q~^T            (an MMA with the identity)
+//   [A; P] = [K~; Q~] K^^T                  (A_rs times beta_r, s < r; P_rs, s <= r)
+//   T = (I + A)^-1                           (blocked, CUDA cores, kept transposed)
+//   W = (T diag(beta)) K~ diag(exp(c))       Ut^T = V^T (T diag(beta))^T
+//   exp(G) . q = Q~ diag(exp(c))
 // which is the generic kernel's arithmetic with W's factor exp(G) = E exp(c)
 // split so that every operand is one of three images built once.
 //
@@ -18,32 +18,32 @@
 // happen in registers, and each 16-byte chunk is stored once.  The products
 // that need an image transposed read it MN-major (kda_sm100.cuh), so no
 // column-wise pass over shared memory is needed.  The cumulative decay G is a
-// per-warp prefix (one shuffle) plus a scan of the 16 warp totals.
+// per-warp prefix (one shuffle) plus a scan of the 16 warp totals.  Record
+// images leave through shared-memory staging and TMA bulk stores.
 //
 // Phases (bar = CTA barrier):
-//   TMA q, k, alpha (and v)  | identity image, beta, ln table
+//   TMA alpha, then q, k, then v | beta, ln table
 //   G, E (registers) bar scan bar
-//   k pass: K~, K^ images    q pass: Q~ image                        bar
-//   MMA [A; P] -> commit a;  MMA Q~^T -> commit t;  K^ image -> record (bulk)
-//   v pass: v image (under the MMAs)
-//   wait a: A^T -> smem, P -> record                                  bar
-//   diagonal 16 x 16 blocks of T (2 warps) | wait t: Q^T rows -> record (14 warps)  bar
-//   3 levels of off-diagonal blocks (2 bar each);  (T diag beta) image  bar
-//   MMA W^T, Ut^T -> wait: W^T rows, Ut^T rows -> record
+//   k pass: K~, K^ images    q pass: Q~ image, exp(G) . q rows -> record   bar
+//   warp 0: K^ image -> record (bulk), MMA [A; P] | warps 1-15: v image
+//   wait: A^T -> smem, P -> staging, T^T zeroed                         bar
+//   diagonal 16 x 16 blocks of T (2 warps)                               bar
+//   2 levels of off-diagonal blocks (32-blocks, 2 bar each); (T diag beta)^T image  bar
+//   MMA W, Ut^T -> wait: W rows, Ut^T rows -> staging -> record (bulk)
 // A chunk whose decay span exceeds kSafeSpanFast is appended to the fallback
 // list and left to the generic kernel.
 //
-// Shared memory (bytes from a 1 KiB-aligned base), 182 KiB, one CTA per SM:
-//   RQ, RK, RA, RV  raw q, k (67 rows), alpha (64 rows), v (67 rows) tiles
+// Shared memory (bytes from a 1 KiB-aligned base), about 174 KiB, one CTA per SM:
+//   RQ, RK, RA, RV  raw q, k (67 rows), alpha (64 rows), v (67 rows) tiles; RV
+//                   later stages the P image
 //   VIMG            v image hi / lo [64 s][128 j], over RQ / RK after the q pass
 //   X               [K~; Q~] image hi / lo [128][128]; the rows of Q~ in its
-//                   first K block later hold the (T diag beta) image
-//   KB              K^ image hi / lo [64][128]; after MMA 1, A^T and T fp32 [64][64]
-//   IDN             identity [64][64] bf16
-//   SCAN            warp totals of G; later TD (T's diagonal blocks, transposed)
-//                   and XS (partial products of the off-diagonal levels)
+//                   first K block later hold the (T diag beta)^T image; after
+//                   the last MMA, the W and Ut^T staging
+//   KB              K^ image hi / lo [64][128]; after MMA 1, A^T and T^T fp32 [64][64]
+//   SCAN            warp totals of G; later the level products
 //   SMALL           ln table, c, exp(c), G_0, beta, mbarriers
-// Tensor memory (256 columns): [0, 64) [A; P], then W^T; [64, 128) Q~^T;
+// Tensor memory (256 columns): [0, 64) [A; P], then [0, 128) W (lanes 0..63);
 // [128, 192) Ut^T.
 #include "kda_prefill.cuh"
 
@@ -60,8 +60,7 @@ constexpr uint32_t X = 68608, X_LO = X + 32768;
 constexpr uint32_t KB = X + 65536, KB_LO = KB + 16384;
 constexpr uint32_t AT = KB, TT = KB + 16384;
 constexpr uint32_t TB = X + 8192, TB_LO = X_LO + 8192;
-constexpr uint32_t IDN = KB + 32768;
-constexpr uint32_t SCAN = IDN + 8192, TD = SCAN, XS = SCAN + 4096;
+constexpr uint32_t SCAN = KB + 32768;
 constexpr uint32_t SMALL = SCAN + 8192;
 constexpr uint32_t LNM = SMALL, CREF = SMALL + 512, EC = SMALL + 1024, G0 = SMALL + 1536, BETA = SMALL + 2048;
 constexpr uint32_t BARS = SMALL + 2304, TBASE = BARS + 64;
@@ -69,7 +68,7 @@ constexpr uint32_t PPS = RV;            // P image staging (hi, lo at +8192) onc
 constexpr uint32_t BYTES = SMALL + 2560;
 static_assert(RK >= RQ + TILE && RA >= RK + TILE && RV >= RA + CH * D * 2 && X >= RV + TILE, "raw tiles overlap");
 static_assert(VIMG_LO + 16384 <= RA, "the v image overlaps the alpha tile");
-static_assert(X % 1024 == 0 && KB % 1024 == 0 && IDN % 1024 == 0 && TB % 1024 == 0, "images need 1 KiB alignment");
+static_assert(X % 1024 == 0 && KB % 1024 == 0 && TB % 1024 == 0, "images need 1 KiB alignment");
 static_assert(BYTES + 1024 <= 232448, "shared memory");
 }  // namespace fs
 
@@ -182,7 +181,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     float *beta = reinterpret_cast<float *>(sm + fs::BETA);
     uint64_t *bar_a_ld = reinterpret_cast<uint64_t *>(sm + fs::BARS);  // alpha tile
     uint64_t *bar_qk = bar_a_ld + 1, *bar_v = bar_a_ld + 2;          // q, k tiles; v tile
-    uint64_t *bar_m1 = bar_a_ld + 3, *bar_t = bar_a_ld + 4, *bar_m2 = bar_a_ld + 5;  // MMA groups
+    uint64_t *bar_m1 = bar_a_ld + 3, *bar_m2 = bar_a_ld + 4;  // MMA groups
     uint32_t *tbase = reinterpret_cast<uint32_t *>(sm + fs::TBASE);
     float *scan = reinterpret_cast<float *>(sm + fs::SCAN);
     float *At = reinterpret_cast<float *>(sm + fs::AT);   // At[s * 64 + r] = A_rs
@@ -196,7 +195,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     char *rec = rec_ptr(p, g, h);
     const uint32_t sbase = smem_u32(sm);
     if (tid == 0) {
-        for (int b = 0; b < 6; ++b) mbar_init(bar_a_ld + b, 1);
+        for (int b = 0; b < 5; ++b) mbar_init(bar_a_ld + b, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(bar_a_ld, uint32_t(CH * D * 2));  // alpha first: the decay pass needs it alone
         tma_load_3d(sm + fs::RA, &tm_a, bar_a_ld, 0, h, cm.row0);
@@ -210,12 +209,6 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         beta[tid] = tid < cm.len ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[size_t(cm.row0 + tid) * p.H + h])
                                  : 0.f;
     if (tid < 128) lnm[tid] = logf(1.0f + float(tid) * (1.0f / 128.0f));  // ln of the bf16 mantissas 1 + m/128
-    {   // identity [64 r][64 s]: chunk (r, c) holds s = 8c .. 8c + 7; bf16 1.0 is 0x3F80
-        const int r = tid >> 3, c = tid & 7, e = r & 7;
-        const uint32_t one = ((r >> 3) == c) ? ((r & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
-        *reinterpret_cast<uint4 *>(sm + fs::IDN + sw128_chunk(r, c, CH)) =
-            make_uint4((e >> 1) == 0 ? one : 0u, (e >> 1) == 1 ? one : 0u, (e >> 1) == 2 ? one : 0u, (e >> 1) == 3 ? one : 0u);
-    }
     if (warp == 0) tmem_alloc(tbase, 256);
     tc_fence_before();
     __syncthreads();
@@ -319,9 +312,12 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             store_split(sm + fs::KB, sm + fs::KB_LO, sw128_chunk(r0 + q, cb, CH), x);
         }
     }
-    // ---- q pass: Q~ = q^ E (X rows 64 + r) -----------------------------------
+    // ---- q pass: Q~ = q^ E (X rows 64 + r); exp(G) . q = Q~ exp(c) -> record
+    // WQ rows 64 + r, hi half only (it feeds only the output); a warp's lanes
+    // cover whole rows, so the stores are coalesced
     if (ok) {
-        float y[2][8];
+        float y[2][8], e_c[8];
+        ld8(ec + ch0, e_c);
         conv_pair(sm + fs::RQ, p, 0, h, ch0, r0, cm.pos0, cm.len, tail, y);
         l2_pair(y, p.eps_l2);
 #pragma unroll
@@ -330,6 +326,11 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = y[q][e] * (q ? E1[e] : E0[e]);
             store_split(sm + fs::X, sm + fs::X_LO, sw128_chunk(CH + r0 + q, cb, 2 * CH), x);
+            uint4 vh, vl;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] *= e_c[e];
+            split8(x, vh, vl);
+            *reinterpret_cast<uint4 *>(rec + Rec::WQ_HI + sw128_chunk(CH + r0 + q, cb, 2 * CH)) = vh;
         }
     }
     fence_proxy_async_smem();
@@ -348,11 +349,6 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             const Operand kbop{sbase + fs::KB, sbase + fs::KB_LO, false, CH * 128};
             mma_split(tm, xop, kbop, D, idesc_bf16_f32(128, CH), 3, false);  // [A; P] (unmasked)
             mma_commit(bar_m1);
-            // Q~^T: Q~ (X rows 64..127) read MN-major times the identity; hi + lo is exact
-            const Operand qt{sbase + fs::X + CH * 128, sbase + fs::X_LO + CH * 128, true, 2 * CH * 128};
-            const Operand id{sbase + fs::IDN, sbase + fs::IDN, false, CH * 128};
-            mma_split(tm + 64, qt, id, CH, idesc_bf16_f32(128, CH, true, false), 2, false);
-            mma_commit(bar_t);
         }
         __syncwarp();
     }
@@ -385,11 +381,13 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         } else {
             const int r = (qd - 2) * 32 + lane;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+            for (int hh = 0; hh < 2; ++hh) {  // P feeds only the output: hi half
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = (cs + 8 * hh + e <= r) ? v[8 * hh + e] : 0.f;
-                store_split(sm + fs::PPS, sm + fs::PPS + 8192, sw128_chunk(r, (cs >> 3) + hh, CH), x);
+                uint4 vh, vl;
+                split8(x, vh, vl);
+                *reinterpret_cast<uint4 *>(sm + fs::PPS + sw128_chunk(r, (cs >> 3) + hh, CH)) = vh;
             }
         }
         // T^T starts at zero: the blocks above the diagonal stay zero
@@ -399,10 +397,9 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok) {
-        bulk_store(rec + Rec::PP_HI, sm + fs::PPS, 16384);  // PP_HI, PP_LO are adjacent
+        bulk_store(rec + Rec::PP_HI, sm + fs::PPS, 8192);
         bulk_commit();
     }
-    bool okt = true;
     if (ok && warp < 2) {
         // ---- diagonal 16 x 16 blocks of T by forward substitution: lane =
         // column c of block b, the column in registers -> T^T row 16 b + c
@@ -419,46 +416,8 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
 #pragma unroll
         for (int r4 = 0; r4 < 16; r4 += 4)
             *reinterpret_cast<float4 *>(dst + r4) = make_float4(tc[r4], tc[r4 + 1], tc[r4 + 2], tc[r4 + 3]);
-    } else if (ok) {
-        // ---- meanwhile (exp(G) . q)^T rows = exp(c_i) Q~^T -> staging; the 16
-        // (quarter, slice) units over warps 2..15
-        okt = mbar_wait(bar_t, 0, p.err);
-        tc_fence_after();
-        if (okt) {
-            const int k0 = (qd >= 2) ? (warp - 2) >> 2 : (warp - 4) >> 2;
-            const int nk = (qd < 2 && k0 == 2) ? 2 : 1;
-            const int i = qd * 32 + lane;
-            const float e_c = ec[i];
-            // hi image rows -> RA; lo image rows 0..63 / 64..127 -> the Q~ rows of X's second K block
-            unsigned char *hi = sm + fs::RA;
-            unsigned char *lo = (i < CH) ? sm + fs::X + 3 * CH * 128 : sm + fs::X_LO + 3 * CH * 128 - CH * 128;
-            for (int k = k0; k < k0 + nk; ++k) {
-                float v[16];
-                tmem_ld16(tm + (uint32_t(qd * 32) << 16) + 64 + 16 * k, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = v[8 * hh + e] * e_c;
-                    uint4 vh, vl;
-                    split8(x, vh, vl);
-                    const uint32_t off = sw128_chunk(i, 2 * k + hh, D);
-                    *reinterpret_cast<uint4 *>(hi + off) = vh;
-                    *reinterpret_cast<uint4 *>(lo + off) = vl;
-                }
-            }
-        }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    ok = __syncthreads_and(ok && okt);
-    if (tid == 0 && ok) {
-        bulk_store(rec + Rec::WQ_HI + Rec::WQ_BLOCK, sm + fs::RA, 16384);
-        bulk_store(rec + Rec::WQ_LO + Rec::WQ_BLOCK, sm + fs::X + 3 * CH * 128, 8192);
-        bulk_store(rec + Rec::WQ_LO + Rec::WQ_BLOCK + 8192, sm + fs::X_LO + 3 * CH * 128, 8192);
-        bulk_commit();
-    }
+    __syncthreads();
     if (ok) {
         // ---- level 1: T_ab = -T_aa A_ab T_bb for (a, b) = (1, 0), (3, 2) ------
         {
@@ -511,38 +470,46 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             store_split(sm + fs::TB, sm + fs::TB_LO, sw128_chunk(s_, c, CH), x);
         }
     }
-    if (tid == 0) bulk_wait_read();  // the staged P and Q^T images are read before X is staged over
+    if (tid == 0) bulk_wait_read();  // the staged P image is read before X is staged over
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0 && lane == 0 && ok) {
-        // W^T / exp(c) = K~^T (T diag beta)^T and Ut^T = V^T (T diag beta)^T: K~, V and (T diag beta)^T read MN-major
+        // W diag(exp(-c)) = (T diag beta) K~: A = (T diag beta) read MN-major,
+        // its second 64-row block past the image (those TMEM lanes are not
+        // read); B = K~ read MN-major.  Ut^T = V^T (T diag beta)^T: V and
+        // (T diag beta)^T read MN-major.
+        const Operand tba{sbase + fs::TB, sbase + fs::TB_LO, true, CH * 128};
         const Operand kt{sbase + fs::X, sbase + fs::X_LO, true, 2 * CH * 128};
         const Operand vt{sbase + fs::VIMG, sbase + fs::VIMG_LO, true, CH * 128};
-        const Operand tb{sbase + fs::TB, sbase + fs::TB_LO, true, CH * 128};
-        const uint32_t id = idesc_bf16_f32(128, CH, true, true);
-        mma_split(tm, kt, tb, CH, id, 3, false);
-        mma_split(tm + 128, vt, tb, CH, id, 3, false);
+        mma_split(tm, tba, kt, CH, idesc_bf16_f32(128, D, true, true), 3, false);
+        mma_split(tm + 128, vt, tba, CH, idesc_bf16_f32(128, CH, true, true), 3, false);
         mma_commit(bar_m2);
     }
     ok = __syncthreads_and(ok && mbar_wait(bar_m2, 0, p.err));
     tc_fence_after();
     if (ok) {
-        // ---- W^T row i (times exp(c_i)) and Ut^T row j = i -> staging in X ----
+        // ---- W row r (times exp(c_i)) and Ut^T row j -> staging in X ----------
         const int i = qd * 32 + lane;
-        float w[16], u[16];
-        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cs, w);
+        if (qd < 2) {  // W: TMEM lanes 0..63 = token r, 32 of the 128 key channels per warp
+            const int r = i, cw = (warp >> 2) * 32;
+            float w[2][16];
+            tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw, w[0]);
+            tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw + 16, w[1]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+                float x[8], e_c[8];
+                ld8(ec + cw + 8 * hh, e_c);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = w[hh >> 1][8 * (hh & 1) + e] * e_c[e];
+                store_split(sm + fs::X, sm + fs::X + 16384, sw128_chunk(r, (cw >> 3) + hh, CH), x);
+            }
+        }
+        float u[16];
         tmem_ld16(tm + (uint32_t(qd * 32) << 16) + 128 + cs, u);
         tmem_wait_ld();
-        const float e_c = ec[i];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = w[8 * hh + e] * e_c;
-            store_split(sm + fs::X, sm + fs::X + 16384, sw128_chunk(i, (cs >> 3) + hh, D), x);
-        }
         unsigned char *ut = sm + fs::X_LO + i * (CH * 4);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -553,8 +520,11 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok) {
-        bulk_store(rec + Rec::WQ_HI, sm + fs::X, 16384);
-        bulk_store(rec + Rec::WQ_LO, sm + fs::X + 16384, 16384);
+        // W rows 0..63 of each 64-wide K block of the WQ images
+        bulk_store(rec + Rec::WQ_HI, sm + fs::X, 8192);
+        bulk_store(rec + Rec::WQ_HI + 16384, sm + fs::X + 8192, 8192);
+        bulk_store(rec + Rec::WQ_LO, sm + fs::X + 16384, 8192);
+        bulk_store(rec + Rec::WQ_LO + 16384, sm + fs::X + 24576, 8192);
         bulk_store(rec + Rec::UT, sm + fs::X_LO, 32768);
         bulk_commit();
         bulk_wait_read();  // shared memory stays until the copies have read it

@@ -117,8 +117,9 @@ __device__ __forceinline__ void tri_offdiag(const float *A, float *T, float *XS,
 // the chunk's 64 tokens plus the 3 before them (the conv halo) and the alpha
 // tile; the kernel forms G, q^, k^ (conv + SiLU + L2) and v (conv + SiLU) in
 // shared memory, so every operand build reads shared memory.  The record
-// images that involve no MMA (exp(G).q transposed, K^, P) go to the record
-// from registers; W^T and Ut^T rows go there from tensor memory.
+// images that involve no MMA (exp(G) . q, K^, P) go to the record from
+// registers; W is staged in shared memory and bulk-stored, Ut^T rows go to
+// the record from tensor memory.
 template <typename Act>
 __global__ void __launch_bounds__(is::NT, 1) prefill_intra_generic_kernel(const PrefillParams p,
                                                                        const __grid_constant__ CUtensorMap tm_q,
@@ -316,14 +317,18 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_generic_kernel(const 
     // ---- phase 1: X = [K exp(G - c); Q exp(G - c)], Kb = K exp(c - G) -> A, P
     if (ok && !exact) {
         // One pass over (row r, 8-channel chunk c) of k^, q^ and E, which are
-        // read once: X rows r and 64 + r = k^ E and q^ E, Kb row r = k^ / E.
+        // read once: X rows r and 64 + r = k^ E and q^ E, Kb row r = k^ / E,
+        // and the record's exp(G) . q row 64 + r of WQ = q^ (E e^c).
+        unsigned char *wq_hi = reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI);
+        unsigned char *wq_lo = reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO);
 #pragma unroll 1
         for (int u = tid; u < CH * (D / 8); u += is::NT) {
             const int r = u / (D / 8), c = u % (D / 8), k0 = 8 * c;
-            float kk[8], qq[8], ee[8], x[8];
+            float kk[8], qq[8], ee[8], cc[8], x[8];
             ld8(KHs + r * D + k0, kk);
             ld8(QHs + r * D + k0, qq);
             ld8(EE + r * D + k0, ee);
+            ld8(ec + k0, cc);
             uint4 vh, vl;
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = kk[e] * ee[e];
@@ -340,6 +345,11 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_generic_kernel(const 
             split8(x, vh, vl);
             *reinterpret_cast<uint4 *>(sm + is::KB_HI + sw128_chunk(r, c, CH)) = vh;
             *reinterpret_cast<uint4 *>(sm + is::KB_LO + sw128_chunk(r, c, CH)) = vl;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = qq[e] * (ee[e] * cc[e]);
+            split8(x, vh, vl);
+            *reinterpret_cast<uint4 *>(wq_hi + sw128_chunk(CH + r, c, 2 * CH)) = vh;
+            *reinterpret_cast<uint4 *>(wq_lo + sw128_chunk(CH + r, c, 2 * CH)) = vl;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -351,19 +361,19 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_generic_kernel(const 
             mma_commit(bar_mma);
         }
     }
-    // chain images that need no MMA: (exp(G) . q)^T (rows i, block 1 of WQ)
-    // and K^ = exp(G_last - G) . k (rows r)
-    if (ok) {
-        build_image<true>(reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI + Rec::WQ_BLOCK),
-                          reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO + Rec::WQ_BLOCK), D, 8, tid, is::NT,
-                          [&](int i, int r0, float(&x)[8]) {
-                              const float e_c = ec[i];
+    // chain images that need no MMA: exp(G) . q (WQ rows 64 + r; above when
+    // !exact) and K^ = exp(G_last - G) . k (rows r)
+    if (ok && exact) {
+        build_image(reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI), reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO),
+                    CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
+                        float a[8], gg[8];
+                        ld8(QHs + r * D + k0, a);
+                        ld8(GGs + r * D + k0, gg);
 #pragma unroll
-                              for (int e = 0; e < 8; ++e) {
-                                  const float gv = GGs[(r0 + e) * D + i];
-                                  x[e] = QHs[(r0 + e) * D + i] * (exact ? expf(gv) : gv * e_c);
-                              }
-                          });
+                        for (int e = 0; e < 8; ++e) x[e] = a[e] * expf(gg[e]);
+                    }, CH, 2 * CH);
+    }
+    if (ok) {
         build_image(reinterpret_cast<unsigned char *>(rec + Rec::KH_HI), reinterpret_cast<unsigned char *>(rec + Rec::KH_LO),
                     CH, 16, tid, is::NT, [&](int r, int k0, float(&x)[8]) {
                         float kv[8], gv[8];
@@ -519,13 +529,13 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_generic_kernel(const 
     ok = __syncthreads_and(ok && mbar_wait(bar_mma, mma_phase, p.err));
     mma_phase ^= 1;
     tc_fence_after();
-    // W^T row i and Ut^T row j = i of the record, from TMEM lane i: the warps
+    // W (staged transposed from TMEM lane i into shared memory, then bulk-
+    // stored as rows 0..63 of WQ) and Ut^T row j = i of the record: the warps
     // of a lane quarter split the 64 token columns
+    unsigned char *whi = sm + is::IN0, *wlo = sm + is::IN0 + 16384;
     const int i = (warp & 3) * 32 + lane;
     const int cbase = (warp >> 2) * (CH / is::QW);
     if (ok) {
-        unsigned char *wt_hi = reinterpret_cast<unsigned char *>(rec + Rec::WQ_HI);
-        unsigned char *wt_lo = reinterpret_cast<unsigned char *>(rec + Rec::WQ_LO);
         float *UT = at<float>(rec, Rec::UT) + size_t(i) * CH;
 #pragma unroll 1
         for (int c0 = cbase; c0 < cbase + CH / is::QW; c0 += 16) {
@@ -534,20 +544,30 @@ __global__ void __launch_bounds__(is::NT, 1) prefill_intra_generic_kernel(const 
             tmem_ld16(tm + (uint32_t((warp & 3) * 32) << 16) + 128 + c0, u);
             tmem_wait_ld();
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = v[8 * hh + e];
-                uint4 vh, vl;
-                split8(x, vh, vl);
-                const uint32_t off = sw128_chunk(i, (c0 >> 3) + hh, D);
-                *reinterpret_cast<uint4 *>(wt_hi + off) = vh;
-                *reinterpret_cast<uint4 *>(wt_lo + off) = vl;
+            for (int e = 0; e < 16; ++e) {
+                const int r = c0 + e;
+                const __nv_bfloat16 wh = __float2bfloat16_rn(v[e]);
+                const __nv_bfloat16 wl = __float2bfloat16_rn(v[e] - __bfloat162float(wh));
+                const uint32_t off = sw128_offset(r, i, CH);
+                *reinterpret_cast<__nv_bfloat16 *>(whi + off) = wh;
+                *reinterpret_cast<__nv_bfloat16 *>(wlo + off) = wl;
             }
 #pragma unroll
             for (int e = 0; e < 16; e += 4)
                 *reinterpret_cast<float4 *>(UT + 4 * ut_chunk(i, (c0 + e) >> 2)) = make_float4(u[e], u[e + 1], u[e + 2], u[e + 3]);
         }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        // a 64-row image's K-block b holds the same bytes as rows 0..63 of K-block b of WQ
+        bulk_store(rec + Rec::WQ_HI, whi, 8192);
+        bulk_store(rec + Rec::WQ_HI + 16384, whi + 8192, 8192);
+        bulk_store(rec + Rec::WQ_LO, wlo, 8192);
+        bulk_store(rec + Rec::WQ_LO + 16384, wlo + 8192, 8192);
+        bulk_commit();
+        bulk_wait_read();  // shared memory is reused by the next chunk-head
     }
     ph ^= 1;
     tc_fence_before();
