@@ -68,8 +68,10 @@ constexpr uint32_t BYTES = BARS + 512;
 static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
 
 // One CTA (8 warps) per (sequence, head), walking the window's chunks in
-// order.  TMEM columns: [(W S)^T | (Q S)^T] [0,128), (K^^T U)^T [128,256),
-// (P U)^T [256,320), S^T [320,448).
+// order.  Thread (j, half) keeps S^T row j, columns 64 half .. + 63, in fp32
+// registers.  TMEM columns: [(W S)^T | (Q S)^T] [0,128), (K^^T U)^T
+// [128,256), (P U)^T [256,320).  Each step asks L2 for the record two chunks
+// ahead, so the next step's bulk loads find it there.
 //   stage 1  [(W S)^T | (Q S)^T] = S^T [W; Q]^T (the record's WQ, K-major)
 //   U^T      = Ut^T - (W S)^T, split into hi / lo images
 //   stage 2  (K^^T U)^T = U^T K^ (K^ read MN-major), (P U)^T = U^T P^T
@@ -132,30 +134,40 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             *reinterpret_cast<uint4 *>(sm + cs::WQ_LO + kb * 16384 + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    if (tid == 0 && c_hi > c_lo) load_rec(rec_ptr(p, sq.chunk0 + c_lo, h));
-    const int sc0 = half * 64;  // this thread's 64 columns of the S^T row
-    // S^T row j: fp32 into TMEM, hi/lo into the A1 images
-    for (int c0 = sc0; c0 < sc0 + 64; c0 += 16) {
-        float v[16];
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-            const float4 x = load_state ? ld4(slot_state + size_t(j) * D + c0 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
+    const uint32_t ut_bytes = uint32_t(Rec::OO - Rec::UT);
+    auto prefetch_rec = [&](const char *r) {  // into L2: the bulk loads and the Ut^T rows of a later step
+        bulk_prefetch_l2(r + Rec::WQ_HI, p.q_lo ? Rec::B1_BYTES : 32768u);
+        if (!p.q_lo) {
+            bulk_prefetch_l2(r + Rec::WQ_LO, 8192);
+            bulk_prefetch_l2(r + Rec::WQ_LO + 16384, 8192);
         }
-        tmem_st16(tl + 320 + c0, v);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = v[8 * hh + e];
-            uint4 vh, vl;
-            split8(x, vh, vl);
-            const uint32_t off = sw128_chunk(j, (c0 >> 3) + hh, D);
-            *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
-            *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
-        }
+        bulk_prefetch_l2(r + Rec::KH_HI, b2_bytes);
+        bulk_prefetch_l2(r + Rec::UT, ut_bytes);
+    };
+    if (tid == 0 && c_hi > c_lo) {
+        load_rec(rec_ptr(p, sq.chunk0 + c_lo, h));
+        if (c_lo + 1 < c_hi) prefetch_rec(rec_ptr(p, sq.chunk0 + c_lo + 1, h));
     }
-    tmem_wait_st();
+    const int sc0 = half * 64;  // this thread's 64 columns of the S^T row
+    // S^T row j (64 columns) in registers; hi/lo into the A1 images
+    float sr[64];
+    const float *srow = slot_state + size_t(j) * D + sc0;
+#pragma unroll
+    for (int e = 0; e < 64; e += 4) {
+        const float4 x = load_state ? ld4(srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        sr[e] = x.x; sr[e + 1] = x.y; sr[e + 2] = x.z; sr[e + 3] = x.w;
+    }
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = sr[8 * cc + e];
+        uint4 vh, vl;
+        split8(x, vh, vl);
+        const uint32_t off = sw128_chunk(j, (sc0 >> 3) + cc, D);
+        *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
+        *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -179,6 +191,7 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             tc_fence_after();
             mma_split(tm + 0, s_img, wq_img, D, id_s1, 3, false);
             mma_commit(bar_m1);
+            if (c + 2 < c_hi) prefetch_rec(rec_ptr(p, g + 2, h));
         }
         // Ut^T row j, entries r = uc0 .. uc0 + 31, while the MMAs run
         float ut[32];
@@ -254,44 +267,33 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
 #pragma unroll
                 for (int e = 0; e < 16; ++e) O[(uc0 + 16 * q + e) * D + j] = v[q][e] + w2[q][e];
         }
-        // S^T row j <- gamma . S^T row j + elc . (K^ U-product)^T row j; refresh the A1 images
-        const ChunkMeta cm = p.chunks[g];
-        for (int c0 = sc0; c0 < sc0 + 64; c0 += 32) {  // 32 columns per TMEM round trip
-            float s[2][16], ds[2][16];
+        // S^T row j <- gamma . S^T row j + elc . (K^^T U)^T row j; refresh the A1 images
+        {
+            float ds[4][16];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                tmem_ld16(tl + 320 + c0 + 16 * q, s[q]);
-                tmem_ld16(tl + 128 + c0 + 16 * q, ds[q]);
-            }
+            for (int q = 0; q < 4; ++q) tmem_ld16(tl + 128 + sc0 + 16 * q, ds[q]);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    s[q][e] = fmaf(gcur[c0 + 16 * q + e], s[q][e], gcur[D + c0 + 16 * q + e] * ds[q][e]);
-                tmem_st16(tl + 320 + c0 + 16 * q, s[q]);
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = s[q][8 * hh + e];
-                    uint4 vh, vl;
-                    split8(x, vh, vl);
-                    const uint32_t off = sw128_chunk(j, ((c0 + 16 * q) >> 3) + hh, D);
-                    *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
-                    *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
-                }
-                for (int k = 0; k < cm.ck_count; ++k) {
-                    const CkptMeta ck = p.ckpts[cm.ck_begin + k];
-                    float *dst = p.states + size_t(ck.dst_slot) * p.H * head_elems + size_t(h) * head_elems +
-                                 size_t(j) * D + c0 + 16 * q;
-#pragma unroll
-                    for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4 *>(dst + e) = make_float4(s[q][e], s[q][e + 1], s[q][e + 2], s[q][e + 3]);
-                }
-            }
+            for (int e = 0; e < 64; ++e) sr[e] = fmaf(gcur[sc0 + e], sr[e], gcur[D + sc0 + e] * ds[e >> 4][e & 15]);
         }
-        tmem_wait_st();
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = sr[8 * cc + e];
+            uint4 vh, vl;
+            split8(x, vh, vl);
+            const uint32_t off = sw128_chunk(j, (sc0 >> 3) + cc, D);
+            *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
+            *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
+        }
+        const ChunkMeta cm = p.chunks[g];
+        for (int k = 0; k < cm.ck_count; ++k) {  // interval checkpoints of this chunk end
+            const CkptMeta ck = p.ckpts[cm.ck_begin + k];
+            float *dst = p.states + size_t(ck.dst_slot) * p.H * head_elems + size_t(h) * head_elems + size_t(j) * D + sc0;
+#pragma unroll
+            for (int e = 0; e < 64; e += 4) *reinterpret_cast<float4 *>(dst + e) = make_float4(sr[e], sr[e + 1], sr[e + 2], sr[e + 3]);
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -299,14 +301,9 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
     }
     // end state S^T row j (this thread's 64 columns) -> slot
     if (ok) {
-        for (int c0 = sc0; c0 < sc0 + 64; c0 += 16) {
-            float s[16];
-            tmem_ld16(tl + 320 + c0, s);
-            tmem_wait_ld();
+        float *drow = slot_state + size_t(j) * D + sc0;
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4 *>(slot_state + size_t(j) * D + c0 + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
-        }
+        for (int e = 0; e < 64; e += 4) *reinterpret_cast<float4 *>(drow + e) = make_float4(sr[e], sr[e + 1], sr[e + 2], sr[e + 3]);
     }
     tc_fence_before();
     __syncthreads();
