@@ -116,8 +116,8 @@ def args_():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing (profiling runs)")
-    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "decode_b1_l2_flushed", "prefill", "mixed",
-                                       "next_rows"], default=None,
+    ap.add_argument("--only", choices=["decode_b64", "verify_b64_t8", "decode_b1_l2_flushed", "decode_b1_prefetch",
+                                       "prefill", "mixed", "next_rows"], default=None,
                     help="run one secondary case alone (for profiling) and print its numbers")
     ap.add_argument("--prefill-tokens", type=int, default=None,
                     help="with --only prefill: a shorter sequence of the same workload (small profiling case)")
@@ -464,6 +464,38 @@ def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
                                   "traffic": profiled_traffic(profile), "bytes_per_launch": byts,
                                   "peak_kind": peak_kind},
                      "l2": L2_NOTE}
+    # a batch-1 decode with L2 flushed, then other work of the layer (a
+    # stand-in: an element-wise op over 8 MiB the decode does not touch, about
+    # the q/k/v projection's traffic at batch 1), with and without
+    # kda_state_prefetch of its slot issued before that work; the decode
+    # launch alone is timed
+    if only is None or only == "decode_b1_prefetch":
+        toks = {k: v.to(dev) for k, v in wl.tokens(210, 1).items()}
+        out = torch.empty(1, H, D, dtype=act, device=dev)
+        io = kda.make_io(toks, out)
+        slot = perm[:1].contiguous()
+        busy_a = torch.ones(2 << 20, dtype=torch.float32, device=dev)
+        busy_b = torch.empty_like(busy_a)
+        res_p = {}
+        for name, pre in (("flushed_then_work", False), ("flushed_prefetch_then_work", True)):
+            for _ in range(3):
+                kda.kda_decode(pool, w, io, slot, 1)
+            times = []
+            for _ in range(iters):
+                flush_l2(flush)
+                if pre:
+                    kda.kda_state_prefetch(pool, slot, 1)
+                torch.mul(busy_a, 1.0001, out=busy_b)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                kda.kda_decode(pool, w, io, slot, 1)
+                e.record(stream)
+                e.synchronize()
+                times.append(s.elapsed_time(e) * 1e3)
+            res_p[name] = {"launch_us": round(float(np.mean(times)), 2)}
+        res_p["note"] = ("L2 flushed, then an 8 MiB element-wise op standing in for the layer's other work, then "
+                         "the timed decode; kda_state_prefetch of the slot issued before that op in the second case")
+        res["decode_b1_prefetch"] = res_p
     st, flags = kda.kda_poll_device_error(pool)
     assert st == 0, f"device error word {flags:#x}"
     return res

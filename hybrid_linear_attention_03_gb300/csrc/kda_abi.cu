@@ -193,6 +193,13 @@ kda_status kda_decode(kda_pool *pool, const kda_weights *w, const kda_io *io, co
     return run_step(pool, w, io, slots, slots, B, 1, stream);
 }
 
+kda_status kda_state_prefetch(kda_pool *pool, const int32_t *slots, int32_t B, kda_stream_t stream) {
+    const CallRange range("kda_state_prefetch");
+    if (!pool || B < 0 || (B > 0 && !slots)) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    return kda::launch_state_prefetch(pool, slots, B, reinterpret_cast<cudaStream_t>(stream));
+}
+
 kda_status kda_verify(kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *in_slots,
                       const int32_t *snap_slots, int32_t B, int32_t T, kda_stream_t stream) {
     const CallRange range("kda_verify");

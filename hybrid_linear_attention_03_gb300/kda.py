@@ -41,10 +41,11 @@ EXPORTS = ("kda_state_pool_bytes", "kda_state_pool_create", "kda_state_pool_dest
            "kda_state_slot_bytes", "kda_state_export", "kda_state_import", "kda_prefill_workspace_bytes_bound",
            "kda_prefill_chunked_dev", "kda_prefix_cache_create", "kda_prefix_cache_destroy", "kda_prefix_cache_plan",
            "kda_prefix_cache_forget", "kda_prefix_cache_get_stats", "kda_prefix_cache_saved", "kda_stream_wait",
-           "kda_state_pool_set_flags", "kda_profile_start", "kda_profile_stop")
+           "kda_state_pool_set_flags", "kda_profile_start", "kda_profile_stop", "kda_state_prefetch")
 
 # kda_kernel_kind
-KERNEL_KINDS = ("step", "slot_copy", "prefill_meta", "prefill_intra", "prefill_chain", "prefill_out", "prefill_tails")
+KERNEL_KINDS = ("step", "slot_copy", "prefill_meta", "prefill_intra", "prefill_chain", "prefill_out", "prefill_tails",
+                "state_prefetch")
 
 KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -122,6 +123,8 @@ def lib() -> ctypes.CDLL:
         L.kda_check_slots.restype = i32
         L.kda_decode.argtypes = [vp, P(kda_weights), P(kda_io), vp, i32, vp]
         L.kda_decode.restype = i32
+        L.kda_state_prefetch.argtypes = [vp, vp, i32, vp]
+        L.kda_state_prefetch.restype = i32
         L.kda_verify.argtypes = [vp, P(kda_weights), P(kda_io), vp, vp, i32, i32, vp]
         L.kda_verify.restype = i32
         L.kda_prefill_workspace_bytes.argtypes = [vp, vp, i32, i32]
@@ -333,6 +336,12 @@ def kda_decode(pool: StatePool, weights: kda_weights, io: kda_io, slots: torch.T
     B = slots.numel() if B is None else B
     _check(lib().kda_decode(pool.handle, ctypes.byref(weights), ctypes.byref(io), _dptr(slots), int(B),
                             _stream(stream)), "kda_decode")
+
+
+def kda_state_prefetch(pool: StatePool, slots: torch.Tensor, B: int | None = None, stream=None) -> None:
+    """Hint: bring the slots' state and conv tail into L2 ahead of a decode."""
+    B = slots.numel() if B is None else B
+    _check(lib().kda_state_prefetch(pool.handle, _dptr(slots), int(B), _stream(stream)), "kda_state_prefetch")
 
 
 def kda_verify(pool: StatePool, weights: kda_weights, io: kda_io, in_slots: torch.Tensor, snap_slots: torch.Tensor,

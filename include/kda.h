@@ -192,6 +192,19 @@ KDA_API kda_status kda_check_slots(const kda_pool *pool, const int32_t *in_slots
 KDA_API kda_status kda_decode(kda_pool *pool, const kda_weights *w, const kda_io *io,
                       const int32_t *slots, int32_t B, kda_stream_t stream);
 
+/* Asks L2 to fetch the state and conv tail of slots[0..B) (a DEVICE array)
+ * ahead of a kda_decode / kda_verify that reads them, for example one layer
+ * early while other layers run: a decode whose state has left L2 otherwise
+ * waits on a chain of round trips to HBM.  A hint: results never depend on
+ * it, it changes no memory, and a slot outside the pool is skipped.  It
+ * pays while the prefetched slots fit in L2 (129 MB; a slot is 4.3 MB at
+ * H = 64, d = 128, bf16), so small batches.  One small kernel on `stream`;
+ * B = 0 is a no-op.  Errors: KDA_ERR_INVALID_ARG (null pool or slots,
+ * B < 0), KDA_ERR_CUDA.
+ * Source: "vLLM Kimi K3 지원", section "Fused Kernels 및 메타데이터 최적화",
+ * KDA Decode bullet (the decode step is bound by its repeated state traffic). */
+KDA_API kda_status kda_state_prefetch(kda_pool *pool, const int32_t *slots, int32_t B, kda_stream_t stream);
+
 /* Speculative verify: B sequences each advance T draft tokens (1 <= T <= 16)
  * in one launch.  Token (b, t) is io row b*T + t.  Sequence b starts from slot
  * in_slots[b] (DEVICE [B]); after its token t the state and conv tail are
@@ -411,6 +424,7 @@ typedef enum {
     KDA_KERNEL_PREFILL_CHAIN,  /* the chunk chain (state passing) */
     KDA_KERNEL_PREFILL_OUT,    /* gated norm of the prefill outputs */
     KDA_KERNEL_PREFILL_TAILS,  /* conv tails of checkpoints and ends */
+    KDA_KERNEL_STATE_PREFETCH, /* kda_state_prefetch */
     KDA_KERNEL_COUNT
 } kda_kernel_kind;
 typedef struct {

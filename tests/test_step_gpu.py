@@ -364,3 +364,28 @@ def test_inputs_written_by_the_preceding_kernel(graph):
         assert m.state_err(slot) <= hp.STATE_TOL
         assert m.tail_equal(slot)
     assert kda.kda_poll_device_error(m.gpu) == (kda.KDA_OK, 0)
+
+
+def test_state_prefetch_changes_nothing():
+    """kda_state_prefetch is an L2 hint: a decode after it equals the same
+    decode without it bit for bit, the pool is untouched by the prefetch
+    itself, and an out-of-range slot in its table is skipped silently."""
+    H, D, act, B = 4, 128, torch.bfloat16, 3
+    ma = Mirror(8, H, D, act, _weights(93, H, D, act))
+    mb = Mirror(8, H, D, act, _weights(93, H, D, act))
+    slots = [5, 0, 3]
+    for m in (ma, mb):
+        m.decode(slots, _tokens(93, 1, B, H, D, act))
+    torch.cuda.synchronize()
+    before = mb.gpu.states().clone(), mb.gpu.tails().clone()
+    table = torch.tensor(slots + [99, -1], dtype=torch.int32, device="cuda")
+    kda.kda_state_prefetch(mb.gpu, table)
+    torch.cuda.synchronize()
+    assert torch.equal(mb.gpu.states(), before[0]) and torch.equal(mb.gpu.tails(), before[1])
+    assert kda.kda_poll_device_error(mb.gpu) == (kda.KDA_OK, 0)
+    tok = _tokens(93, 2, B, H, D, act)
+    out_a, _ = ma.decode(slots, tok)
+    out_b, _ = mb.decode(slots, tok)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(ma.gpu.states(), mb.gpu.states()) and torch.equal(ma.gpu.tails(), mb.gpu.tails())
