@@ -64,6 +64,9 @@ def source_sha(paths):
 
 
 PREFILL_SOURCES = ("hybrid_linear_attention_03_gb300/csrc/kda_prefill.cu",
+                   "hybrid_linear_attention_03_gb300/csrc/kda_prefill.cuh",
+                   "hybrid_linear_attention_03_gb300/csrc/kda_prefill_intra_fast.cu",
+                   "hybrid_linear_attention_03_gb300/csrc/kda_prefill_intra_generic.cu",
                    "hybrid_linear_attention_03_gb300/csrc/kda_sm100.cuh",
                    "hybrid_linear_attention_03_gb300/csrc/kda_internal.h")
 # Algorithmic FLOP per (chunk, head) at C = 64, d_k = d_v = 128 (full-square products):
@@ -544,7 +547,7 @@ def prefill_case(kda, dev, iters=3, warmup=1, L=None):
     n_intra, intra_ms = prof["prefill_intra"]
     intra_flop = chunk_heads * INTRA_FLOP_PER_CHUNK_HEAD
     intra_tf = intra_flop / (intra_ms * 1e-3) / 1e12
-    tr = profiled_prefill_traffic("kda_prefill_intra_dram.md")
+    tr = profiled_prefill_traffic("kda_prefill_intra_fast_chain_4k_full.md")
     call_flop = chunk_heads * (INTRA_FLOP_PER_CHUNK_HEAD + CHAIN_FLOP_PER_CHUNK_HEAD)
     call_bytes = L * PREFILL_BYTES_PER_TOKEN
     return {"workload": wl.name if L == wl.extra["L"] else f"{wl.name} (first {L} tokens)",
@@ -552,16 +555,18 @@ def prefill_case(kda, dev, iters=3, warmup=1, L=None):
             "workspace_bytes": ws.numel(),
             "kernels_ms_per_call": {k: round(v[1], 4) for k, v in prof.items() if k != "dropped" and v[0]},
             "kernel_launches_per_call": {k: v[0] for k, v in prof.items() if k != "dropped" and v[0]},
-            "roofline": {"bound": "tensor", "kernel": "prefill_intra_kernel", "achieved": round(intra_tf, 2),
+            "roofline": {"bound": "tensor", "kernel": "prefill_intra_fast_kernel", "achieved": round(intra_tf, 2),
                          "peak": tf_peak, "unit": "TFLOP/s", "frac": round(intra_tf / tf_peak, 4),
                          "traffic": None if tr is None else tr * chunk_heads // max(n_intra, 1),
                          "flop_per_launch": intra_flop // max(n_intra, 1),
                          "launch_us": round(intra_ms * 1e3 / max(n_intra, 1), 2),
                          "note": f"algorithmic intra-chunk FLOP (A, P, W, Ut and the triangular inverse: "
-                                 f"{INTRA_FLOP_PER_CHUNK_HEAD} per chunk-head) over the intra kernel's device time, "
-                                 f"CUDA events around each of its launches inside the call; peak = {peak_kind} "
-                                 f"dense bf16 (burst); traffic = ncu DRAM bytes per chunk-head of a small case x "
-                                 f"the chunk-heads of one launch"},
+                                 f"{INTRA_FLOP_PER_CHUNK_HEAD} per chunk-head) over the factored-decay intra "
+                                 f"kernel's device time, CUDA events around each of its launches inside the call "
+                                 f"(one launch per window of chunks; the exact-decay kernel's hand-over list is "
+                                 f"timed apart as prefill_intra_exact); peak = {peak_kind} dense bf16 (burst); "
+                                 f"traffic = ncu DRAM bytes per chunk-head of a small case x the chunk-heads of "
+                                 f"one launch"},
             "whole_call": {"algorithmic_flop": call_flop, "tflops": round(call_flop / (ms * 1e-3) / 1e12, 2),
                            "frac_bf16": round(call_flop / (ms * 1e-3) / 1e12 / tf_peak, 4),
                            "algorithmic_bytes": call_bytes, "gbs": round(call_bytes / (ms * 1e-3) / 1e9, 1),

@@ -590,7 +590,7 @@ kda_status intra_generic_prepare() {
 template <typename Act>
 kda_status launch_intra_generic(const PrefillParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
                                 const CUtensorMap &mv, const CUtensorMap &ma, dim3 grid, cudaStream_t s) {
-    const ProfScope prof(KDA_KERNEL_PREFILL_INTRA, s);
+    const ProfScope prof(KDA_KERNEL_PREFILL_INTRA_EXACT, s);
     prefill_intra_generic_kernel<Act><<<grid, is::NT, 1024 + is::BYTES<Act>(), s>>>(p, mq, mk, mv, ma);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -45,7 +45,7 @@ EXPORTS = ("kda_state_pool_bytes", "kda_state_pool_create", "kda_state_pool_dest
 
 # kda_kernel_kind
 KERNEL_KINDS = ("step", "slot_copy", "prefill_meta", "prefill_intra", "prefill_chain", "prefill_out", "prefill_tails",
-                "state_prefetch")
+                "state_prefetch", "prefill_intra_exact")
 
 KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
 

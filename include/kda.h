@@ -420,11 +420,15 @@ typedef enum {
     KDA_KERNEL_SLOT_COPY,      /* kda_state_checkpoint */
     KDA_KERNEL_PREFILL_META,   /* prefill tables: the device builder (kda_prefill_chunked_dev), or the
                                   copies of the host-built tables (kda_prefill_chunked) */
-    KDA_KERNEL_PREFILL_INTRA,  /* intra-chunk prefill kernel */
+    KDA_KERNEL_PREFILL_INTRA,  /* intra-chunk prefill kernel with the decay factored around the chunk's
+                                  midpoint (bf16 inputs: every chunk-head of a window) */
     KDA_KERNEL_PREFILL_CHAIN,  /* the chunk chain (state passing) */
     KDA_KERNEL_PREFILL_OUT,    /* gated norm of the prefill outputs */
     KDA_KERNEL_PREFILL_TAILS,  /* conv tails of checkpoints and ends */
     KDA_KERNEL_STATE_PREFETCH, /* kda_state_prefetch */
+    KDA_KERNEL_PREFILL_INTRA_EXACT, /* intra-chunk prefill kernel with per-pair decay exponents (bf16
+                                  inputs: the chunk-heads the factored kernel hands over; fp32 inputs:
+                                  every chunk-head) */
     KDA_KERNEL_COUNT
 } kda_kernel_kind;
 typedef struct {
