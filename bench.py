@@ -67,8 +67,7 @@ PREFILL_SOURCES = ("hybrid_linear_attention_03_gb300/csrc/kda_prefill.cu",
                    "hybrid_linear_attention_03_gb300/csrc/kda_prefill.cuh",
                    "hybrid_linear_attention_03_gb300/csrc/kda_prefill_intra_fast.cu",
                    "hybrid_linear_attention_03_gb300/csrc/kda_prefill_intra_generic.cu",
-                   "hybrid_linear_attention_03_gb300/csrc/kda_sm100.cuh",
-                   "hybrid_linear_attention_03_gb300/csrc/kda_internal.h")
+                   "hybrid_linear_attention_03_gb300/csrc/kda_sm100.cuh")
 # Algorithmic FLOP per (chunk, head) at C = 64, d_k = d_v = 128 (full-square products):
 # intra-chunk A, P, W, Ut (2 C^2 d each) and the triangular inverse (C^3 / 3);
 # chain W S, Q S, K^T U (2 C d^2 each) and P U (2 C^2 d).
@@ -467,37 +466,95 @@ def secondary(kda, dev, hbm_peak, peak_kind, only=None, iters=20):
                                   "traffic": profiled_traffic(profile), "bytes_per_launch": byts,
                                   "peak_kind": peak_kind},
                      "l2": L2_NOTE}
-    # a batch-1 decode with L2 flushed, then other work of the layer (a
-    # stand-in: an element-wise op over 8 MiB the decode does not touch, about
-    # the q/k/v projection's traffic at batch 1), with and without
-    # kda_state_prefetch of its slot issued before that work; the decode
-    # launch alone is timed
+    # Batch-1 decodes inside a CUDA graph after other work of the layer.  Each
+    # repetition of the graph runs [L2 flush] [kda_state_prefetch of n_seq
+    # slots] a stand-in for the layer's other work (an element-wise op over 8
+    # MiB the decodes do not touch, then copies that write their inputs the
+    # way a projection would), then n_seq batch-1 decodes, each on its own
+    # slot, so every decode after a flush finds its state in HBM.  A decode's
+    # cost is the replay time with the decodes minus the same graph without
+    # them, over the decodes, so the flush and the stand-in cancel.  Cases: L2
+    # warm (no flush), L2 flushed, flushed with the slots prefetched before the
+    # stand-in work, and with the slots and the layer weights.
     if only is None or only == "decode_b1_prefetch":
-        toks = {k: v.to(dev) for k, v in wl.tokens(210, 1).items()}
-        out = torch.empty(1, H, D, dtype=act, device=dev)
-        io = kda.make_io(toks, out)
-        slot = perm[:1].contiguous()
+        n_seq, reps, replays = 16, 8, 4
+        toks = {k: v.to(dev) for k, v in wl.tokens(210, n_seq).items()}
+        src = {k: v.clone() for k, v in toks.items()}
+        out = torch.empty(n_seq, H, D, dtype=act, device=dev)
+        ios = [kda.make_io({k: v[i:i + 1] for k, v in toks.items()}, out[i:i + 1]) for i in range(n_seq)]
+        slots = perm[:n_seq].contiguous()
+        slot1 = [slots[i:i + 1] for i in range(n_seq)]
         busy_a = torch.ones(2 << 20, dtype=torch.float32, device=dev)
         busy_b = torch.empty_like(busy_a)
+        gs = torch.cuda.Stream(device=dev)
+
+        def body(flushed, pre, decode):
+            for _ in range(reps):
+                if flushed:
+                    flush_l2(flush)
+                if pre is not None:
+                    kda.kda_state_prefetch(pool, slots, n_seq, weights=w if pre == "state+weights" else None)
+                torch.mul(busy_a, 1.0001, out=busy_b)
+                for k in toks:
+                    toks[k].copy_(src[k])
+                if decode:
+                    for i in range(n_seq):
+                        kda.kda_decode(pool, w, ios[i], slot1[i], 1)
+
+        def replay_us(flushed, pre, decode):
+            with torch.cuda.stream(gs):
+                body(flushed, pre, decode)  # warm-up outside capture
+            gs.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=gs):
+                body(flushed, pre, decode)
+            g.replay()
+            torch.cuda.synchronize()
+            st = torch.cuda.current_stream()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(st)
+            for _ in range(replays):
+                g.replay()
+            e.record(st)
+            e.synchronize()
+            del g
+            return s.elapsed_time(e) * 1e3 / replays
+
         res_p = {}
-        for name, pre in (("flushed_then_work", False), ("flushed_prefetch_then_work", True)):
-            for _ in range(3):
-                kda.kda_decode(pool, w, io, slot, 1)
+        for name, flushed, pre in (("l2_warm", False, None), ("l2_flushed", True, None),
+                                   ("l2_flushed_state_prefetched", True, "state"),
+                                   ("l2_flushed_state_weights_prefetched", True, "state+weights")):
+            with_d = replay_us(flushed, pre, True)
+            without = replay_us(flushed, pre, False)
+            res_p[name] = {"decode_us": round((with_d - without) / (reps * n_seq), 2)}
+        # the same decode as one event-timed launch outside a graph, after the
+        # same stand-in work, with L2 warm and flushed: a spin with no memory
+        # traffic first lets the host enqueue the rest, so no host gap is timed
+        single = {}
+        for name, flushed in (("l2_warm", False), ("l2_flushed", True)):
             times = []
             for _ in range(iters):
-                flush_l2(flush)
-                if pre:
-                    kda.kda_state_prefetch(pool, slot, 1)
+                if flushed:
+                    flush_l2(flush)
+                torch.cuda._sleep(400_000)
                 torch.mul(busy_a, 1.0001, out=busy_b)
+                for k in toks:
+                    toks[k].copy_(src[k])
                 s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 s.record(stream)
-                kda.kda_decode(pool, w, io, slot, 1)
+                kda.kda_decode(pool, w, ios[0], slot1[0], 1)
                 e.record(stream)
                 e.synchronize()
                 times.append(s.elapsed_time(e) * 1e3)
-            res_p[name] = {"launch_us": round(float(np.mean(times)), 2)}
-        res_p["note"] = ("L2 flushed, then an 8 MiB element-wise op standing in for the layer's other work, then "
-                         "the timed decode; kda_state_prefetch of the slot issued before that op in the second case")
+            single[name] = {"launch_us": round(float(np.mean(times)), 2)}
+        res_p["single_launch"] = single
+        res_p["note"] = (f"per batch-1 decode inside a CUDA graph: {n_seq} decodes on {n_seq} slots after an 8 MiB "
+                         "element-wise op and copies writing their inputs (standing in for the layer's other work), "
+                         f"{reps} repetitions per graph; replay time with the decodes minus without, over the "
+                         "decodes; L2 flushed (512 MiB written, then read) before each repetition except in the "
+                         "warm case; kda_state_prefetch of the slots issued before the stand-in work in the "
+                         "prefetch cases; single_launch: one decode between two CUDA events after the same work, "
+                         "outside a graph (launch latency included)")
         res["decode_b1_prefetch"] = res_p
     st, flags = kda.kda_poll_device_error(pool)
     assert st == 0, f"device error word {flags:#x}"

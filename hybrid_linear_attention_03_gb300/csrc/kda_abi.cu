@@ -193,11 +193,12 @@ kda_status kda_decode(kda_pool *pool, const kda_weights *w, const kda_io *io, co
     return run_step(pool, w, io, slots, slots, B, 1, stream);
 }
 
-kda_status kda_state_prefetch(kda_pool *pool, const int32_t *slots, int32_t B, kda_stream_t stream) {
+kda_status kda_state_prefetch(kda_pool *pool, const kda_weights *w, const int32_t *slots, int32_t B,
+                              kda_stream_t stream) {
     const CallRange range("kda_state_prefetch");
-    if (!pool || B < 0 || (B > 0 && !slots)) return KDA_ERR_INVALID_ARG;
+    if (!pool || B < 0 || (B > 0 && !slots) || (w && !valid_weights(w))) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;
-    return kda::launch_state_prefetch(pool, slots, B, reinterpret_cast<cudaStream_t>(stream));
+    return kda::launch_state_prefetch(pool, w, slots, B, reinterpret_cast<cudaStream_t>(stream));
 }
 
 kda_status kda_verify(kda_pool *pool, const kda_weights *w, const kda_io *io, const int32_t *in_slots,

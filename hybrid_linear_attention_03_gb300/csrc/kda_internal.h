@@ -71,7 +71,8 @@ class ProfScope {
 };
 
 // L2 prefetch of the slots' state and conv tail (device slot table [B]).
-kda_status launch_state_prefetch(const kda_pool *pool, const int32_t *slots, int B, cudaStream_t stream);
+kda_status launch_state_prefetch(const kda_pool *pool, const kda_weights *w, const int32_t *slots, int B,
+                                 cudaStream_t stream);
 
 // Slot-to-slot copy of state + tail.
 kda_status launch_slot_copy(const kda_pool *pool, const int32_t *src, const int32_t *dst, int n,

@@ -123,7 +123,7 @@ def lib() -> ctypes.CDLL:
         L.kda_check_slots.restype = i32
         L.kda_decode.argtypes = [vp, P(kda_weights), P(kda_io), vp, i32, vp]
         L.kda_decode.restype = i32
-        L.kda_state_prefetch.argtypes = [vp, vp, i32, vp]
+        L.kda_state_prefetch.argtypes = [vp, vp, vp, i32, vp]
         L.kda_state_prefetch.restype = i32
         L.kda_verify.argtypes = [vp, P(kda_weights), P(kda_io), vp, vp, i32, i32, vp]
         L.kda_verify.restype = i32
@@ -338,10 +338,13 @@ def kda_decode(pool: StatePool, weights: kda_weights, io: kda_io, slots: torch.T
                             _stream(stream)), "kda_decode")
 
 
-def kda_state_prefetch(pool: StatePool, slots: torch.Tensor, B: int | None = None, stream=None) -> None:
-    """Hint: bring the slots' state and conv tail into L2 ahead of a decode."""
+def kda_state_prefetch(pool: StatePool, slots: torch.Tensor, B: int | None = None, stream=None,
+                       weights: kda_weights | None = None) -> None:
+    """Hint: bring the slots' state and conv tail (and the weights, if given)
+    into L2 ahead of a decode."""
     B = slots.numel() if B is None else B
-    _check(lib().kda_state_prefetch(pool.handle, _dptr(slots), int(B), _stream(stream)), "kda_state_prefetch")
+    wp = ctypes.byref(weights) if weights is not None else None
+    _check(lib().kda_state_prefetch(pool.handle, wp, _dptr(slots), int(B), _stream(stream)), "kda_state_prefetch")
 
 
 def kda_verify(pool: StatePool, weights: kda_weights, io: kda_io, in_slots: torch.Tensor, snap_slots: torch.Tensor,

@@ -195,15 +195,18 @@ KDA_API kda_status kda_decode(kda_pool *pool, const kda_weights *w, const kda_io
 /* Asks L2 to fetch the state and conv tail of slots[0..B) (a DEVICE array)
  * ahead of a kda_decode / kda_verify that reads them, for example one layer
  * early while other layers run: a decode whose state has left L2 otherwise
- * waits on a chain of round trips to HBM.  A hint: results never depend on
- * it, it changes no memory, and a slot outside the pool is skipped.  It
- * pays while the prefetched slots fit in L2 (129 MB; a slot is 4.3 MB at
- * H = 64, d = 128, bf16), so small batches.  One small kernel on `stream`;
- * B = 0 is a no-op.  Errors: KDA_ERR_INVALID_ARG (null pool or slots,
- * B < 0), KDA_ERR_CUDA.
+ * waits on a chain of round trips to HBM.  With w non-null the layer's conv
+ * taps and norm weight are fetched too (w is checked like kda_decode's; NULL
+ * fetches the slots only).  A hint: results never depend on it, it changes
+ * no memory, and a slot outside the pool is skipped.  It pays while the
+ * prefetched slots fit in L2 (129 MB; a slot is 4.3 MB at H = 64, d = 128,
+ * bf16), so small batches.  One small kernel on `stream`; B = 0 is a no-op.
+ * Errors: KDA_ERR_INVALID_ARG (null pool or slots, B < 0, bad weights),
+ * KDA_ERR_CUDA.
  * Source: "vLLM Kimi K3 지원", section "Fused Kernels 및 메타데이터 최적화",
  * KDA Decode bullet (the decode step is bound by its repeated state traffic). */
-KDA_API kda_status kda_state_prefetch(kda_pool *pool, const int32_t *slots, int32_t B, kda_stream_t stream);
+KDA_API kda_status kda_state_prefetch(kda_pool *pool, const kda_weights *w, const int32_t *slots, int32_t B,
+                                      kda_stream_t stream);
 
 /* Speculative verify: B sequences each advance T draft tokens (1 <= T <= 16)
  * in one launch.  Token (b, t) is io row b*T + t.  Sequence b starts from slot

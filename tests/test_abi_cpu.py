@@ -107,5 +107,12 @@ def test_profile_argument_errors(lib):
     assert lib.kda_profile_stop(ctypes.byref(out)) == kda.KDA_ERR_INVALID_ARG
 
 
+def test_state_prefetch_argument_errors(lib):
+    """kda_state_prefetch rejects a null pool, a null table and a negative
+    batch before launching anything."""
+    assert lib.kda_state_prefetch(None, None, None, 1, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_state_prefetch(None, None, None, -1, None) == kda.KDA_ERR_INVALID_ARG
+
+
 def test_pool_flags_reject_a_null_pool_and_unknown_bits(lib):
     assert lib.kda_state_pool_set_flags(None, 0) == kda.KDA_ERR_INVALID_ARG

@@ -369,7 +369,8 @@ def test_inputs_written_by_the_preceding_kernel(graph):
 def test_state_prefetch_changes_nothing():
     """kda_state_prefetch is an L2 hint: a decode after it equals the same
     decode without it bit for bit, the pool is untouched by the prefetch
-    itself, and an out-of-range slot in its table is skipped silently."""
+    itself (with and without the weights), and an out-of-range slot in its
+    table is skipped silently."""
     H, D, act, B = 4, 128, torch.bfloat16, 3
     ma = Mirror(8, H, D, act, _weights(93, H, D, act))
     mb = Mirror(8, H, D, act, _weights(93, H, D, act))
@@ -380,6 +381,7 @@ def test_state_prefetch_changes_nothing():
     before = mb.gpu.states().clone(), mb.gpu.tails().clone()
     table = torch.tensor(slots + [99, -1], dtype=torch.int32, device="cuda")
     kda.kda_state_prefetch(mb.gpu, table)
+    kda.kda_state_prefetch(mb.gpu, table, weights=mb.w)
     torch.cuda.synchronize()
     assert torch.equal(mb.gpu.states(), before[0]) and torch.equal(mb.gpu.tails(), before[1])
     assert kda.kda_poll_device_error(mb.gpu) == (kda.KDA_OK, 0)
