@@ -21,23 +21,23 @@
 //
 // Schedule: the chunks of a call are cut into windows.  Per window the intra
 // kernel(s) run on the caller's stream, then the window's chain on a
-// high-priority side stream and its gated norm on a third, so the chain and
-// the norm of one window overlap the intra work of the next.  The
-// per-(chunk, head) records live in a ring of two windows: window w + 2
-// reuses window w's records once its norm has run, so the workspace does not
-// grow with the prompt.  The tails run on the caller's stream after the join.
+// high-priority side stream, so the chain of one window overlaps the intra
+// work of the next.  The per-(chunk, head) records live in a ring of two
+// windows: window w + 2 reuses window w's records once its chain has run, so
+// the workspace does not grow with the prompt.  The tails run on the caller's
+// stream after the join.
 //   meta   (device-built tables only, one CTA): sequence, chunk and
 //          checkpoint tables from device arrays.
 //   chain  (sequence, head): sequential over chunks; S^T (fp32) lives in
-//          TMEM; the next chunk's operand images stream in by TMA bulk copies
-//          while the current chunk computes; interval checkpoints; end state
-//          -> slot.
-//   out    (chunk, head): gated RMSNorm of O -> out.
+//          registers; the next chunk's operand images stream in by TMA bulk
+//          copies while the current chunk computes; the gated RMSNorm of
+//          each chunk's O -> out; interval checkpoints; end state -> slot.
 //   tails  checkpoint tails, then end tails -> slots.
 #include "kda_prefill.cuh"
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -47,11 +47,14 @@ namespace pf {
 namespace {
 
 constexpr int kRingWindows = 2;   // windows of records the ring holds
-constexpr int kWindowChunks = 32; // chunks per window of a call long enough to be split
+constexpr int kWindowChunks = 48; // chunks per window of a call long enough to be split
 constexpr int kSplitChunks = 64;  // calls with fewer chunks run as one window
 constexpr int kEventSlots = 8;    // per-window events, reused cyclically (more than kRingWindows + 1)
 
 // ============================================================== chain ====
+// bf16 value of a 16-bit shared-memory word
+__device__ __forceinline__ float bf16_word(uint16_t w) { return __uint_as_float(uint32_t(w) << 16); }
+
 namespace cs {  // chain shared-memory map
 constexpr uint32_t A1_HI = 0, A1_LO = 32768;             // S^T images [128 j][128 i]
 constexpr uint32_t B1 = 65536;                            // the record's WQ images (64 KiB)
@@ -62,10 +65,17 @@ constexpr uint32_t PP_HI = B2 + uint32_t(Rec::PP_HI - Rec::KH_HI), PP_LO = B2 + 
 constexpr uint32_t GAM = B2 + uint32_t(Rec::GAM - Rec::KH_HI), ELC = B2 + uint32_t(Rec::ELC - Rec::KH_HI);
 constexpr uint32_t A2_HI = 181248, A2_LO = 181248 + 16384;  // U^T images [128 j][64 r]
 constexpr uint32_t GCUR = A2_LO + 16384;                   // gamma, elc of the current chunk [2][128]
-constexpr uint32_t BARS = GCUR + 1024;
-constexpr uint32_t BYTES = BARS + 512;
+constexpr uint32_t RED = GCUR + 1024;                      // per-warp sums of O^2 [4 lane quarters][64 tokens]
+constexpr uint32_t BARS = RED + 1024;
+// bf16 gate tile of a chunk (tokens [32 half][128 channels]): half 0 in the
+// record's PP lo slot of B2 (never loaded for bf16 outputs), half 1 here
+constexpr uint32_t GATE0 = PP_LO, GATE1 = (BARS + 512 + 1023) / 1024 * 1024;
+constexpr uint32_t BYTES = GATE1 + 8192;
 }  // namespace cs
 static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
+static_assert(cs::GATE0 + 8192 <= cs::B2 + Rec::B2_BYTES && cs::GATE0 >= cs::B2 + Rec::B2_BYTES_HI &&
+                  cs::GATE0 % 1024 == 0,
+              "gate half 0 sits in the PP lo slot");
 
 // One CTA (8 warps) per (sequence, head), walking the window's chunks in
 // order.  Thread (j, half) keeps S^T row j, columns 64 half .. + 63, in fp32
@@ -76,15 +86,26 @@ static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
 //   U^T      = Ut^T - (W S)^T, split into hi / lo images
 //   stage 2  (K^^T U)^T = U^T K^ (K^ read MN-major), (P U)^T = U^T P^T
 //   S^T     <- S^T diag(gamma) + (K^^T U)^T diag(elc),  O^T = (Q S)^T + (P U)^T
+//   out      = w_n . O / sqrt(mean_j O^2 + eps) . sigmoid(gate), per token
 // Without the lo halves of Q and P (q_lo = 0, bf16 outputs) the Q rows of
 // the WQ lo image stay zero in shared memory and (P U)^T takes one product.
-__global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams p) {
+// bf16: the chunk's gate tile arrives by two TMA loads (tm_g: a box of 32
+// tokens) issued a step ahead, and each half of the outputs that the chunk
+// fills replaces its gate half in place and leaves by a TMA store (tm_o);
+// fp32, and the partial halves of a sequence's last chunk: each thread loads
+// its 32 gate values or stores its outputs itself.
+template <typename Act>
+__global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams p,
+                                                           const __grid_constant__ CUtensorMap tm_g,
+                                                           const __grid_constant__ CUtensorMap tm_o) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1 KiB-aligned, still shared
     uint64_t *bar_b1 = reinterpret_cast<uint64_t *>(sm + cs::BARS);
-    uint64_t *bar_b2 = bar_b1 + 1, *bar_m1 = bar_b1 + 2, *bar_m2 = bar_b1 + 3;
-    uint32_t *tbase = reinterpret_cast<uint32_t *>(bar_b1 + 4);
+    uint64_t *bar_b2 = bar_b1 + 1, *bar_m1 = bar_b1 + 2, *bar_m2 = bar_b1 + 3, *bar_g = bar_b1 + 4;
+    uint32_t *tbase = reinterpret_cast<uint32_t *>(bar_b1 + 5);
+    constexpr bool kGateTile = sizeof(Act) == 2;
     float *gcur = reinterpret_cast<float *>(sm + cs::GCUR);
+    float *red = reinterpret_cast<float *>(sm + cs::RED);
     // 8 warps: warps w and w + 4 share TMEM lanes 32*(w % 4) .. +31 (value
     // channel j = TMEM lane) and split every row's columns between them.
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -104,7 +125,7 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
     float *slot_state = p.states + size_t(sq.slot) * p.H * head_elems + size_t(h) * head_elems;  // S^T [j][i]
     const uint32_t sbase = smem_u32(sm);
     if (tid == 0) {
-        for (int b = 0; b < 4; ++b) mbar_init(bar_b1 + b, 1);
+        for (int b = 0; b < 5; ++b) mbar_init(bar_b1 + b, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tbase, 512);
@@ -134,7 +155,7 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             *reinterpret_cast<uint4 *>(sm + cs::WQ_LO + kb * 16384 + 8192 + off) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    const uint32_t ut_bytes = uint32_t(Rec::OO - Rec::UT);
+    const uint32_t ut_bytes = uint32_t(Rec::BYTES - Rec::UT);
     auto prefetch_rec = [&](const char *r) {  // into L2: the bulk loads and the Ut^T rows of a later step
         bulk_prefetch_l2(r + Rec::WQ_HI, p.q_lo ? Rec::B1_BYTES : 32768u);
         if (!p.q_lo) {
@@ -144,9 +165,24 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         bulk_prefetch_l2(r + Rec::KH_HI, b2_bytes);
         bulk_prefetch_l2(r + Rec::UT, ut_bytes);
     };
+    const size_t HD = size_t(p.H) * D;
+    // bf16 gate tiles and output halves move through one thread: thread 0
+    // loads the first chunk's gate tile, thread 32 the others (and stores
+    // the outputs; its bulk group is waited on before they are overwritten)
+    auto load_gate = [&](int row0) {
+        mbar_arrive_expect_tx(bar_g, 2 * 8192);
+        tma_load_3d(sm + cs::GATE0, &tm_g, bar_g, 0, h, row0);
+        tma_load_3d(sm + cs::GATE1, &tm_g, bar_g, 0, h, row0 + 32);
+    };
+    auto store_out = [&](const ChunkMeta &m) {  // the staged (full) output halves of chunk m
+        if (m.len >= 32) tma_store_3d(&tm_o, sm + cs::GATE0, 0, h, m.row0);
+        if (m.len >= 64) tma_store_3d(&tm_o, sm + cs::GATE1, 0, h, m.row0 + 32);
+        bulk_commit();
+    };
     if (tid == 0 && c_hi > c_lo) {
         load_rec(rec_ptr(p, sq.chunk0 + c_lo, h));
         if (c_lo + 1 < c_hi) prefetch_rec(rec_ptr(p, sq.chunk0 + c_lo + 1, h));
+        if (kGateTile) load_gate(p.chunks[sq.chunk0 + c_lo].row0);
     }
     const int sc0 = half * 64;  // this thread's 64 columns of the S^T row
     // S^T row j (64 columns) in registers; hi/lo into the A1 images
@@ -181,12 +217,20 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
     const Operand kh_img{sbase + cs::KH_HI, sbase + cs::KH_LO, true, CH * 128};
     const Operand pp_img{sbase + cs::PP_HI, sbase + cs::PP_LO, false, CH * 128};
     const int uc0 = half * 32;  // this thread's 32 columns of the U / O rows
+    const float wn = to_f32(static_cast<const Act *>(p.norm_w)[j]);
+    ChunkMeta pcm{};  // the previous chunk (its outputs still staged)
     for (int c = c_lo; c < c_hi && ok; ++c) {
         const int g = sq.chunk0 + c;
         char *rec = rec_ptr(p, g, h);
+        const ChunkMeta cm = p.chunks[g];
         const uint32_t par = uint32_t((c - c_lo) & 1);
         ok = __syncthreads_and(mbar_wait(bar_b1, par, p.err));
         if (!ok) break;
+        if (kGateTile && tid == 32 && c > c_lo) {  // previous outputs out, this chunk's gate tile in
+            store_out(pcm);
+            bulk_wait_read();
+            load_gate(cm.row0);
+        }
         if (tid == 0) {
             tc_fence_after();
             mma_split(tm + 0, s_img, wq_img, D, id_s1, 3, false);
@@ -245,6 +289,14 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             mma_split(tm + 256, u_img, pp_img, CH, id_pp, p.q_lo ? 3 : 1, false);
             mma_commit(bar_m2);
         }
+        // fp32: the gate logits of tokens uc0 .. uc0 + 31 at channel j, under the MMAs
+        constexpr int kGt = kGateTile ? 1 : 32;
+        float gt[kGt];
+        if (!kGateTile) {
+            const Act *gp = static_cast<const Act *>(p.gate) + size_t(cm.row0 + uc0) * HD + size_t(h) * D + j;
+#pragma unroll
+            for (int e = 0; e < kGt; ++e) gt[e] = uc0 + e < cm.len ? to_f32(gp[size_t(e) * HD]) : 0.f;
+        }
         ok = __syncthreads_and(mbar_wait(bar_m2, par, p.err));
         if (!ok) break;
         tc_fence_after();
@@ -252,20 +304,55 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             mbar_arrive_expect_tx(bar_b2, b2_bytes);
             bulk_load(sm + cs::B2, rec_ptr(p, g + 1, h) + Rec::KH_HI, b2_bytes, bar_b2);
         }
-        // O column j (rows uc0 .. uc0 + 31) = (Q S)^T + (P U)^T -> record, coalesced across the warp
+        // O at channel j, tokens uc0 .. uc0 + 31 = (Q S)^T + (P U)^T, then the
+        // gated RMSNorm over the head's channels -> out (coalesced across the warp)
         {
-            float* O = reinterpret_cast<float *>(rec + Rec::OO);
-            float v[2][16], w2[2][16];
+            float o[32];
+            {
+                float v[2][16], w2[2][16];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                tmem_ld16(tl + 64 + uc0 + 16 * q, v[q]);
-                tmem_ld16(tl + 256 + uc0 + 16 * q, w2[q]);
+                for (int q = 0; q < 2; ++q) {
+                    tmem_ld16(tl + 64 + uc0 + 16 * q, v[q]);
+                    tmem_ld16(tl + 256 + uc0 + 16 * q, w2[q]);
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[16 * q + e] = v[q][e] + w2[q][e];
             }
-            tmem_wait_ld();
+            // per token, the sum of O^2 over this warp's 32 channels: a
+            // transpose-reduce over the lanes leaves token uc0 + lane's in lane
+            float a[32];
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
+            for (int e = 0; e < 32; ++e) a[e] = o[e] * o[e];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) O[(uc0 + 16 * q + e) * D + j] = v[q][e] + w2[q][e];
+            for (int wd = 16; wd >= 1; wd >>= 1) {
+                const bool up = (lane & wd) != 0;
+#pragma unroll
+                for (int e = 0; e < wd; ++e) {
+                    const float send = up ? a[e] : a[e + wd];
+                    const float keep = up ? a[e + wd] : a[e];
+                    a[e] = keep + __shfl_xor_sync(0xffffffffu, send, wd);
+                }
+            }
+            red[(warp & 3) * CH + uc0 + lane] = a[0];
+            // the four warps of this half of the tokens (named barrier 1 + half)
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
+            const float ss = (red[uc0 + lane] + red[CH + uc0 + lane]) + (red[2 * CH + uc0 + lane] + red[3 * CH + uc0 + lane]);
+            const float rl = rsqrtf(ss * (1.0f / D) + p.eps_rms);
+            Act *op = static_cast<Act *>(p.out) + size_t(cm.row0 + uc0) * HD + size_t(h) * D + j;
+            uint16_t *gs = reinterpret_cast<uint16_t *>(sm + (half ? cs::GATE1 : cs::GATE0)) + j;
+            if (kGateTile) ok = mbar_wait(bar_g, par, p.err) && ok;
+            const bool staged = kGateTile && uc0 + 32 <= cm.len;  // this half leaves by a TMA store
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float r = __shfl_sync(0xffffffffu, rl, e);
+                const float gv = kGateTile ? bf16_word(gs[e * D]) : gt[kGateTile ? 0 : e];
+                const float y = wn * (o[e] * r) * (kGateTile ? sigmoid_tanh(gv) : sigmoid_fast(gv));
+                if (staged) gs[e * D] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+                else if (uc0 + e < cm.len) op[size_t(e) * HD] = from_f32<Act>(y);
+            }
         }
         // S^T row j <- gamma . S^T row j + elc . (K^^T U)^T row j; refresh the A1 images
         {
@@ -287,7 +374,6 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
             *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
         }
-        const ChunkMeta cm = p.chunks[g];
         for (int k = 0; k < cm.ck_count; ++k) {  // interval checkpoints of this chunk end
             const CkptMeta ck = p.ckpts[cm.ck_begin + k];
             float *dst = p.states + size_t(ck.dst_slot) * p.H * head_elems + size_t(h) * head_elems + size_t(j) * D + sc0;
@@ -296,8 +382,9 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        ok = __syncthreads_and(ok);
         tc_fence_after();
+        pcm = cm;
     }
     // end state S^T row j (this thread's 64 columns) -> slot
     if (ok) {
@@ -305,42 +392,28 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
 #pragma unroll
         for (int e = 0; e < 64; e += 4) *reinterpret_cast<float4 *>(drow + e) = make_float4(sr[e], sr[e + 1], sr[e + 2], sr[e + 3]);
     }
+    if (kGateTile && tid == 32) {  // the last chunk's outputs; every store done before the CTA leaves
+        if (ok && c_hi > c_lo) store_out(pcm);
+        bulk_wait();
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-// ================================================================ out ====
-template <typename Act>
-__global__ void __launch_bounds__(128) prefill_out_kernel(const PrefillParams p) {
-    const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const ChunkMeta cm = p.chunks[g];
-    const float *O = reinterpret_cast<const float *>(rec_ptr(p, g, h) + Rec::OO);
-    const Act *gate = static_cast<const Act *>(p.gate);
-    Act *out = static_cast<Act *>(p.out);
-    const size_t HD = size_t(p.H) * D;
-    const Act *nwp = static_cast<const Act *>(p.norm_w) + lane * 4;  // no alignment asked of norm_w
-    const float4 wn = make_float4(to_f32(nwp[0]), to_f32(nwp[1]), to_f32(nwp[2]), to_f32(nwp[3]));
-    for (int t = warp; t < cm.len; t += 4) {
-        const size_t base = size_t(cm.row0 + t) * HD + size_t(h) * D + lane * 4;
-        const float4 o4 = ld4(O + t * D + lane * 4);
-        const float4 g4 = act4(gate + base);
-        float ss = fmaf(o4.x, o4.x, fmaf(o4.y, o4.y, fmaf(o4.z, o4.z, o4.w * o4.w)));
-        for (int s = 16; s; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
-        const float r = rsqrtf(ss * (1.0f / D) + p.eps_rms);
-        store4(out + base, make_float4(wn.x * (o4.x * r) * sigmoid_f(g4.x), wn.y * (o4.y * r) * sigmoid_f(g4.y),
-                                       wn.z * (o4.z * r) * sigmoid_f(g4.z), wn.w * (o4.w * r) * sigmoid_f(g4.w)));
-    }
-}
-
 // ============================================================== tails ====
 // Conv tail after `pos` tokens of a segment: raw inputs at pos-3 .. pos-1
 // (before the segment: the slot's old tail, or zeros for a new sequence).
-// One block per checkpoint request when ckpt_pass, else per sequence; the
-// request pass runs first because it may read a sequence slot's old tail.
+// blockIdx.x is the checkpoint request when ckpt_pass, else the sequence; a
+// thread moves 8 consecutive channels (16 or 32 bytes, one stream: H d is a
+// multiple of 8) of the three rows, blockIdx.y the block of 256 x 8
+// channels.  The request pass runs first because it may read a sequence
+// slot's old tail.
 template <typename Act>
 __global__ void __launch_bounds__(256) prefill_tails_kernel(const PrefillParams p, int ckpt_pass) {
     const int item = blockIdx.x;
+    const int ch = 8 * (int(blockIdx.y) * 256 + int(threadIdx.x));
+    if (ch >= p.n_ch) return;
     int seq, pos, dst;
     if (ckpt_pass) {
         const CkptMeta ck = p.ckpts[item];
@@ -354,20 +427,25 @@ __global__ void __launch_bounds__(256) prefill_tails_kernel(const PrefillParams 
     }
     if (seq < 0 || dst < 0 || p.seqs[seq].slot < 0) return;  // disabled by the device metadata check
     const SeqMeta sq = p.seqs[seq];
-    const Act *old = static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch;
-    Act *nt = static_cast<Act *>(p.tails) + size_t(dst) * 3 * p.n_ch;
-    const int HD = p.H * D;
-    for (int ch = threadIdx.x; ch < p.n_ch; ch += blockDim.x) {
-        const int s = ch / HD, rem = ch - s * HD;
-        const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
-        Act x[3];
-        for (int jj = 0; jj < 3; ++jj) {
-            const int q = pos - 3 + jj;
-            if (q >= 0) x[jj] = src[size_t(sq.row0 + q) * HD + rem];
-            else x[jj] = sq.has_init ? old[size_t(3 + q) * p.n_ch + ch] : from_f32<Act>(0.f);
-        }
-        for (int jj = 0; jj < 3; ++jj) nt[size_t(jj) * p.n_ch + ch] = x[jj];
+    constexpr int kWords = int(sizeof(Act)) / 2;  // 16-byte words per 8 values
+    const uint4 *old = reinterpret_cast<const uint4 *>(static_cast<const Act *>(p.tails) + size_t(sq.slot) * 3 * p.n_ch + ch);
+    uint4 *nt = reinterpret_cast<uint4 *>(static_cast<Act *>(p.tails) + size_t(dst) * 3 * p.n_ch + ch);
+    const int HD = p.H * D, s = ch / HD, rem = ch - s * HD;
+    const Act *src = static_cast<const Act *>(s == 0 ? p.q : (s == 1 ? p.k : p.v));
+    const size_t row_words = size_t(p.n_ch) / 8 * kWords;  // one tail row in 16-byte words
+    uint4 x[3][kWords];
+#pragma unroll
+    for (int jj = 0; jj < 3; ++jj) {
+        const int q = pos - 3 + jj;
+        const uint4 *from = q >= 0 ? reinterpret_cast<const uint4 *>(src + size_t(sq.row0 + q) * HD + rem)
+                                   : (sq.has_init ? old + size_t(3 + q) * row_words : nullptr);
+#pragma unroll
+        for (int u = 0; u < kWords; ++u) x[jj][u] = from ? from[u] : make_uint4(0u, 0u, 0u, 0u);
     }
+#pragma unroll
+    for (int jj = 0; jj < 3; ++jj)
+#pragma unroll
+        for (int u = 0; u < kWords; ++u) nt[size_t(jj) * row_words + u] = x[jj][u];
 }
 
 // ============================================================ metadata ===
@@ -506,8 +584,9 @@ __global__ void __launch_bounds__(kMetaThreads) prefill_meta_kernel(const MetaAr
 // ================================================================ host ===
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace: the tables, the fast kernel's fallback list (count + g * H + h
-// entries of one window), then the record ring.
+// Workspace: the tables, the fast kernel's two fallback lists (counts, then
+// g * H + h entries of one window each; windows alternate), then the record
+// ring.
 struct WsLayout {
     size_t seqs, chunks, ckpts, fb, rec, total;
     int window;        // chunks per window
@@ -527,7 +606,7 @@ WsLayout ws_layout(int N, long long n_chunks, long long n_reqs, int H, int windo
     L.chunks = align256(L.seqs + sizeof(SeqMeta) * size_t(N));
     L.ckpts = align256(L.chunks + sizeof(ChunkMeta) * size_t(n_chunks));
     L.fb = align256(L.ckpts + sizeof(CkptMeta) * size_t(std::max<long long>(n_reqs, 1)));
-    L.rec = (L.fb + 16 + sizeof(uint32_t) * size_t(window) * size_t(H) + 1023) / 1024 * 1024;
+    L.rec = (L.fb + 32 + 2 * sizeof(uint32_t) * size_t(window) * size_t(H) + 1023) / 1024 * 1024;
     L.total = L.rec + Rec::BYTES * size_t(L.ring_windows) * size_t(window) * size_t(H);
     return L;
 }
@@ -616,9 +695,8 @@ constexpr size_t kChainSmem = 1024 + cs::BYTES;
 // kernels.  Not memory: nothing here allocates device memory.
 struct SideStream {
     cudaStream_t s = nullptr;  // chain (highest priority)
-    cudaStream_t o = nullptr;  // gated norm of finished windows
-    cudaEvent_t intra_done[kEventSlots] = {}, chain_done[kEventSlots] = {}, out_done[kEventSlots] = {};
-    cudaEvent_t start = nullptr, s_done = nullptr, o_done = nullptr;
+    cudaEvent_t intra_done[kEventSlots] = {}, chain_done[kEventSlots] = {};
+    cudaEvent_t start = nullptr, s_done = nullptr;
     bool ok = false;
 };
 
@@ -632,15 +710,12 @@ SideStream *side_stream() {
         int lo = 0, hi = 0;
         if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return;
         if (cudaStreamCreateWithPriority(&x.s, cudaStreamNonBlocking, hi) != cudaSuccess) return;
-        if (cudaStreamCreateWithPriority(&x.o, cudaStreamNonBlocking, lo) != cudaSuccess) return;
         for (int i = 0; i < kEventSlots; ++i)
             if (cudaEventCreateWithFlags(&x.intra_done[i], cudaEventDisableTiming) != cudaSuccess ||
-                cudaEventCreateWithFlags(&x.chain_done[i], cudaEventDisableTiming) != cudaSuccess ||
-                cudaEventCreateWithFlags(&x.out_done[i], cudaEventDisableTiming) != cudaSuccess)
+                cudaEventCreateWithFlags(&x.chain_done[i], cudaEventDisableTiming) != cudaSuccess)
                 return;
         if (cudaEventCreateWithFlags(&x.start, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&x.s_done, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&x.o_done, cudaEventDisableTiming) != cudaSuccess)
+            cudaEventCreateWithFlags(&x.s_done, cudaEventDisableTiming) != cudaSuccess)
             return;
         x.ok = true;
     });
@@ -659,15 +734,18 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
     kda_status st;
     if ((st = kFast ? intra_fast_prepare() : KDA_OK) != KDA_OK) return st;
     if ((st = intra_generic_prepare<Act>()) != KDA_OK) return st;
-    if ((st = set_smem(prefill_chain_kernel, kChainSmem)) != KDA_OK) return st;
+    if ((st = set_smem(prefill_chain_kernel<Act>, kChainSmem)) != KDA_OK) return st;
     PrefillParams p = p0;
     p.ring_chunks = L.ring_windows * L.window;
     p.q_lo = kFast ? 0 : 1;  // exp(G) . q and P feed only the output: bf16 outputs keep their hi halves
-    CUtensorMap mq, mk, mv, ma;
+    CUtensorMap mq, mk, mv, ma, mg, mo;
+    std::memset(&mg, 0, sizeof(mg));  // fp32: the chain loads its gate values and stores its outputs itself
+    std::memset(&mo, 0, sizeof(mo));
     if (n_chunks > 0) {
         const int es = int(sizeof(Act));
         if (!make_map(&mq, io->q, n_tok, p.H, es, CH + HALO) || !make_map(&mk, io->k, n_tok, p.H, es, CH + HALO) ||
-            !make_map(&mv, io->v, n_tok, p.H, es, CH + HALO) || !make_map(&ma, io->alpha, n_tok, p.H, es, CH))
+            !make_map(&mv, io->v, n_tok, p.H, es, CH + HALO) || !make_map(&ma, io->alpha, n_tok, p.H, es, CH) ||
+            (kFast && (!make_map(&mg, io->gate, n_tok, p.H, es, 32) || !make_map(&mo, io->out, n_tok, p.H, es, 32))))
             return KDA_ERR_CUDA;
     }
     int dev = 0, sms = 152;
@@ -680,7 +758,7 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
     static std::mutex enqueue_mu;
     std::lock_guard<std::mutex> lock(enqueue_mu);
     SideStream *side = n_win >= 2 ? side_stream() : nullptr;
-    cudaStream_t cs = side ? side->s : stream, os = side ? side->o : stream;
+    cudaStream_t cs = side ? side->s : stream;
     // An event call that fails after kernels are queued on the side streams:
     // join them to the caller's stream as far as the runtime still allows, so
     // nothing of this call runs after the caller's stream has moved past it
@@ -688,13 +766,15 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
     auto fail = [&]() {
         if (side) {
             cudaEventRecord(side->s_done, cs);
-            cudaEventRecord(side->o_done, os);
             cudaStreamWaitEvent(stream, side->s_done, 0);
-            cudaStreamWaitEvent(stream, side->o_done, 0);
         }
         cudaGetLastError();
         return KDA_ERR_CUDA;
     };
+    // the fast kernel of window w lists the chunks it leaves to the generic
+    // kernel in list w mod 2; the generic kernel walks it on the chain's stream
+    // just before that window's chain, which then clears its count for window w + 2
+    if (kFast && cudaMemsetAsync(p.fb_count, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (side) {  // the chain stream starts after everything already on the caller's stream
         if (cudaEventRecord(side->start, stream) != cudaSuccess || cudaStreamWaitEvent(cs, side->start, 0) != cudaSuccess)
             return fail();
@@ -702,19 +782,19 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
     for (long long w = 0; w < n_win; ++w) {
         const long long lo = std::min(n_chunks, w * W), hi = std::min(n_chunks, (w + 1) * W);
         const int ev = int(w % kEventSlots);
-        // window w writes the records window w - kRingWindows used: after that window's norm
+        // window w writes the records window w - kRingWindows used: after that window's chain
         if (side && w >= L.ring_windows &&
-            cudaStreamWaitEvent(stream, side->out_done[(w - L.ring_windows) % kEventSlots], 0) != cudaSuccess)
+            cudaStreamWaitEvent(stream, side->chain_done[(w - L.ring_windows) % kEventSlots], 0) != cudaSuccess)
             return fail();
+        PrefillParams pw = p;  // this window's fallback list
+        pw.fb_count = p.fb_count + (w & 1);
+        pw.fb_list = p.fb_list + size_t(w & 1) * size_t(W) * size_t(p.H);
         if (hi > lo) {
             p.chunk_base = int(lo);
+            pw.chunk_base = int(lo);
             const dim3 grid(unsigned(hi - lo), unsigned(p.H));
             if (kFast) {
-                // the fast kernel lists the chunks it leaves to the generic kernel
-                // (p.fb_list set: the fast kernel appends to it, the generic kernel walks it)
-                if (cudaMemsetAsync(p.fb_count, 0, sizeof(uint32_t), stream) != cudaSuccess) return fail();
-                if ((st = launch_intra_fast(p, mq, mk, mv, ma, grid, stream)) != KDA_OK) return fail();
-                if ((st = launch_intra_generic<Act>(p, mq, mk, mv, ma, dim3(fb_ctas), stream)) != KDA_OK) return fail();
+                if ((st = launch_intra_fast(pw, mq, mk, mv, ma, grid, stream)) != KDA_OK) return fail();
             } else {
                 PrefillParams pg = p;
                 pg.fb_list = nullptr;  // grid mode: one CTA per (chunk, head) of the window
@@ -730,37 +810,27 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
                 cudaStreamWaitEvent(cs, side->intra_done[ev], 0) != cudaSuccess)
                 return fail();
         }
+        if (kFast && hi > lo) {
+            if ((st = launch_intra_generic<Act>(pw, mq, mk, mv, ma, dim3(fb_ctas), cs)) != KDA_OK) return fail();
+            if (cudaMemsetAsync(pw.fb_count, 0, sizeof(uint32_t), cs) != cudaSuccess) return fail();
+        }
         if (rg.hi > rg.lo) {
             p.seq_base = rg.lo;
             const ProfScope prof(KDA_KERNEL_PREFILL_CHAIN, cs);
-            prefill_chain_kernel<<<unsigned(rg.hi - rg.lo) * unsigned(p.H), 256, kChainSmem, cs>>>(p);
+            prefill_chain_kernel<Act><<<unsigned(rg.hi - rg.lo) * unsigned(p.H), 256, kChainSmem, cs>>>(p, mg, mo);
         }
-        if (hi > lo) {  // gated norm of the window's chunks once their chain is done, off the chain's stream
-            if (side) {
-                if (cudaEventRecord(side->chain_done[ev], cs) != cudaSuccess ||
-                    cudaStreamWaitEvent(os, side->chain_done[ev], 0) != cudaSuccess)
-                    return fail();
-            }
-            PrefillParams po = p;
-            po.chunk_base = int(lo);
-            {
-                const ProfScope prof(KDA_KERNEL_PREFILL_OUT, os);
-                prefill_out_kernel<Act><<<dim3(unsigned(hi - lo), unsigned(p.H)), 128, 0, os>>>(po);
-            }
-            if (side && cudaEventRecord(side->out_done[ev], os) != cudaSuccess) return fail();
-        }
+        if (side && cudaEventRecord(side->chain_done[ev], cs) != cudaSuccess) return fail();
     }
     if (side) {
-        if (cudaEventRecord(side->s_done, cs) != cudaSuccess || cudaEventRecord(side->o_done, os) != cudaSuccess ||
-            cudaStreamWaitEvent(stream, side->s_done, 0) != cudaSuccess ||
-            cudaStreamWaitEvent(stream, side->o_done, 0) != cudaSuccess)
+        if (cudaEventRecord(side->s_done, cs) != cudaSuccess || cudaStreamWaitEvent(stream, side->s_done, 0) != cudaSuccess)
             return fail();
     }
     p.chunk_base = 0;
     {
         const ProfScope prof(KDA_KERNEL_PREFILL_TAILS, stream);
-        if (n_reqs > 0) prefill_tails_kernel<Act><<<n_reqs, 256, 0, stream>>>(p, 1);
-        prefill_tails_kernel<Act><<<N, 256, 0, stream>>>(p, 0);
+        const unsigned ch_blocks = unsigned((p.n_ch / 8 + 255) / 256);
+        if (n_reqs > 0) prefill_tails_kernel<Act><<<dim3(unsigned(n_reqs), ch_blocks), 256, 0, stream>>>(p, 1);
+        prefill_tails_kernel<Act><<<dim3(unsigned(N), ch_blocks), 256, 0, stream>>>(p, 0);
     }
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -779,8 +849,8 @@ kda_status launch_tables(const kda_pool *pool, const kda_weights *w, const kda_i
     p.seqs = reinterpret_cast<const SeqMeta *>(ws + L.seqs);
     p.chunks = reinterpret_cast<const ChunkMeta *>(ws + L.chunks);
     p.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.ckpts);
-    p.fb_count = reinterpret_cast<uint32_t *>(ws + L.fb);
-    p.fb_list = p.fb_count + 4;
+    p.fb_count = reinterpret_cast<uint32_t *>(ws + L.fb);  // [2]
+    p.fb_list = p.fb_count + 8;                             // [2][window * H]
     p.rec = ws + L.rec;
     p.states = pool->states;
     p.tails = pool->tails;

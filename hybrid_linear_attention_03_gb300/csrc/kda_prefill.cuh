@@ -17,7 +17,8 @@
 //   GAM  exp(G_last) per key channel;  ELC  exp(G_last - c) per key channel
 //   UT   Ut^T fp32 [128 value channels][64 tokens]; in row j the 16-byte
 //        chunk c (tokens 4c .. 4c + 3) sits at chunk position c ^ (j mod 16)
-//   OO   O fp32 [64 tokens][128 value channels] (the chain writes it)
+// 145 KiB in all.  O never reaches memory: the chain applies the gated norm
+// to it and writes the layer output.
 // Records live in a ring: chunk g, head h uses slot (g mod ring_chunks, h).
 #pragma once
 
@@ -60,8 +61,7 @@ struct Rec {
     static constexpr size_t GAM = PP_HI + 8192, ELC = GAM + 512;
     static constexpr size_t PP_LO = GAM + 1024;
     static constexpr size_t UT = PP_LO + 8192;
-    static constexpr size_t OO = UT + 32768;
-    static constexpr size_t BYTES = OO + 32768;
+    static constexpr size_t BYTES = UT + 32768;
     static constexpr uint32_t B1_BYTES = uint32_t(KH_HI - WQ_HI);     // WQ images
     static constexpr uint32_t B2_BYTES = uint32_t(UT - KH_HI);        // KH, PP hi, GAM, ELC, PP lo
     static constexpr uint32_t B2_BYTES_HI = uint32_t(PP_LO - KH_HI);  // the same without PP lo
@@ -107,6 +107,13 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // -88, where 2^(-x log2 e) is +inf.
 __device__ __forceinline__ float sigmoid_fast(float x) {
     return rcp_approx(1.0f + ex2_approx(-x * 1.4426950408889634f));
+}
+// sigma(x) = (1 + tanh(x / 2)) / 2 with PTX's approximate tanh (one
+// operation; relative error about 2^-11): for bf16 results only.
+__device__ __forceinline__ float sigmoid_tanh(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
+    return fmaf(0.5f, t, 0.5f);
 }
 
 // Chunk position of tokens 4c .. 4c + 3 in row j of the record's Ut^T (the

@@ -223,8 +223,12 @@ KDA_API kda_status kda_verify(kda_pool *pool, const kda_weights *w, const kda_io
                       const int32_t *in_slots, const int32_t *snap_slots, int32_t B, int32_t T,
                       kda_stream_t stream);
 
-/* Workspace bytes kda_prefill_chunked needs for these sequence lengths
- * (cu_seqlens: HOST [N+1], nondecreasing from 0).  0 on invalid input. */
+/* Workspace bytes kda_prefill_chunked prefers for these sequence lengths
+ * (cu_seqlens: HOST [N+1], nondecreasing from 0).  0 on invalid input.
+ * The workspace holds the sequence, chunk and checkpoint tables and a ring
+ * of per-(chunk, head) records (145 KiB each at d = 128) for two windows of
+ * at most 48 chunks, so it is bounded by the window, not the prompt: about
+ * 0.9 GB for any prompt length at H = 64 (the tables add 24 B per chunk). */
 KDA_API size_t kda_prefill_workspace_bytes(const kda_pool *pool, const int32_t *cu_seqlens, int32_t N,
                                    int32_t chunk);
 
@@ -237,7 +241,11 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_pool *pool, const int32_t *
  * not be a slot of this call, and a sequence's end may be checkpointed too.
  * cu_seqlens, slots, has_initial_state and reqs are HOST arrays (checked
  * here: KDA_ERR_SLOT_RANGE, KDA_ERR_ALIAS, KDA_ERR_INVALID_ARG).
- * workspace: device, 256-aligned, >= kda_prefill_workspace_bytes.
+ * workspace: device, 256-aligned.  With kda_prefill_workspace_bytes bytes the
+ * call runs in its preferred windows; a smaller workspace runs it in smaller
+ * windows (down to one chunk), with the same results bit for bit, and one too
+ * small for the tables plus a ring of one-chunk windows returns
+ * KDA_ERR_WORKSPACE with nothing enqueued.
  * Source: "vLLM Kimi K3 지원", section "Fused Kernels 및 메타데이터 최적화",
  * KDA Prefill bullet (FlashKDA), and section "에이전틱 캐시 유지 정책"
  * (interval-based retention: checkpoints every 32K tokens and at prompt
@@ -260,9 +268,11 @@ KDA_API kda_status kda_prefill_chunked(kda_pool *pool, const kda_weights *w, con
  * that the scratch is a fixed array of KDA_NOALLOC_SCRATCH_BYTES (64 MiB)
  * compiled into the library: every GPU that loads the library holds it
  * until the process exits, and no call allocates or frees device memory.
- * A call that needs more scratch than that (its kda_prefill_workspace_bytes
- * figure for its own requests; with d = 128 about 370 (chunk, head) pairs of
- * 64 tokens) returns KDA_ERR_WORKSPACE and enqueues nothing.
+ * The call runs in the largest windows the array holds (see
+ * kda_prefill_chunked's workspace), so prompts of any length fit at H = 64;
+ * a call whose tables plus a ring of one-chunk windows exceed the array (at
+ * d = 128, more than about 450 heads) returns KDA_ERR_WORKSPACE and enqueues
+ * nothing.
  * Every call looks up the array's device address with the call's device
  * current (so a device reset that reloads the library's module leaves no
  * stale address behind).  The first lookup on a device may load the module:
@@ -425,8 +435,8 @@ typedef enum {
                                   copies of the host-built tables (kda_prefill_chunked) */
     KDA_KERNEL_PREFILL_INTRA,  /* intra-chunk prefill kernel with the decay factored around the chunk's
                                   midpoint (bf16 inputs: every chunk-head of a window) */
-    KDA_KERNEL_PREFILL_CHAIN,  /* the chunk chain (state passing) */
-    KDA_KERNEL_PREFILL_OUT,    /* gated norm of the prefill outputs */
+    KDA_KERNEL_PREFILL_CHAIN,  /* the chunk chain (state passing, gated norm of the outputs) */
+    KDA_KERNEL_PREFILL_OUT,    /* unused (the chain applies the gated norm); keeps the values below */
     KDA_KERNEL_PREFILL_TAILS,  /* conv tails of checkpoints and ends */
     KDA_KERNEL_STATE_PREFETCH, /* kda_state_prefetch */
     KDA_KERNEL_PREFILL_INTRA_EXACT, /* intra-chunk prefill kernel with per-pair decay exponents (bf16

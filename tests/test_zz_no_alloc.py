@@ -80,7 +80,7 @@ def test_noalloc_prefill_refuses_requests_beyond_the_scratch():
     """The scratch holds the tables and a ring of per-(chunk, head) records
     whose windows shrink to fit; a layer with so many heads that even one
     chunk's records exceed 64 MiB is refused, with nothing enqueued."""
-    Hb = 400  # one chunk of 400 heads needs 400 records of 177 KiB: more than 64 MiB
+    Hb = 480  # one chunk of 480 heads needs 480 records of 145 KiB: more than 64 MiB
     pool = kda.StatePool(2, Hb, D, D, act)
     w = {k: v.cuda() for k, v in I.layer_weights(61, Hb, D, D, 4, act).items()}
     wgt = kda.make_weights(w["conv_w"], w["norm_w"])
@@ -97,8 +97,8 @@ def test_noalloc_prefill_refuses_requests_beyond_the_scratch():
 
 def test_noalloc_prefill_of_a_long_prompt_runs_in_small_windows():
     """A prompt whose preferred workspace is larger than the scratch (4096
-    tokens, 16 heads: 2 windows of 32 chunks x 16 heads of records, about
-    181 MiB) runs in the scratch with smaller windows and equals the
+    tokens, 16 heads: 2 windows of 48 chunks x 16 heads of records, about
+    218 MiB) runs in the scratch with smaller windows and equals the
     workspace prefill bit for bit."""
     Hs, L = 16, 4096
     pa = kda.StatePool(2, Hs, D, D, act)
