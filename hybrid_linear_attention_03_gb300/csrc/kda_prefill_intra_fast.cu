@@ -205,9 +205,11 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         mbar_arrive_expect_tx(bar_v, fs::TILE);
         tma_load_3d(sm + fs::RV, &tm_v, bar_v, 0, h, cm.row0 - HALO);
     }
-    if (tid < CH)
-        beta[tid] = tid < cm.len ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[size_t(cm.row0 + tid) * p.H + h])
-                                 : 0.f;
+    // beta of the chunk's tokens: loaded now, stored to shared memory after
+    // the decay pass (first read by the A drain), so the load is off the setup path
+    const float beta_ld = tid < CH && tid < cm.len
+                              ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[size_t(cm.row0 + tid) * p.H + h])
+                              : 0.f;
     if (tid < 128) lnm[tid] = logf(1.0f + float(tid) * (1.0f / 128.0f));  // ln of the bf16 mantissas 1 + m/128
     if (warp == 0) tmem_alloc(tbase, 256);
     tc_fence_before();
@@ -253,6 +255,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             *reinterpret_cast<float4 *>(g0s + ch0 + 4) = make_float4(l0[4], l0[5], l0[6], l0[7]);
         }
     }
+    if (tid < CH) beta[tid] = beta_ld;
     __syncthreads();
     int wide = 0;
     if (tid < D) {  // exclusive scan of the 16 warp totals of channel tid
