@@ -118,9 +118,16 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
     const int c_lo = max(sq.chunk0, p.win_lo) - sq.chunk0;
     const int c_hi = min(sq.chunk0 + sq.n_chunks, p.win_hi) - sq.chunk0;
     if (c_hi <= c_lo && !(sq.n_chunks == 0 && p.win_lo == 0)) return;
+    // a one-chunk sequence from a zero state that the intra kernel finished
+    // (outputs, end state, checkpoints): nothing left here
+    if (p.solo && sq.n_chunks == 1 && !sq.has_init && p.solo[size_t(n) * p.H + h]) return;
     // A window that continues a sequence reads the state the previous window
     // left in the slot.
     const bool load_state = sq.has_init || c_lo > 0;
+    // a sequence that starts here from a zero state: its first step has
+    // W S = Q S = 0, so that step skips stage 1 and the S image is built
+    // only at its end
+    const bool s_zero = !load_state;
     const size_t head_elems = size_t(D) * D;
     float *slot_state = p.states + size_t(sq.slot) * p.H * head_elems + size_t(h) * head_elems;  // S^T [j][i]
     const uint32_t sbase = smem_u32(sm);
@@ -193,16 +200,18 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         const float4 x = load_state ? ld4(srow + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         sr[e] = x.x; sr[e + 1] = x.y; sr[e + 2] = x.z; sr[e + 3] = x.w;
     }
+    if (!s_zero) {
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-        float x[8];
+        for (int cc = 0; cc < 8; ++cc) {
+            float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = sr[8 * cc + e];
-        uint4 vh, vl;
-        split8(x, vh, vl);
-        const uint32_t off = sw128_chunk(j, (sc0 >> 3) + cc, D);
-        *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
-        *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
+            for (int e = 0; e < 8; ++e) x[e] = sr[8 * cc + e];
+            uint4 vh, vl;
+            split8(x, vh, vl);
+            const uint32_t off = sw128_chunk(j, (sc0 >> 3) + cc, D);
+            *reinterpret_cast<uint4 *>(sm + cs::A1_HI + off) = vh;
+            *reinterpret_cast<uint4 *>(sm + cs::A1_LO + off) = vl;
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -224,6 +233,8 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         char *rec = rec_ptr(p, g, h);
         const ChunkMeta cm = p.chunks[g];
         const uint32_t par = uint32_t((c - c_lo) & 1);
+        const bool z = s_zero && c == c_lo;                            // S = 0: no stage 1
+        const uint32_t par1 = uint32_t((c - c_lo - (s_zero ? 1 : 0)) & 1);  // stage-1 commits so far
         ok = __syncthreads_and(mbar_wait(bar_b1, par, p.err));
         if (!ok) break;
         if (kGateTile && tid == 32 && c > c_lo) {  // previous outputs out, this chunk's gate tile in
@@ -233,8 +244,10 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         }
         if (tid == 0) {
             tc_fence_after();
-            mma_split(tm + 0, s_img, wq_img, D, id_s1, 3, false);
-            mma_commit(bar_m1);
+            if (!z) {
+                mma_split(tm + 0, s_img, wq_img, D, id_s1, 3, false);
+                mma_commit(bar_m1);
+            }
             if (c + 2 < c_hi) prefetch_rec(rec_ptr(p, g + 2, h));
         }
         // Ut^T row j, entries r = uc0 .. uc0 + 31, while the MMAs run
@@ -245,9 +258,11 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             const float4 x = ld4(UTg + 4 * ut_chunk(j, (uc0 + e) >> 2));
             ut[e] = x.x; ut[e + 1] = x.y; ut[e + 2] = x.z; ut[e + 3] = x.w;
         }
-        ok = __syncthreads_and(mbar_wait(bar_m1, par, p.err));
-        if (!ok) break;
-        tc_fence_after();
+        if (!z) {
+            ok = __syncthreads_and(mbar_wait(bar_m1, par1, p.err));
+            if (!ok) break;
+            tc_fence_after();
+        }
         if (tid == 0 && c + 1 < c_hi) {  // W and Q images are consumed: stream in the next chunk's
             const char *rn = rec_ptr(p, g + 1, h);
             mbar_arrive_expect_tx(bar_b1, b1_bytes);
@@ -262,9 +277,14 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
         // U^T row j = Ut^T - (W S)^T  -> hi/lo images (this thread's 32 columns)
         {
             float v[2][16];
-            tmem_ld16(tl + uc0, v[0]);
-            tmem_ld16(tl + uc0 + 16, v[1]);
-            tmem_wait_ld();
+            if (z) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[0][e] = v[1][e] = 0.f;
+            } else {
+                tmem_ld16(tl + uc0, v[0]);
+                tmem_ld16(tl + uc0 + 16, v[1]);
+                tmem_wait_ld();
+            }
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 float x[8];
@@ -311,9 +331,13 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             {
                 float v[2][16], w2[2][16];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    tmem_ld16(tl + 64 + uc0 + 16 * q, v[q]);
-                    tmem_ld16(tl + 256 + uc0 + 16 * q, w2[q]);
+                for (int q = 0; q < 2; ++q) tmem_ld16(tl + 256 + uc0 + 16 * q, w2[q]);
+                if (z) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[0][e] = v[1][e] = 0.f;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) tmem_ld16(tl + 64 + uc0 + 16 * q, v[q]);
                 }
                 tmem_wait_ld();
 #pragma unroll
@@ -585,10 +609,11 @@ __global__ void __launch_bounds__(kMetaThreads) prefill_meta_kernel(const MetaAr
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Workspace: the tables, the fast kernel's two fallback lists (counts, then
-// g * H + h entries of one window each; windows alternate), then the record
-// ring.
+// g * H + h entries of one window each; windows alternate), the flags of the
+// one-chunk sequences the fast kernel finished ([N][H] bytes), then the
+// record ring.
 struct WsLayout {
-    size_t seqs, chunks, ckpts, fb, rec, total;
+    size_t seqs, chunks, ckpts, fb, solo, rec, total;
     int window;        // chunks per window
     int ring_windows;  // windows the record ring holds
 };
@@ -606,7 +631,8 @@ WsLayout ws_layout(int N, long long n_chunks, long long n_reqs, int H, int windo
     L.chunks = align256(L.seqs + sizeof(SeqMeta) * size_t(N));
     L.ckpts = align256(L.chunks + sizeof(ChunkMeta) * size_t(n_chunks));
     L.fb = align256(L.ckpts + sizeof(CkptMeta) * size_t(std::max<long long>(n_reqs, 1)));
-    L.rec = (L.fb + 32 + 2 * sizeof(uint32_t) * size_t(window) * size_t(H) + 1023) / 1024 * 1024;
+    L.solo = align256(L.fb + 32 + 2 * sizeof(uint32_t) * size_t(window) * size_t(H));
+    L.rec = (L.solo + size_t(N) * size_t(H) + 1023) / 1024 * 1024;
     L.total = L.rec + Rec::BYTES * size_t(L.ring_windows) * size_t(window) * size_t(H);
     return L;
 }
@@ -738,6 +764,7 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
     PrefillParams p = p0;
     p.ring_chunks = L.ring_windows * L.window;
     p.q_lo = kFast ? 0 : 1;  // exp(G) . q and P feed only the output: bf16 outputs keep their hi halves
+    if (!kFast) p.solo = nullptr;  // only the bf16 intra kernel finishes one-chunk sequences itself
     CUtensorMap mq, mk, mv, ma, mg, mo;
     std::memset(&mg, 0, sizeof(mg));  // fp32: the chain loads its gate values and stores its outputs itself
     std::memset(&mo, 0, sizeof(mo));
@@ -851,6 +878,7 @@ kda_status launch_tables(const kda_pool *pool, const kda_weights *w, const kda_i
     p.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.ckpts);
     p.fb_count = reinterpret_cast<uint32_t *>(ws + L.fb);  // [2]
     p.fb_list = p.fb_count + 8;                             // [2][window * H]
+    p.solo = reinterpret_cast<uint8_t *>(ws + L.solo);      // [N][H]
     p.rec = ws + L.rec;
     p.states = pool->states;
     p.tails = pool->tails;

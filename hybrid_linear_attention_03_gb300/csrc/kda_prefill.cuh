@@ -81,6 +81,8 @@ struct PrefillParams {
     const void *conv_w, *norm_w;
     uint32_t *fb_count;      // chunk-heads the fast intra kernel hands to the generic one ...
     uint32_t *fb_list;       // ... as g * H + h
+    uint8_t *solo;           // bf16: [n_seqs][H], 1 where the intra kernel finished a one-chunk
+                             // sequence from a zero state itself (the chain skips it), else 0
     int32_t H, n_ch, n_seqs, n_chunks, n_ckpts;
     int32_t ring_chunks;     // chunks the record ring holds
     int32_t chunk_base;      // intra, out: global index of blockIdx.x == 0

@@ -166,6 +166,145 @@ __device__ __forceinline__ void store_split(unsigned char *hi, unsigned char *lo
     *reinterpret_cast<uint4 *>(lo + off) = vl;
 }
 
+// The rest of a one-chunk sequence from a zero state, after the Ut^T product
+// (TMEM [128, 192)); K^ is on its way back from the record into KB (bar_qk,
+// phase 1), P's hi image is in the P staging, exp(G_last - c) in the G_0 slot.
+//   U = Ut: the U^T hi/lo image -> X;  the gate tile -> RA (rows of 256 B)
+//   O^T = U^T P^T (one product) -> TMEM [0, 64);  (K^^T U)^T = U^T K^ -> [64, 192)
+//   S^T = (K^^T U)^T diag(exp(G_last - c)) -> the slot (and checkpoint slots)
+//   out = w_n . O / sqrt(mean O^2 + eps) . sigmoid(gate), staged over the
+//   gate tile, then stored row by row (rows past the sequence untouched)
+struct SoloChunk {
+    int32_t seq, row0, len, ck_begin, ck_count, slot;
+};
+__device__ __noinline__ void solo_tail(const PrefillParams &p, unsigned char *sm, uint32_t sbase, uint32_t tm,
+                                       const SoloChunk cm, int h, bool ok) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, cs = (warp >> 2) * 16, j = qd * 32 + lane;  // TMEM lane = value channel j
+    uint64_t *bar_qk = reinterpret_cast<uint64_t *>(sm + fs::BARS) + 1;
+    uint64_t *bar_m1 = reinterpret_cast<uint64_t *>(sm + fs::BARS) + 3;
+    const float *elc = reinterpret_cast<const float *>(sm + fs::G0);
+    float *red = reinterpret_cast<float *>(sm + fs::SCAN);  // [4 lane quarters][64 tokens], then rs [64]
+    uint32_t *fail = reinterpret_cast<uint32_t *>(sm + fs::SCAN + 2048);
+    const size_t HD = size_t(p.H) * D;
+    // the gate tile: 64 rows x 256 bytes, two 16-byte pieces a thread, coalesced
+    uint4 gl[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int idx = tid + q * fs::NT, r = idx >> 4, c16 = idx & 15;
+        gl[q] = r < cm.len ? *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.gate) +
+                                                             (size_t(cm.row0 + r) * HD + size_t(h) * D) + c16 * 8)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tid == 0) *fail = 0u;
+    if (ok) {  // U^T row j, tokens cs .. cs + 15 -> the hi / lo image rows (K-major, K = token)
+        float u[16];
+        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + 128 + cs, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = u[8 * hh + e];
+            store_split(sm + fs::X, sm + fs::X + 16384, sw128_chunk(j, (cs >> 3) + hh, D), x);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int idx = tid + q * fs::NT;
+        *reinterpret_cast<uint4 *>(sm + fs::RA + (idx >> 4) * 256 + (idx & 15) * 16) = gl[q];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && ok) {
+        if (mbar_wait(bar_qk, 1, p.err)) {
+            const Operand u_img{sbase + fs::X, sbase + fs::X + 16384, false, D * 128};
+            const Operand pp_img{sbase + fs::PPS, sbase + fs::PPS + 8192, false, CH * 128};
+            const Operand kh_img{sbase + fs::KB, sbase + fs::KB_LO, true, CH * 128};
+            mma_split(tm, u_img, pp_img, CH, idesc_bf16_f32(128, CH), 1, false);
+            mma_split(tm + 64, u_img, kh_img, CH, idesc_bf16_f32(128, D, false, true), 3, false);
+            mma_commit(bar_m1);
+        } else {
+            *fail = 1u;
+        }
+    }
+    ok = __syncthreads_and(ok) && *fail == 0u;
+    ok = __syncthreads_and(ok && mbar_wait(bar_m1, 1, p.err));
+    tc_fence_after();
+    float o[16];
+    if (ok) {
+        // S^T row j, key channels 32 cb .. 32 cb + 31
+        const int cb = warp >> 2;
+        float sv[2][16];
+        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + 64 + 32 * cb, sv[0]);
+        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + 64 + 32 * cb + 16, sv[1]);
+        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cs, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[e >> 4][e & 15] *= elc[32 * cb + e];
+        const size_t head = size_t(D) * D, off = size_t(h) * head + size_t(j) * D + 32 * cb;
+        float *dst = p.states + size_t(cm.slot) * p.H * head + off;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4 *>(dst + e) =
+                make_float4(sv[e >> 4][e & 15], sv[e >> 4][(e & 15) + 1], sv[e >> 4][(e & 15) + 2], sv[e >> 4][(e & 15) + 3]);
+        for (int k = 0; k < cm.ck_count; ++k) {  // checkpoints at this chunk's end
+            float *cd = p.states + size_t(p.ckpts[cm.ck_begin + k].dst_slot) * p.H * head + off;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4 *>(cd + e) =
+                    make_float4(sv[e >> 4][e & 15], sv[e >> 4][(e & 15) + 1], sv[e >> 4][(e & 15) + 2], sv[e >> 4][(e & 15) + 3]);
+        }
+        // per token, the sum of O^2 over the warp's 32 channels: add the lane
+        // pairs l, l ^ 16, then a transpose-reduce over 16 lanes leaves token
+        // cs + (lane mod 16)'s in lane
+        float a[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            a[e] = o[e] * o[e];
+            a[e] += __shfl_xor_sync(0xffffffffu, a[e], 16);
+        }
+#pragma unroll
+        for (int wd = 8; wd >= 1; wd >>= 1) {
+            const bool up = (lane & wd) != 0;
+#pragma unroll
+            for (int e = 0; e < wd; ++e) {
+                const float send = up ? a[e] : a[e + wd];
+                const float keep = up ? a[e + wd] : a[e];
+                a[e] = keep + __shfl_xor_sync(0xffffffffu, send, wd);
+            }
+        }
+        if (lane < 16) red[qd * CH + cs + lane] = a[0];
+    }
+    __syncthreads();
+    if (ok && tid < CH)
+        red[4 * CH + tid] = rsqrtf(((red[tid] + red[CH + tid]) + (red[2 * CH + tid] + red[3 * CH + tid])) * (1.0f / D) +
+                                   p.eps_rms);
+    __syncthreads();
+    if (ok) {  // y over the gate tile, in place (one thread per (token, channel))
+        const float wn = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.norm_w)[j]);
+        uint16_t *gs = reinterpret_cast<uint16_t *>(sm + fs::RA) + j;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int r = cs + e;
+            const float gv = __uint_as_float(uint32_t(gs[r * D]) << 16);
+            gs[r * D] = __bfloat16_as_ushort(__float2bfloat16_rn(wn * (o[e] * red[4 * CH + r]) * sigmoid_tanh(gv)));
+        }
+    }
+    __syncthreads();
+    if (ok) {  // rows of the output, a warp per row, 8 bytes a lane
+        for (int r = warp; r < cm.len; r += fs::NT / 32)
+            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.out) + (size_t(cm.row0 + r) * HD + size_t(h) * D) +
+                                       lane * 4) = *reinterpret_cast<const uint2 *>(sm + fs::RA + r * 256 + lane * 8);
+    }
+    if (tid == 0) p.solo[size_t(cm.seq) * p.H + h] = ok ? 1 : 0;
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
 __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const PrefillParams p,
                                                                     const __grid_constant__ CUtensorMap tm_q,
                                                                     const __grid_constant__ CUtensorMap tm_k,
@@ -193,6 +332,9 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     if (cm.len <= 0) return;  // a padding entry of a device-built table: no chunk here
     const SeqMeta sq = p.seqs[cm.seq];
     char *rec = rec_ptr(p, g, h);
+    // a one-chunk sequence from a zero state: U = Ut, so this CTA also forms
+    // O = P U and the end state itself and the chain skips the sequence
+    const bool solo = p.solo && sq.n_chunks == 1 && !sq.has_init;
     const uint32_t sbase = smem_u32(sm);
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(bar_a_ld + b, 1);
@@ -272,13 +414,16 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         cref[tid] = c;
         ec[tid] = expf(c);
         at<float>(rec, Rec::GAM)[tid] = expf(run);
-        at<float>(rec, Rec::ELC)[tid] = expf(run - c);
+        const float elc = expf(run - c);
+        at<float>(rec, Rec::ELC)[tid] = elc;
+        if (solo) g0s[tid] = elc;  // kept for the end state (G_0 is read above)
         wide = gfirst - run > kSafeSpanFast;
     }
     const bool exact = __syncthreads_or(wide) != 0;
     if (!ok || exact) {
         // a chunk this kernel cannot take: the generic kernel's list gets it
         if (ok && tid == 0) p.fb_list[atomicAdd(p.fb_count, 1u)] = uint32_t(g) * uint32_t(p.H) + uint32_t(h);
+        if (solo && tid == 0) p.solo[size_t(cm.seq) * p.H + h] = 0;  // the chain takes it
         mbar_wait(bar_qk, 0, p.err);  // no copy may land after the CTA is gone
         mbar_wait(bar_v, 0, p.err);
         tc_fence_before();
@@ -333,7 +478,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] *= e_c[e];
             split8(x, vh, vl);
-            *reinterpret_cast<uint4 *>(rec + Rec::WQ_HI + sw128_chunk(CH + r0 + q, cb, 2 * CH)) = vh;
+            if (!solo) *reinterpret_cast<uint4 *>(rec + Rec::WQ_HI + sw128_chunk(CH + r0 + q, cb, 2 * CH)) = vh;
         }
     }
     fence_proxy_async_smem();
@@ -399,7 +544,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && ok) {
+    if (tid == 0 && ok && !solo) {
         bulk_store(rec + Rec::PP_HI, sm + fs::PPS, 8192);
         bulk_commit();
     }
@@ -486,12 +631,21 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         const Operand tba{sbase + fs::TB, sbase + fs::TB_LO, true, CH * 128};
         const Operand kt{sbase + fs::X, sbase + fs::X_LO, true, 2 * CH * 128};
         const Operand vt{sbase + fs::VIMG, sbase + fs::VIMG_LO, true, CH * 128};
-        mma_split(tm, tba, kt, CH, idesc_bf16_f32(128, D, true, true), 3, false);
+        if (!solo) mma_split(tm, tba, kt, CH, idesc_bf16_f32(128, D, true, true), 3, false);
         mma_split(tm + 128, vt, tba, CH, idesc_bf16_f32(128, CH, true, true), 3, false);
         mma_commit(bar_m2);
+        if (solo) {  // K^ back from the record into KB (A^T and T^T are done with)
+            bulk_wait();
+            mbar_arrive_expect_tx(bar_qk, 32768);
+            bulk_load(sm + fs::KB, rec + Rec::KH_HI, 32768, bar_qk);
+        }
     }
     ok = __syncthreads_and(ok && mbar_wait(bar_m2, 0, p.err));
     tc_fence_after();
+    if (solo) {
+        solo_tail(p, sm, sbase, tm, SoloChunk{cm.seq, cm.row0, cm.len, cm.ck_begin, cm.ck_count, sq.slot}, h, ok);
+        return;
+    }
     if (ok) {
         // ---- W row r (times exp(c_i)) and Ut^T row j -> staging in X ----------
         const int i = qd * 32 + lane;
