@@ -755,7 +755,7 @@ struct SeqRange {
 
 template <typename Act>
 kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int N, long long n_chunks, int n_reqs,
-                      const WsLayout &L, const std::vector<SeqRange> *ranges, cudaStream_t stream) {
+                      const WsLayout &L, const std::vector<SeqRange> *ranges, bool solo, cudaStream_t stream) {
     constexpr bool kFast = sizeof(Act) == 2;
     kda_status st;
     if ((st = kFast ? intra_fast_prepare() : KDA_OK) != KDA_OK) return st;
@@ -764,7 +764,9 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
     PrefillParams p = p0;
     p.ring_chunks = L.ring_windows * L.window;
     p.q_lo = kFast ? 0 : 1;  // exp(G) . q and P feed only the output: bf16 outputs keep their hi halves
-    if (!kFast) p.solo = nullptr;  // only the bf16 intra kernel finishes one-chunk sequences itself
+    // only the bf16 intra kernel finishes one-chunk sequences itself, and
+    // only its variant for calls that may have them
+    if (!kFast || !solo) p.solo = nullptr;
     CUtensorMap mq, mk, mv, ma, mg, mo;
     std::memset(&mg, 0, sizeof(mg));  // fp32: the chain loads its gate values and stores its outputs itself
     std::memset(&mo, 0, sizeof(mo));
@@ -864,10 +866,11 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
 
 // Launch parameters over the workspace's tables (written, or enqueued to be
 // written, on the stream) and the kernels.  n_chunks sizes the grids; n_tok
-// is the token extent of the activation arrays the tensor maps describe.
+// is the token extent of the activation arrays the tensor maps describe;
+// solo picks the intra variant that finishes one-chunk sequences itself.
 kda_status launch_tables(const kda_pool *pool, const kda_weights *w, const kda_io *io, char *ws, const WsLayout &L,
                          int N, int n_reqs, long long n_chunks, int n_tok, const std::vector<SeqRange> *ranges,
-                         cudaStream_t stream) {
+                         bool solo, cudaStream_t stream) {
     PrefillParams p{};
     p.chunk_base = 0;
     p.win_lo = 0;
@@ -900,8 +903,8 @@ kda_status launch_tables(const kda_pool *pool, const kda_weights *w, const kda_i
     p.eps_l2 = w->eps_l2;
     p.eps_rms = w->eps_rms;
     if (pool->desc.act == KDA_BF16)
-        return launch_act<__nv_bfloat16>(p, io, n_tok, N, n_chunks, n_reqs, L, ranges, stream);
-    return launch_act<float>(p, io, n_tok, N, n_chunks, n_reqs, L, ranges, stream);
+        return launch_act<__nv_bfloat16>(p, io, n_tok, N, n_chunks, n_reqs, L, ranges, solo, stream);
+    return launch_act<float>(p, io, n_tok, N, n_chunks, n_reqs, L, ranges, solo, stream);
 }
 
 }  // namespace
@@ -981,7 +984,10 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
                                             cudaMemcpyHostToDevice, stream) != cudaSuccess)
             return KDA_ERR_CUDA;
     }
-    return launch_tables(pool, w, io, ws, L, N, n_reqs, n_chunks, cu_seqlens[N], &ranges, stream);
+    // the intra variant that finishes one-chunk sequences pays only where two or more are here
+    int n_solo = 0;
+    for (int s = 0; s < N; ++s) n_solo += (seqs[s].n_chunks == 1 && !seqs[s].has_init) ? 1 : 0;
+    return launch_tables(pool, w, io, ws, L, N, n_reqs, n_chunks, cu_seqlens[N], &ranges, n_solo >= 2, stream);
 }
 
 size_t prefill_workspace_bytes_bound(const kda_pool *pool, int N, int max_tokens, int n_reqs, int chunk) {
@@ -1026,7 +1032,7 @@ kda_status launch_prefill_dev(const kda_pool *pool, const kda_weights *w, const 
         const ProfScope prof(KDA_KERNEL_PREFILL_META, stream);
         prefill_meta_kernel<<<1, kMetaThreads, 0, stream>>>(a);
     }
-    return launch_tables(pool, w, io, ws, LD.L, N, n_reqs, max_chunks, max_tokens, nullptr, stream);
+    return launch_tables(pool, w, io, ws, LD.L, N, n_reqs, max_chunks, max_tokens, nullptr, N >= 2, stream);
 }
 
 // ------------------------------------------------------ no-allocation entry --

@@ -177,7 +177,7 @@ __device__ __forceinline__ void store_split(unsigned char *hi, unsigned char *lo
 struct SoloChunk {
     int32_t seq, row0, len, ck_begin, ck_count, slot;
 };
-__device__ __noinline__ void solo_tail(const PrefillParams &p, unsigned char *sm, uint32_t sbase, uint32_t tm,
+__device__ __forceinline__ void solo_tail(const PrefillParams &p, unsigned char *sm, uint32_t sbase, uint32_t tm,
                                        const SoloChunk cm, int h, bool ok) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qd = warp & 3, cs = (warp >> 2) * 16, j = qd * 32 + lane;  // TMEM lane = value channel j
@@ -305,6 +305,10 @@ __device__ __noinline__ void solo_tail(const PrefillParams &p, unsigned char *sm
     if (warp == 0) tmem_dealloc(tm, 256);
 }
 
+// kSolo: the variant that also finishes one-chunk sequences from a zero
+// state (p.solo set); the other has no such path (its code would slow the
+// main path by about 2 %) and is launched for calls without them.
+template <bool kSolo>
 __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const PrefillParams p,
                                                                     const __grid_constant__ CUtensorMap tm_q,
                                                                     const __grid_constant__ CUtensorMap tm_k,
@@ -334,7 +338,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     char *rec = rec_ptr(p, g, h);
     // a one-chunk sequence from a zero state: U = Ut, so this CTA also forms
     // O = P U and the end state itself and the chain skips the sequence
-    const bool solo = p.solo && sq.n_chunks == 1 && !sq.has_init;
+    const bool solo = kSolo && sq.n_chunks == 1 && !sq.has_init;
     const uint32_t sbase = smem_u32(sm);
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(bar_a_ld + b, 1);
@@ -416,14 +420,14 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         at<float>(rec, Rec::GAM)[tid] = expf(run);
         const float elc = expf(run - c);
         at<float>(rec, Rec::ELC)[tid] = elc;
-        if (solo) g0s[tid] = elc;  // kept for the end state (G_0 is read above)
+        g0s[tid] = elc;  // kept for a one-chunk sequence's end state (G_0 is read above)
         wide = gfirst - run > kSafeSpanFast;
     }
     const bool exact = __syncthreads_or(wide) != 0;
     if (!ok || exact) {
         // a chunk this kernel cannot take: the generic kernel's list gets it
         if (ok && tid == 0) p.fb_list[atomicAdd(p.fb_count, 1u)] = uint32_t(g) * uint32_t(p.H) + uint32_t(h);
-        if (solo && tid == 0) p.solo[size_t(cm.seq) * p.H + h] = 0;  // the chain takes it
+        if (kSolo && solo && tid == 0) p.solo[size_t(cm.seq) * p.H + h] = 0;  // the chain takes it
         mbar_wait(bar_qk, 0, p.err);  // no copy may land after the CTA is gone
         mbar_wait(bar_v, 0, p.err);
         tc_fence_before();
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] *= e_c[e];
             split8(x, vh, vl);
-            if (!solo) *reinterpret_cast<uint4 *>(rec + Rec::WQ_HI + sw128_chunk(CH + r0 + q, cb, 2 * CH)) = vh;
+            *reinterpret_cast<uint4 *>(rec + Rec::WQ_HI + sw128_chunk(CH + r0 + q, cb, 2 * CH)) = vh;
         }
     }
     fence_proxy_async_smem();
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && ok && !solo) {
+    if (tid == 0 && ok) {
         bulk_store(rec + Rec::PP_HI, sm + fs::PPS, 8192);
         bulk_commit();
     }
@@ -631,7 +635,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         const Operand tba{sbase + fs::TB, sbase + fs::TB_LO, true, CH * 128};
         const Operand kt{sbase + fs::X, sbase + fs::X_LO, true, 2 * CH * 128};
         const Operand vt{sbase + fs::VIMG, sbase + fs::VIMG_LO, true, CH * 128};
-        if (!solo) mma_split(tm, tba, kt, CH, idesc_bf16_f32(128, D, true, true), 3, false);
+        mma_split(tm, tba, kt, CH, idesc_bf16_f32(128, D, true, true), 3, false);
         mma_split(tm + 128, vt, tba, CH, idesc_bf16_f32(128, CH, true, true), 3, false);
         mma_commit(bar_m2);
         if (solo) {  // K^ back from the record into KB (A^T and T^T are done with)
@@ -642,7 +646,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     }
     ok = __syncthreads_and(ok && mbar_wait(bar_m2, 0, p.err));
     tc_fence_after();
-    if (solo) {
+    if (kSolo && solo) {
         solo_tail(p, sm, sbase, tm, SoloChunk{cm.seq, cm.row0, cm.len, cm.ck_begin, cm.ck_count, sq.slot}, h, ok);
         return;
     }
@@ -692,8 +696,11 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
 }  // namespace
 
 kda_status intra_fast_prepare() {
-    return cudaFuncSetAttribute(prefill_intra_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                int(1024 + fs::BYTES)) == cudaSuccess
+    const int bytes = int(1024 + fs::BYTES);
+    return cudaFuncSetAttribute(prefill_intra_fast_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+                       cudaSuccess &&
+                   cudaFuncSetAttribute(prefill_intra_fast_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        bytes) == cudaSuccess
                ? KDA_OK
                : KDA_ERR_CUDA;
 }
@@ -701,7 +708,10 @@ kda_status intra_fast_prepare() {
 kda_status launch_intra_fast(const PrefillParams &p, const CUtensorMap &mq, const CUtensorMap &mk,
                              const CUtensorMap &mv, const CUtensorMap &ma, dim3 grid, cudaStream_t s) {
     const ProfScope prof(KDA_KERNEL_PREFILL_INTRA, s);
-    prefill_intra_fast_kernel<<<grid, fs::NT, 1024 + fs::BYTES, s>>>(p, mq, mk, mv, ma);
+    if (p.solo)
+        prefill_intra_fast_kernel<true><<<grid, fs::NT, 1024 + fs::BYTES, s>>>(p, mq, mk, mv, ma);
+    else
+        prefill_intra_fast_kernel<false><<<grid, fs::NT, 1024 + fs::BYTES, s>>>(p, mq, mk, mv, ma);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
