@@ -647,7 +647,8 @@ def _event_us(stream, fn, iters):
 def next_rows_case(kda, dev, iters=20):
     """The widened rows, each measured: (1) prefill with device-built
     metadata in a CUDA graph against the host-built tables, for 1 and 64
-    short sequences; (2) the prefix cache: host planning time for a 32K-token
+    short sequences continuing their slots, and the same calls for new
+    sequences (zero state); (2) the prefix cache: host planning time for a 32K-token
     prompt, and the GPU time of resuming from a saved prefix (slot copy plus
     the 64-token tail) against prefilling the whole prompt; (3) one slot's
     state export / import through pinned host memory."""
@@ -687,6 +688,11 @@ def next_rows_case(kda, dev, iters=20):
                 graph.replay()
 
         dev_us = _event_us(stream, replay, iters)
+        # the same sequences started from a zero state: each is one chunk, which
+        # the intra kernel finishes itself (the chain skips them)
+        no_init = [0] * N
+        new_us = _event_us(stream, lambda: kda.kda_prefill_chunked(pool, w, io, cu, slots, no_init, 64, (), ws_h, stream),
+                           iters)
         # the metadata alone: the device builder kernel, against the host call's
         # table build (host wall time of the call, launches included) and the
         # device time of its tables' copies; library event profile
@@ -703,6 +709,7 @@ def next_rows_case(kda, dev, iters=20):
         stream.synchronize()
         meta[f"n{N}_x64_tokens"] = {
             "host_tables_us": round(host_us, 2), "device_tables_graph_us": round(dev_us, 2),
+            "host_tables_new_sequences_us": round(new_us, 2),
             "meta_kernel_us": round(prof_dev["prefill_meta"][1] * 1e3 / max(prof_dev["prefill_meta"][0], 1), 2),
             "host_tables_copy_us": round(prof_host["prefill_meta"][1] * 1e3 / max(prof_host["prefill_meta"][0], 1),
                                          2),

@@ -973,21 +973,24 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
     }
     char *ws = static_cast<char *>(workspace);
     {
-        const ProfScope prof(KDA_KERNEL_PREFILL_META, stream);  // the host tables' copies to the device
-        if (N > 0 && cudaMemcpyAsync(ws + L.seqs, seqs.data(), sizeof(SeqMeta) * seqs.size(),
-                                     cudaMemcpyHostToDevice, stream) != cudaSuccess)
-            return KDA_ERR_CUDA;
-        if (!chunks.empty() && cudaMemcpyAsync(ws + L.chunks, chunks.data(), sizeof(ChunkMeta) * chunks.size(),
-                                               cudaMemcpyHostToDevice, stream) != cudaSuccess)
-            return KDA_ERR_CUDA;
-        if (!cks.empty() && cudaMemcpyAsync(ws + L.ckpts, cks.data(), sizeof(CkptMeta) * cks.size(),
-                                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        // the three tables laid out as in the workspace, then one copy
+        const size_t end = cks.empty() ? L.chunks + sizeof(ChunkMeta) * chunks.size()
+                                       : L.ckpts + sizeof(CkptMeta) * cks.size();
+        std::vector<char> host(end, 0);
+        if (N > 0) std::memcpy(host.data() + L.seqs, seqs.data(), sizeof(SeqMeta) * seqs.size());
+        if (!chunks.empty()) std::memcpy(host.data() + L.chunks, chunks.data(), sizeof(ChunkMeta) * chunks.size());
+        if (!cks.empty()) std::memcpy(host.data() + L.ckpts, cks.data(), sizeof(CkptMeta) * cks.size());
+        const ProfScope prof(KDA_KERNEL_PREFILL_META, stream);  // the host tables' copy to the device
+        if (end > 0 && cudaMemcpyAsync(ws, host.data(), end, cudaMemcpyHostToDevice, stream) != cudaSuccess)
             return KDA_ERR_CUDA;
     }
-    // the intra variant that finishes one-chunk sequences pays only where two or more are here
-    int n_solo = 0;
+    // the intra variant that finishes one-chunk sequences itself: where they
+    // are at least a sixteenth of the chunks (elsewhere its path costs more
+    // than the chain steps it saves)
+    long long n_solo = 0;
     for (int s = 0; s < N; ++s) n_solo += (seqs[s].n_chunks == 1 && !seqs[s].has_init) ? 1 : 0;
-    return launch_tables(pool, w, io, ws, L, N, n_reqs, n_chunks, cu_seqlens[N], &ranges, n_solo >= 2, stream);
+    const bool solo = n_solo > 0 && 16 * n_solo >= n_chunks;
+    return launch_tables(pool, w, io, ws, L, N, n_reqs, n_chunks, cu_seqlens[N], &ranges, solo, stream);
 }
 
 size_t prefill_workspace_bytes_bound(const kda_pool *pool, int N, int max_tokens, int n_reqs, int chunk) {
@@ -1032,7 +1035,9 @@ kda_status launch_prefill_dev(const kda_pool *pool, const kda_weights *w, const 
         const ProfScope prof(KDA_KERNEL_PREFILL_META, stream);
         prefill_meta_kernel<<<1, kMetaThreads, 0, stream>>>(a);
     }
-    return launch_tables(pool, w, io, ws, LD.L, N, n_reqs, max_chunks, max_tokens, nullptr, N >= 2, stream);
+    // device tables: the one-chunk variant when sequences may average 16 chunks or fewer
+    return launch_tables(pool, w, io, ws, LD.L, N, n_reqs, max_chunks, max_tokens, nullptr,
+                         N > 0 && 16LL * N >= max_chunks, stream);
 }
 
 // ------------------------------------------------------ no-allocation entry --
