@@ -590,8 +590,9 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         {
             const int i = lane, j0 = 2 * warp;
             float x0 = 0.f, x1 = 0.f;
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
+            // T_11 is lower triangular: T_k,j0 and T_k,j0+1 vanish for k < j0
+#pragma unroll 4
+            for (int k = j0; k < 32; ++k) {
                 const float av = At[k * CH + 32 + i];
                 x0 = fmaf(av, Tt[j0 * CH + k], x0);
                 x1 = fmaf(av, Tt[(j0 + 1) * CH + k], x1);
@@ -650,24 +651,9 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         solo_tail(p, sm, sbase, tm, SoloChunk{cm.seq, cm.row0, cm.len, cm.ck_begin, cm.ck_count, sq.slot}, h, ok);
         return;
     }
+    // ---- Ut^T row i -> staging in X_LO, on its way out while W is drained --
     if (ok) {
-        // ---- W row r (times exp(c_i)) and Ut^T row j -> staging in X ----------
         const int i = qd * 32 + lane;
-        if (qd < 2) {  // W: TMEM lanes 0..63 = token r, 32 of the 128 key channels per warp
-            const int r = i, cw = (warp >> 2) * 32;
-            float w[2][16];
-            tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw, w[0]);
-            tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw + 16, w[1]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                float x[8], e_c[8];
-                ld8(ec + cw + 8 * hh, e_c);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = w[hh >> 1][8 * (hh & 1) + e] * e_c[e];
-                store_split(sm + fs::X, sm + fs::X + 16384, sw128_chunk(r, (cw >> 3) + hh, CH), x);
-            }
-        }
         float u[16];
         tmem_ld16(tm + (uint32_t(qd * 32) << 16) + 128 + cs, u);
         tmem_wait_ld();
@@ -680,13 +666,36 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && ok) {
+        bulk_store(rec + Rec::UT, sm + fs::X_LO, 32768);
+        bulk_commit();
+    }
+    // ---- W row r (times exp(c_i)) -> staging in X ---------------------------
+    if (ok && qd < 2) {  // W: TMEM lanes 0..63 = token r, 32 of the 128 key channels per warp
+        const int r = qd * 32 + lane, cw = (warp >> 2) * 32;
+        float w[2][16];
+        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw, w[0]);
+        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw + 16, w[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+            float x[8], e_c[8];
+            ld8(ec + cw + 8 * hh, e_c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = w[hh >> 1][8 * (hh & 1) + e] * e_c[e];
+            store_split(sm + fs::X, sm + fs::X + 16384, sw128_chunk(r, (cw >> 3) + hh, CH), x);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
     if (tid == 0 && ok) {
         // W rows 0..63 of each 64-wide K block of the WQ images
         bulk_store(rec + Rec::WQ_HI, sm + fs::X, 8192);
         bulk_store(rec + Rec::WQ_HI + 16384, sm + fs::X + 8192, 8192);
         bulk_store(rec + Rec::WQ_LO, sm + fs::X + 16384, 8192);
         bulk_store(rec + Rec::WQ_LO + 16384, sm + fs::X + 24576, 8192);
-        bulk_store(rec + Rec::UT, sm + fs::X_LO, 32768);
         bulk_commit();
         bulk_wait_read();  // shared memory stays until the copies have read it
     }
