@@ -206,3 +206,35 @@ def test_stream_wait_reports_a_timeout_then_completion():
     assert kda.kda_stream_wait(stream, 0.0) == kda.KDA_ERR_TIMEOUT
     assert kda.kda_stream_wait(stream, 120.0) == kda.KDA_OK
     assert kda.kda_poll_device_error(m.gpu, stream) == (kda.KDA_OK, 0)
+
+
+def test_one_chunk_sequences_from_zero_state_match_oracle():
+    """One-chunk sequences that start from a zero state are finished inside
+    the intra-chunk kernel when they make up a large share of a call (the
+    chain skips them), and by the chain otherwise.  Both batches, with a
+    checkpoint at a short sequence's end and a resumed short sequence among
+    them, match the oracle."""
+    H, act = 2, torch.bfloat16
+    m = Mirror(48, H, D, act, I.layer_weights(41, H, D, D, 4, act))
+    # many short sequences: the intra kernel finishes the new ones itself
+    lens = [64, 17, 1, 64, 40, 63, 5, 64, 33, 2]
+    N = len(lens)
+    slots = list(range(N))
+    has_init = [0] * N
+    has_init[4] = 1  # a short continuation still goes through the chain
+    warm = I.token_inputs(41, 0, 24, H, D, D, 2.0, act)
+    prefill_gpu(m, hp.to_device(warm), [24], [4], [0])
+    prefill_oracle(m, warm, [24], [4], [0])
+    reqs = [(1, 17, 30), (7, 64, 31)]
+    inp = I.token_inputs(41, 1, sum(lens), H, D, D, 2.0, act)
+    out = prefill_gpu(m, hp.to_device(inp), lens, slots, has_init, reqs)
+    ref = prefill_oracle(m, inp, lens, slots, has_init, reqs)
+    _check(m, out, ref, slots, reqs)
+    # one short sequence beside a long one: the chain takes both
+    lens2 = [50, 2000]
+    slots2 = [20, 21]
+    inp2 = I.token_inputs(41, 2, sum(lens2), H, D, D, 2.0, act)
+    out2 = prefill_gpu(m, hp.to_device(inp2), lens2, slots2, [0, 0], [(0, 50, 32)])
+    ref2 = prefill_oracle(m, inp2, lens2, slots2, [0, 0], [(0, 50, 32)])
+    _check(m, out2, ref2, slots2, [(0, 50, 32)])
+    assert kda.kda_poll_device_error(m.gpu) == (kda.KDA_OK, 0)
