@@ -25,7 +25,7 @@
 //   TMA alpha, then q, k, then v | beta, ln table
 //   G, E (registers) bar scan bar
 //   k pass: K~, K^ images    q pass: Q~ image, exp(G) . q rows -> record   bar
-//   warp 0: K^ image -> record (bulk), MMA [A; P] | warps 1-15: v image
+//   warp 0: K^ image -> record (bulk), MMA [A; P]; all warps: v image
 //   wait: A^T -> smem, P -> staging, T^T zeroed                         bar
 //   diagonal 16 x 16 blocks of T (2 warps)                               bar
 //   2 levels of off-diagonal blocks (32-blocks, 2 bar each); (T diag beta)^T image  bar
@@ -504,16 +504,17 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         }
         __syncwarp();
     }
-    // ---- v pass (under the MMAs, warps 1..15): v image over the raw q, k tiles
+    // ---- v pass under the MMAs: v image over the raw q, k tiles, one unit
+    // (2 tokens x 8 channels) a thread; warp 0 takes its units once its lane
+    // 0 has issued the MMAs (a second round for 32 units on the other warps
+    // cost more than that wait)
     bool okv = mbar_wait(bar_v, 0, p.err);
-    if (okv && warp != 0) {
-        for (int u = tid - 32; u < 512; u += 480) {  // warp 1 also takes units 480..511
-            const int vpr = u >> 4, vcb = u & 15;
-            float y[2][8];
-            conv_pair(sm + fs::RV, p, 2, h, 8 * vcb, 2 * vpr, cm.pos0, cm.len, tail, y);
+    if (okv) {
+        const int vpr = tid >> 4, vcb = tid & 15;
+        float y[2][8];
+        conv_pair(sm + fs::RV, p, 2, h, 8 * vcb, 2 * vpr, cm.pos0, cm.len, tail, y);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) store_split(sm + fs::VIMG, sm + fs::VIMG_LO, sw128_chunk(2 * vpr + q, vcb, CH), y[q]);
-        }
+        for (int q = 0; q < 2; ++q) store_split(sm + fs::VIMG, sm + fs::VIMG_LO, sw128_chunk(2 * vpr + q, vcb, CH), y[q]);
     }
     okv = okv && mbar_wait(bar_m1, 0, p.err);
     if (tid == 0) bulk_wait_read();  // KB becomes A^T and T^T below
