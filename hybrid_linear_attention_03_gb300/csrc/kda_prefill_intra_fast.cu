@@ -22,7 +22,7 @@
 // images leave through shared-memory staging and TMA bulk stores.
 //
 // Phases (bar = CTA barrier):
-//   TMA alpha, then q, k, then v | beta, ln table
+//   TMA alpha, then q, k, then v | beta
 //   G, E (registers) bar scan bar
 //   k pass: K~, K^ images    q pass: Q~ image, exp(G) . q rows -> record   bar
 //   warp 0: K^ image -> record (bulk), MMA [A; P]; all warps: v image
@@ -42,7 +42,7 @@
 //                   the last MMA, the W and Ut^T staging
 //   KB              K^ image hi / lo [64][128]; after MMA 1, A^T and T^T fp32 [64][64]
 //   SCAN            warp totals of G; later the level products
-//   SMALL           ln table, c, exp(c), G_0, beta, mbarriers
+//   SMALL           c, exp(c), G_0, beta, mbarriers
 // Tensor memory (256 columns): [0, 64) [A; P], then [0, 128) W (lanes 0..63);
 // [128, 192) Ut^T.
 #include "kda_prefill.cuh"
@@ -62,7 +62,7 @@ constexpr uint32_t AT = KB, TT = KB + 16384;
 constexpr uint32_t TB = X + 8192, TB_LO = X_LO + 8192;
 constexpr uint32_t SCAN = KB + 32768;
 constexpr uint32_t SMALL = SCAN + 8192;
-constexpr uint32_t LNM = SMALL, CREF = SMALL + 512, EC = SMALL + 1024, G0 = SMALL + 1536, BETA = SMALL + 2048;
+constexpr uint32_t CREF = SMALL + 512, EC = SMALL + 1024, G0 = SMALL + 1536, BETA = SMALL + 2048;  // [SMALL, +512) free
 constexpr uint32_t BARS = SMALL + 2304, TBASE = BARS + 64;
 constexpr uint32_t PPS = RV;            // P image staging (hi, lo at +8192) once the v pass has consumed raw v
 constexpr uint32_t BYTES = SMALL + 2560;
@@ -82,9 +82,11 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&x)[8]) {
     x[4] = bf_lo(u.z); x[5] = bf_hi(u.z); x[6] = bf_lo(u.w); x[7] = bf_hi(u.w);
 }
 
-// ln(alpha) of 8 packed bf16 values, the generic kernel's log_alpha8 on a
-// 16-byte register word (no trip through local memory).
-__device__ __forceinline__ void log_alpha8_u4(const uint4 u, const float *lnm, int n_valid, float (&l)[8]) {
+// ln(alpha) of 8 packed bf16 values in a 16-byte register word: PTX's
+// lg2.approx (absolute error about 2^-22 in log2) times ln 2 while the warp's
+// valid values are all positive normals, else logf.  Over a chunk the decay
+// sums 64 of these, so the error stays near 1e-5 in the exponent.
+__device__ __forceinline__ void log_alpha8_u4(const uint4 u, int n_valid, float (&l)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     bool normal = true;
 #pragma unroll
@@ -96,7 +98,9 @@ __device__ __forceinline__ void log_alpha8_u4(const uint4 u, const float *lnm, i
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const uint32_t b = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-            l[e] = fmaf(float(int((b >> 7) & 0xFFu) - 127), 0.6931471805599453f, lnm[b & 0x7Fu]);
+            float lg;
+            asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(__uint_as_float(b << 16)));
+            l[e] = lg * 0.6931471805599453f;
         }
     } else {
 #pragma unroll
@@ -317,7 +321,6 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1 KiB-aligned base, kept a shared-memory pointer (offset, not an integer round trip)
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    float *lnm = reinterpret_cast<float *>(sm + fs::LNM);
     float *cref = reinterpret_cast<float *>(sm + fs::CREF);
     float *ec = reinterpret_cast<float *>(sm + fs::EC);
     float *g0s = reinterpret_cast<float *>(sm + fs::G0);
@@ -356,7 +359,6 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     const float beta_ld = tid < CH && tid < cm.len
                               ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[size_t(cm.row0 + tid) * p.H + h])
                               : 0.f;
-    if (tid < 128) lnm[tid] = logf(1.0f + float(tid) * (1.0f / 128.0f));  // ln of the bf16 mantissas 1 + m/128
     if (warp == 0) tmem_alloc(tbase, 256);
     tc_fence_before();
     __syncthreads();
@@ -375,8 +377,8 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     {
         const uint4 a0 = lds16(sm + fs::RA + r0 * (D * 2) + ch0 * 2), a1 = lds16(sm + fs::RA + (r0 + 1) * (D * 2) + ch0 * 2);
         float l0[8], l1[8];
-        log_alpha8_u4(a0, lnm, r0 < cm.len ? 8 : 0, l0);
-        log_alpha8_u4(a1, lnm, r0 + 1 < cm.len ? 8 : 0, l1);
+        log_alpha8_u4(a0, r0 < cm.len ? 8 : 0, l0);
+        log_alpha8_u4(a1, r0 + 1 < cm.len ? 8 : 0, l1);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             l0[e] = r0 < cm.len ? fmaxf(l0[e], kLogAlphaMin) : 0.f;
