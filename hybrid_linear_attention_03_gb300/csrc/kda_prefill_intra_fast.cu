@@ -574,18 +574,32 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     }
     __syncthreads();
     if (ok) {
+        // The level products are bound by shared-memory wavefronts: the operand
+        // shared by a warp's lanes comes 4 k at a time as one 16-byte load.
         // ---- level 1: T_ab = -T_aa A_ab T_bb for (a, b) = (1, 0), (3, 2) ------
         {
             const int blk = tid >> 8, j = (tid >> 4) & 15, i = tid & 15;
             const int a16 = 16 * (2 * blk + 1), b16 = a16 - 16;
             float acc = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) acc = fmaf(At[(b16 + k) * CH + a16 + i], Tt[(b16 + j) * CH + b16 + k], acc);
+            for (int k = 0; k < 16; k += 4) {
+                const float4 tq = *reinterpret_cast<const float4 *>(Tt + (b16 + j) * CH + b16 + k);
+                acc = fmaf(At[(b16 + k) * CH + a16 + i], tq.x, acc);
+                acc = fmaf(At[(b16 + k + 1) * CH + a16 + i], tq.y, acc);
+                acc = fmaf(At[(b16 + k + 2) * CH + a16 + i], tq.z, acc);
+                acc = fmaf(At[(b16 + k + 3) * CH + a16 + i], tq.w, acc);
+            }
             XS[blk * 256 + j * 16 + i] = acc;
             __syncthreads();
             float t = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) t = fmaf(Tt[(a16 + k) * CH + a16 + i], XS[blk * 256 + j * 16 + k], t);
+            for (int k = 0; k < 16; k += 4) {
+                const float4 xq = *reinterpret_cast<const float4 *>(XS + blk * 256 + j * 16 + k);
+                t = fmaf(Tt[(a16 + k) * CH + a16 + i], xq.x, t);
+                t = fmaf(Tt[(a16 + k + 1) * CH + a16 + i], xq.y, t);
+                t = fmaf(Tt[(a16 + k + 2) * CH + a16 + i], xq.z, t);
+                t = fmaf(Tt[(a16 + k + 3) * CH + a16 + i], xq.w, t);
+            }
             Tt[(b16 + j) * CH + a16 + i] = -t;
         }
         __syncthreads();
@@ -594,21 +608,31 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
             const int i = lane, j0 = 2 * warp;
             float x0 = 0.f, x1 = 0.f;
             // T_11 is lower triangular: T_k,j0 and T_k,j0+1 vanish for k < j0
-#pragma unroll 4
-            for (int k = j0; k < 32; ++k) {
-                const float av = At[k * CH + 32 + i];
-                x0 = fmaf(av, Tt[j0 * CH + k], x0);
-                x1 = fmaf(av, Tt[(j0 + 1) * CH + k], x1);
+            // (the terms from j0 rounded down to a multiple of 4 add zeros)
+            for (int k = j0 & ~3; k < 32; k += 4) {
+                const float4 ta = *reinterpret_cast<const float4 *>(Tt + j0 * CH + k);
+                const float4 tb = *reinterpret_cast<const float4 *>(Tt + (j0 + 1) * CH + k);
+                const float a0 = At[k * CH + 32 + i], a1 = At[(k + 1) * CH + 32 + i];
+                const float a2 = At[(k + 2) * CH + 32 + i], a3 = At[(k + 3) * CH + 32 + i];
+                x0 = fmaf(a0, ta.x, x0); x1 = fmaf(a0, tb.x, x1);
+                x0 = fmaf(a1, ta.y, x0); x1 = fmaf(a1, tb.y, x1);
+                x0 = fmaf(a2, ta.z, x0); x1 = fmaf(a2, tb.z, x1);
+                x0 = fmaf(a3, ta.w, x0); x1 = fmaf(a3, tb.w, x1);
             }
             X2t[j0 * 32 + i] = x0;
             X2t[(j0 + 1) * 32 + i] = x1;
             __syncthreads();
             float t0 = 0.f, t1 = 0.f;
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-                const float tv = Tt[(32 + k) * CH + 32 + i];
-                t0 = fmaf(tv, X2t[j0 * 32 + k], t0);
-                t1 = fmaf(tv, X2t[(j0 + 1) * 32 + k], t1);
+#pragma unroll 2
+            for (int k = 0; k < 32; k += 4) {
+                const float4 xa = *reinterpret_cast<const float4 *>(X2t + j0 * 32 + k);
+                const float4 xb = *reinterpret_cast<const float4 *>(X2t + (j0 + 1) * 32 + k);
+                const float v0 = Tt[(32 + k) * CH + 32 + i], v1 = Tt[(33 + k) * CH + 32 + i];
+                const float v2 = Tt[(34 + k) * CH + 32 + i], v3 = Tt[(35 + k) * CH + 32 + i];
+                t0 = fmaf(v0, xa.x, t0); t1 = fmaf(v0, xb.x, t1);
+                t0 = fmaf(v1, xa.y, t0); t1 = fmaf(v1, xb.y, t1);
+                t0 = fmaf(v2, xa.z, t0); t1 = fmaf(v2, xb.z, t1);
+                t0 = fmaf(v3, xa.w, t0); t1 = fmaf(v3, xb.w, t1);
             }
             Tt[j0 * CH + 32 + i] = -t0;
             Tt[(j0 + 1) * CH + 32 + i] = -t1;
