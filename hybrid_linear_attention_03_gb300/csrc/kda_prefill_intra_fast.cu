@@ -306,7 +306,7 @@ __device__ __forceinline__ void solo_tail(const PrefillParams &p, unsigned char 
     if (tid == 0) p.solo[size_t(cm.seq) * p.H + h] = ok ? 1 : 0;
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (warp == 1) tmem_dealloc(tm, 256);
 }
 
 // kSolo: the variant that also finishes one-chunk sequences from a zero
@@ -336,7 +336,16 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     float *X2t = reinterpret_cast<float *>(sm + fs::SCAN + 2048);  // level 2: [32 j][32 i]
     const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const ChunkMeta cm = p.chunks[g];
-    if (cm.len <= 0) return;  // a padding entry of a device-built table: no chunk here
+    // warp 1 takes the tensor memory while the chunk's fields are on their
+    // way (warp 0's lane 0 issues the tile loads as soon as they are here)
+    if (warp == 1) tmem_alloc(tbase, 256);
+    if (cm.len <= 0) {  // a padding entry of a device-built table: no chunk here
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 1) tmem_dealloc(*tbase, 256);
+        return;
+    }
     const SeqMeta sq = p.seqs[cm.seq];
     char *rec = rec_ptr(p, g, h);
     // a one-chunk sequence from a zero state: U = Ut, so this CTA also forms
@@ -359,7 +368,6 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     const float beta_ld = tid < CH && tid < cm.len
                               ? __bfloat162float(static_cast<const __nv_bfloat16 *>(p.beta)[size_t(cm.row0 + tid) * p.H + h])
                               : 0.f;
-    if (warp == 0) tmem_alloc(tbase, 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -434,7 +442,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         mbar_wait(bar_v, 0, p.err);
         tc_fence_before();
         __syncthreads();
-        if (warp == 0) tmem_dealloc(tm, 256);
+        if (warp == 1) tmem_dealloc(tm, 256);
         return;
     }
     float E0[8], E1[8];
@@ -726,7 +734,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         bulk_commit();
         bulk_wait_read();  // shared memory stays until the copies have read it
     }
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (warp == 1) tmem_dealloc(tm, 256);
 }
 
 }  // namespace
