@@ -345,6 +345,14 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
 #pragma unroll
                     for (int e = 0; e < 16; ++e) o[16 * q + e] = v[q][e] + w2[q][e];
             }
+            // sigma of the gate logits first: it needs no reduction, so its
+            // MUFU work overlaps the shuffles below
+            uint16_t *gs = reinterpret_cast<uint16_t *>(sm + (half ? cs::GATE1 : cs::GATE0)) + j;
+            if (kGateTile) ok = mbar_wait(bar_g, par, p.err) && ok;
+            float sg[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                sg[e] = kGateTile ? sigmoid_tanh(bf16_word(gs[e * D])) : sigmoid_fast(gt[kGateTile ? 0 : e]);
             // per token, the sum of O^2 over this warp's 32 channels: a
             // transpose-reduce over the lanes leaves token uc0 + lane's in lane
             float a[32];
@@ -365,17 +373,17 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
             const float ss = (red[uc0 + lane] + red[CH + uc0 + lane]) + (red[2 * CH + uc0 + lane] + red[3 * CH + uc0 + lane]);
             const float rl = rsqrtf(ss * (1.0f / D) + p.eps_rms);
-            Act *op = static_cast<Act *>(p.out) + size_t(cm.row0 + uc0) * HD + size_t(h) * D + j;
-            uint16_t *gs = reinterpret_cast<uint16_t *>(sm + (half ? cs::GATE1 : cs::GATE0)) + j;
-            if (kGateTile) ok = mbar_wait(bar_g, par, p.err) && ok;
-            const bool staged = kGateTile && uc0 + 32 <= cm.len;  // this half leaves by a TMA store
+            if (kGateTile && uc0 + 32 <= cm.len) {  // a full half: staged over its gate tile for a TMA store
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float r = __shfl_sync(0xffffffffu, rl, e);
-                const float gv = kGateTile ? bf16_word(gs[e * D]) : gt[kGateTile ? 0 : e];
-                const float y = wn * (o[e] * r) * (kGateTile ? sigmoid_tanh(gv) : sigmoid_fast(gv));
-                if (staged) gs[e * D] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-                else if (uc0 + e < cm.len) op[size_t(e) * HD] = from_f32<Act>(y);
+                for (int e = 0; e < 32; ++e)
+                    gs[e * D] = __bfloat16_as_ushort(__float2bfloat16_rn(wn * (o[e] * __shfl_sync(0xffffffffu, rl, e)) * sg[e]));
+            } else {
+                Act *op = static_cast<Act *>(p.out) + size_t(cm.row0 + uc0) * HD + size_t(h) * D + j;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float y = wn * (o[e] * __shfl_sync(0xffffffffu, rl, e)) * sg[e];
+                    if (uc0 + e < cm.len) op[size_t(e) * HD] = from_f32<Act>(y);
+                }
             }
         }
         // S^T row j <- gamma . S^T row j + elc . (K^^T U)^T row j; refresh the A1 images
