@@ -70,7 +70,8 @@ constexpr uint32_t BARS = RED + 1024;
 // bf16 gate tile of a chunk (tokens [32 half][128 channels]): half 0 in the
 // record's PP lo slot of B2 (never loaded for bf16 outputs), half 1 here
 constexpr uint32_t GATE0 = PP_LO, GATE1 = (BARS + 512 + 1023) / 1024 * 1024;
-constexpr uint32_t BYTES = GATE1 + 8192;
+constexpr uint32_t RS = GATE1 + 8192;                       // per warp: 1 / rms of its 32 tokens
+constexpr uint32_t BYTES = RS + 1024;
 }  // namespace cs
 static_assert(cs::B2 + Rec::B2_BYTES <= cs::A2_HI, "chain smem map overlaps");
 static_assert(cs::GATE0 + 8192 <= cs::B2 + Rec::B2_BYTES && cs::GATE0 >= cs::B2 + Rec::B2_BYTES_HI &&
@@ -372,16 +373,24 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             // the four warps of this half of the tokens (named barrier 1 + half)
             asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory");
             const float ss = (red[uc0 + lane] + red[CH + uc0 + lane]) + (red[2 * CH + uc0 + lane] + red[3 * CH + uc0 + lane]);
-            const float rl = rsqrtf(ss * (1.0f / D) + p.eps_rms);
+            // token uc0 + lane's 1 / rms, to every lane of the warp through its own slot
+            float *rsw = reinterpret_cast<float *>(sm + cs::RS) + warp * 32;
+            rsw[lane] = rsqrtf(ss * (1.0f / D) + p.eps_rms);
+            __syncwarp();
+            float rv[32];
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 r4 = *reinterpret_cast<const float4 *>(rsw + e);
+                rv[e] = r4.x; rv[e + 1] = r4.y; rv[e + 2] = r4.z; rv[e + 3] = r4.w;
+            }
             if (kGateTile && uc0 + 32 <= cm.len) {  // a full half: staged over its gate tile for a TMA store
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    gs[e * D] = __bfloat16_as_ushort(__float2bfloat16_rn(wn * (o[e] * __shfl_sync(0xffffffffu, rl, e)) * sg[e]));
+                for (int e = 0; e < 32; ++e) gs[e * D] = __bfloat16_as_ushort(__float2bfloat16_rn(wn * (o[e] * rv[e]) * sg[e]));
             } else {
                 Act *op = static_cast<Act *>(p.out) + size_t(cm.row0 + uc0) * HD + size_t(h) * D + j;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float y = wn * (o[e] * __shfl_sync(0xffffffffu, rl, e)) * sg[e];
+                    const float y = wn * (o[e] * rv[e]) * sg[e];
                     if (uc0 + e < cm.len) op[size_t(e) * HD] = from_f32<Act>(y);
                 }
             }
