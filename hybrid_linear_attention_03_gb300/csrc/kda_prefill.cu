@@ -346,14 +346,15 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
 #pragma unroll
                     for (int e = 0; e < 16; ++e) o[16 * q + e] = v[q][e] + w2[q][e];
             }
-            // sigma of the gate logits first: it needs no reduction, so its
-            // MUFU work overlaps the shuffles below
+            // w_n . sigma of the gate logits first: it needs no reduction, so
+            // its MUFU work overlaps the shuffles below
             uint16_t *gs = reinterpret_cast<uint16_t *>(sm + (half ? cs::GATE1 : cs::GATE0)) + j;
             if (kGateTile) ok = mbar_wait(bar_g, par, p.err) && ok;
             float sg[32];
+            const float hwn = 0.5f * wn;
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-                sg[e] = kGateTile ? sigmoid_tanh(bf16_word(gs[e * D])) : sigmoid_fast(gt[kGateTile ? 0 : e]);
+                sg[e] = kGateTile ? scaled_sigmoid_tanh(bf16_word(gs[e * D]), hwn) : wn * sigmoid_fast(gt[kGateTile ? 0 : e]);
             // per token, the sum of O^2 over this warp's 32 channels: a
             // transpose-reduce over the lanes leaves token uc0 + lane's in lane
             float a[32];
@@ -385,12 +386,12 @@ __global__ void __launch_bounds__(256) prefill_chain_kernel(const PrefillParams 
             }
             if (kGateTile && uc0 + 32 <= cm.len) {  // a full half: staged over its gate tile for a TMA store
 #pragma unroll
-                for (int e = 0; e < 32; ++e) gs[e * D] = __bfloat16_as_ushort(__float2bfloat16_rn(wn * (o[e] * rv[e]) * sg[e]));
+                for (int e = 0; e < 32; ++e) gs[e * D] = __bfloat16_as_ushort(__float2bfloat16_rn((o[e] * rv[e]) * sg[e]));
             } else {
                 Act *op = static_cast<Act *>(p.out) + size_t(cm.row0 + uc0) * HD + size_t(h) * D + j;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float y = wn * (o[e] * rv[e]) * sg[e];
+                    const float y = (o[e] * rv[e]) * sg[e];
                     if (uc0 + e < cm.len) op[size_t(e) * HD] = from_f32<Act>(y);
                 }
             }

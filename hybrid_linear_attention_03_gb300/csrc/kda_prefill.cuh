@@ -112,11 +112,13 @@ __device__ __forceinline__ float sigmoid_fast(float x) {
 }
 // sigma(x) = (1 + tanh(x / 2)) / 2 with PTX's approximate tanh (one
 // operation; relative error about 2^-11): for bf16 results only.
-__device__ __forceinline__ float sigmoid_tanh(float x) {
+// w . sigma(x) = hw + hw . tanh(x / 2) with hw = w / 2.
+__device__ __forceinline__ float scaled_sigmoid_tanh(float x, float hw) {
     float t;
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
-    return fmaf(0.5f, t, 0.5f);
+    return fmaf(hw, t, hw);
 }
+__device__ __forceinline__ float sigmoid_tanh(float x) { return scaled_sigmoid_tanh(x, 0.5f); }
 
 // Chunk position of tokens 4c .. 4c + 3 in row j of the record's Ut^T (the
 // XOR spreads the rows a warp writes over all shared-memory banks).

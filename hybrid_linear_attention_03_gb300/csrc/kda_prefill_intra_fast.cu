@@ -363,6 +363,12 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         mbar_arrive_expect_tx(bar_v, fs::TILE);
         tma_load_3d(sm + fs::RV, &tm_v, bar_v, 0, h, cm.row0 - HALO);
     }
+    // the head's conv taps (3 streams x 1 KiB, 24 lines) into L1 now: each
+    // conv pass starts with every warp reading them, and consecutive CTAs on
+    // an SM belong to other heads
+    if (tid >= 64 && tid < 64 + 24)
+        prefetch_l1(static_cast<const __nv_bfloat16 *>(p.conv_w) +
+                    (size_t((tid - 64) >> 3) * p.H * D + size_t(h) * D) * 4 + ((tid - 64) & 7) * 64);
     // beta of the chunk's tokens: loaded now, stored to shared memory after
     // the decay pass (first read by the A drain), so the load is off the setup path
     const float beta_ld = tid < CH && tid < cm.len
