@@ -769,6 +769,7 @@ SideStream *side_stream() {
 // Sequences [lo, hi) whose chunks meet a window (host-built tables).
 struct SeqRange {
     int lo, hi;
+    int32_t row0_base;  // a window inside one sequence: chunk g starts at row row0_base + C g
 };
 
 template <typename Act>
@@ -833,7 +834,8 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
         if (side && w >= L.ring_windows &&
             cudaStreamWaitEvent(stream, side->chain_done[(w - L.ring_windows) % kEventSlots], 0) != cudaSuccess)
             return fail();
-        PrefillParams pw = p;  // this window's fallback list
+        PrefillParams pw = p;  // this window's fallback list and row rule
+        pw.row0_base = ranges ? (*ranges)[size_t(w)].row0_base : kNoRowBase;
         pw.fb_count = p.fb_count + (w & 1);
         pw.fb_list = p.fb_list + size_t(w & 1) * size_t(W) * size_t(p.H);
         if (hi > lo) {
@@ -851,7 +853,7 @@ kda_status launch_act(const PrefillParams &p0, const kda_io *io, int n_tok, int 
         p.win_lo = int(lo);
         p.win_hi = int(hi);
         // the chain of window 0 also settles the sequences that have no chunks
-        const SeqRange rg = (ranges && w > 0) ? (*ranges)[size_t(w)] : SeqRange{0, N};
+        const SeqRange rg = (ranges && w > 0) ? (*ranges)[size_t(w)] : SeqRange{0, N, kNoRowBase};
         if (side) {
             if (cudaEventRecord(side->intra_done[ev], stream) != cudaSuccess ||
                 cudaStreamWaitEvent(cs, side->intra_done[ev], 0) != cudaSuccess)
@@ -894,6 +896,7 @@ kda_status launch_tables(const kda_pool *pool, const kda_weights *w, const kda_i
     p.win_lo = 0;
     p.win_hi = int(n_chunks);
     p.seq_base = 0;
+    p.row0_base = kNoRowBase;
     p.seqs = reinterpret_cast<const SeqMeta *>(ws + L.seqs);
     p.chunks = reinterpret_cast<const ChunkMeta *>(ws + L.chunks);
     p.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.ckpts);
@@ -983,11 +986,16 @@ kda_status launch_prefill(const kda_pool *pool, const kda_weights *w, const kda_
     if (ck != cks.size()) return KDA_ERR_INVALID_ARG;
     // the sequences whose chunks meet each window (their chunks are contiguous)
     const long long n_win = std::max<long long>((n_chunks + window - 1) / window, 1);
-    std::vector<SeqRange> ranges(static_cast<size_t>(n_win), SeqRange{0, 0});
+    std::vector<SeqRange> ranges(static_cast<size_t>(n_win), SeqRange{0, 0, kNoRowBase});
     for (long long wv = 0; wv < n_win; ++wv) {
         const long long lo = wv * window, hi = std::min(n_chunks, lo + window);
         if (hi <= lo) continue;
-        ranges[size_t(wv)] = {chunks[size_t(lo)].seq, chunks[size_t(hi - 1)].seq + 1};
+        const int s0 = chunks[size_t(lo)].seq, s1 = chunks[size_t(hi - 1)].seq;
+        ranges[size_t(wv)] = {s0, s1 + 1, kNoRowBase};
+        if (s0 == s1) {  // chunk g of sequence s starts at row cu_s + C (g - chunk0_s)
+            const long long base = (long long)cu_seqlens[s0] - (long long)CH * seqs[size_t(s0)].chunk0;
+            if (base > kNoRowBase && base <= INT32_MAX) ranges[size_t(wv)].row0_base = int32_t(base);
+        }
     }
     char *ws = static_cast<char *>(workspace);
     {

@@ -89,8 +89,11 @@ struct PrefillParams {
     int32_t win_lo, win_hi;  // chain: global chunk range of this launch
     int32_t seq_base;        // chain: sequence of blockIdx.x / H == 0
     int32_t q_lo;            // the record keeps the lo halves of exp(G) . q and P (fp32 outputs)
+    int32_t row0_base;       // intra: chunk g's first row is row0_base + C g (a window inside one
+                             // sequence, host-built tables), or kNoRowBase
     float eps_l2, eps_rms;
 };
+constexpr int32_t kNoRowBase = -2147483647 - 1;
 
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 // PTX's approximate 2^x and 1/x (flush-to-zero; relative errors of a few

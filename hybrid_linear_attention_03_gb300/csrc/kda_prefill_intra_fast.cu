@@ -335,11 +335,33 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     float *XS = reinterpret_cast<float *>(sm + fs::SCAN);        // level 1: [2][16 j][16 i]
     float *X2t = reinterpret_cast<float *>(sm + fs::SCAN + 2048);  // level 2: [32 j][32 i]
     const int g = p.chunk_base + blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // The tiles: alpha first (the decay pass needs it alone), then q, k, v
+    // with the 3-row conv halo.  Inside one sequence (host-built tables) the
+    // chunk's first row follows from g, so they are requested before the
+    // chunk's fields arrive; otherwise as soon as those are here.
+    auto load_tiles = [&](int row0) {
+        for (int b = 0; b < 5; ++b) mbar_init(bar_a_ld + b, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar_a_ld, uint32_t(CH * D * 2));
+        tma_load_3d(sm + fs::RA, &tm_a, bar_a_ld, 0, h, row0);
+        mbar_arrive_expect_tx(bar_qk, 2 * fs::TILE);
+        tma_load_3d(sm + fs::RK, &tm_k, bar_qk, 0, h, row0 - HALO);
+        tma_load_3d(sm + fs::RQ, &tm_q, bar_qk, 0, h, row0 - HALO);
+        mbar_arrive_expect_tx(bar_v, fs::TILE);
+        tma_load_3d(sm + fs::RV, &tm_v, bar_v, 0, h, row0 - HALO);
+    };
+    const bool row_rule = p.row0_base != kNoRowBase;
+    if (row_rule && tid == 0) load_tiles(p.row0_base + CH * g);
     const ChunkMeta cm = p.chunks[g];
     // warp 1 takes the tensor memory while the chunk's fields are on their
     // way (warp 0's lane 0 issues the tile loads as soon as they are here)
     if (warp == 1) tmem_alloc(tbase, 256);
     if (cm.len <= 0) {  // a padding entry of a device-built table: no chunk here
+        if (row_rule && tid == 0) {  // (host-built tables have none; no copy may land after the CTA is gone)
+            mbar_wait(bar_a_ld, 0, p.err);
+            mbar_wait(bar_qk, 0, p.err);
+            mbar_wait(bar_v, 0, p.err);
+        }
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -352,17 +374,7 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     // O = P U and the end state itself and the chain skips the sequence
     const bool solo = kSolo && sq.n_chunks == 1 && !sq.has_init;
     const uint32_t sbase = smem_u32(sm);
-    if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(bar_a_ld + b, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(bar_a_ld, uint32_t(CH * D * 2));  // alpha first: the decay pass needs it alone
-        tma_load_3d(sm + fs::RA, &tm_a, bar_a_ld, 0, h, cm.row0);
-        mbar_arrive_expect_tx(bar_qk, 2 * fs::TILE);
-        tma_load_3d(sm + fs::RK, &tm_k, bar_qk, 0, h, cm.row0 - HALO);
-        tma_load_3d(sm + fs::RQ, &tm_q, bar_qk, 0, h, cm.row0 - HALO);
-        mbar_arrive_expect_tx(bar_v, fs::TILE);
-        tma_load_3d(sm + fs::RV, &tm_v, bar_v, 0, h, cm.row0 - HALO);
-    }
+    if (!row_rule && tid == 0) load_tiles(cm.row0);
     // the head's conv taps (3 streams x 1 KiB, 24 lines) into L1 now: each
     // conv pass starts with every warp reading them, and consecutive CTAs on
     // an SM belong to other heads
