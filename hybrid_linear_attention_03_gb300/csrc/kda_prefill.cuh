@@ -95,6 +95,11 @@ struct PrefillParams {
 };
 constexpr int32_t kNoRowBase = -2147483647 - 1;
 
+// Brings the cache line holding gsrc into this SM's L1.
+__device__ __forceinline__ void prefetch_l1(const void *gsrc) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(gsrc)) : "memory");
+}
+
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
 // PTX's approximate 2^x and 1/x (flush-to-zero; relative errors of a few
 // 1e-7 and about 1 ulp).

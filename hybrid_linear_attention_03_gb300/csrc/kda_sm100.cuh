@@ -119,11 +119,6 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 
 // Asks the memory system to bring `bytes` (a multiple of 16, 16-byte aligned
 // start) of global memory into L2; completes on its own, nothing to wait for.
-// Brings the cache line holding gsrc into this SM's L1.
-__device__ __forceinline__ void prefetch_l1(const void *gsrc) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(gsrc)) : "memory");
-}
-
 __device__ __forceinline__ void bulk_prefetch_l2(const void *gsrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes)
                  : "memory");
