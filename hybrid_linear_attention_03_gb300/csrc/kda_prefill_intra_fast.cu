@@ -354,7 +354,8 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     if (row_rule && tid == 0) load_tiles(p.row0_base + CH * g);
     const ChunkMeta cm = p.chunks[g];
     // warp 1 takes the tensor memory while the chunk's fields are on their
-    // way (warp 0's lane 0 issues the tile loads as soon as they are here)
+    // way (without a row rule, warp 0's lane 0 issues the tile loads as soon
+    // as they are here)
     if (warp == 1) tmem_alloc(tbase, 256);
     if (cm.len <= 0) {  // a padding entry of a device-built table: no chunk here
         if (row_rule && tid == 0) {  // (host-built tables have none; no copy may land after the CTA is gone)
