@@ -174,6 +174,28 @@ def test_prefill_across_chunk_windows_matches_oracle():
     _check(m, out, ref, [0, 1, 2], reqs)
 
 
+def test_prefill_window_inside_a_sequence_that_starts_mid_batch():
+    """114 chunks in windows of 48: the middle window (chunks 48..95) lies
+    inside sequence 1, which starts at row 100, so each CTA there derives its
+    tile rows from the chunk index (row 100 + 64 (g - 2)) instead of waiting
+    for the chunk table.  Sequence 1 continues a warmed slot, with a
+    checkpoint inside that window; the other two start from zero."""
+    H, act = 2, torch.bfloat16
+    lens = [100, 7000, 70]
+    m = Mirror(16, H, D, act, I.layer_weights(61, H, D, D, 4, act))
+    warm_lens = [0, 40, 0]
+    warm = I.token_inputs(61, 0, sum(warm_lens), H, D, D, 3.0, act)
+    out = prefill_gpu(m, hp.to_device(warm), warm_lens, [0, 1, 2], [0, 0, 0])
+    ref = prefill_oracle(m, warm, warm_lens, [0, 1, 2], [0, 0, 0])
+    _check(m, out, ref, [0, 1, 2])
+    inp = I.token_inputs(61, 1, sum(lens), H, D, D, 3.0, act)
+    reqs = [(0, 100, 8), (1, 3200, 9), (1, 7000, 10), (2, 70, 11)]
+    out = prefill_gpu(m, hp.to_device(inp), lens, [0, 1, 2], [0, 1, 0], reqs)
+    ref = prefill_oracle(m, inp, lens, [0, 1, 2], [0, 1, 0], reqs)
+    _check(m, out, ref, [0, 1, 2], reqs)
+    assert kda.kda_poll_device_error(m.gpu) == (kda.KDA_OK, 0)
+
+
 def test_prefill_results_do_not_depend_on_batch_composition():
     """A sequence prefilled alone and inside a batch (between sequences whose
     lengths put its chunk ends mid-group) gives the same outputs, state and
