@@ -683,14 +683,16 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
     __syncthreads();
     tc_fence_after();
     if (warp == 0 && lane == 0 && ok) {
-        // W diag(exp(-c)) = (T diag beta) K~: A = (T diag beta) read MN-major,
-        // its second 64-row block past the image (those TMEM lanes are not
-        // read); B = K~ read MN-major.  Ut^T = V^T (T diag beta)^T: V and
+        // W diag(exp(-c)) = (T diag beta) K~: A = (T diag beta) read MN-major
+        // with a zero block stride, so its second 64-row block re-reads the
+        // first and TMEM lanes 64..127 hold W again (all 16 warps drain it);
+        // B = K~ read MN-major.  Ut^T = V^T (T diag beta)^T: V and
         // (T diag beta)^T read MN-major.
         const Operand tba{sbase + fs::TB, sbase + fs::TB_LO, true, CH * 128};
+        const Operand tba2{sbase + fs::TB, sbase + fs::TB_LO, true, 0};
         const Operand kt{sbase + fs::X, sbase + fs::X_LO, true, 2 * CH * 128};
         const Operand vt{sbase + fs::VIMG, sbase + fs::VIMG_LO, true, CH * 128};
-        mma_split(tm, tba, kt, CH, idesc_bf16_f32(128, D, true, true), 3, false);
+        mma_split(tm, tba2, kt, CH, idesc_bf16_f32(128, D, true, true), 3, false);
         mma_split(tm + 128, vt, tba, CH, idesc_bf16_f32(128, CH, true, true), 3, false);
         mma_commit(bar_m2);
         if (solo) {  // K^ back from the record into KB (A^T and T^T are done with)
@@ -726,18 +728,17 @@ __global__ void __launch_bounds__(fs::NT, 1) prefill_intra_fast_kernel(const Pre
         bulk_commit();
     }
     // ---- W row r (times exp(c_i)) -> staging in X ---------------------------
-    if (ok && qd < 2) {  // W: TMEM lanes 0..63 = token r, 32 of the 128 key channels per warp
-        const int r = qd * 32 + lane, cw = (warp >> 2) * 32;
-        float w[2][16];
-        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw, w[0]);
-        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw + 16, w[1]);
+    if (ok) {  // W: token r in TMEM lanes r and 64 + r; 16 of the 128 key channels per warp
+        const int r = (qd & 1) * 32 + lane, cw = (warp >> 2) * 32 + (qd >> 1) * 16;
+        float w[16];
+        tmem_ld16(tm + (uint32_t(qd * 32) << 16) + cw, w);
         tmem_wait_ld();
 #pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
+        for (int hh = 0; hh < 2; ++hh) {
             float x[8], e_c[8];
             ld8(ec + cw + 8 * hh, e_c);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = w[hh >> 1][8 * (hh & 1) + e] * e_c[e];
+            for (int e = 0; e < 8; ++e) x[e] = w[8 * hh + e] * e_c[e];
             store_split(sm + fs::X, sm + fs::X + 16384, sw128_chunk(r, (cw >> 3) + hh, CH), x);
         }
     }
